@@ -1,0 +1,405 @@
+"""Benchmark: fused RAG prefill (query-centric KV-cache fusion) vs full prefill on one GB300.
+
+Workload: a Llama-3-8B-shaped random-init bf16 decoder (32 layers, d 4096, 32 Q /
+8 KV heads, head dim 128, FFN 14336, vocab 128256, weights N(0, 0.02)); one
+request of 10 retrieved chunks x 512 tokens + 64 query tokens (uniform ids),
+critical layer 16, 15 % recompute (N = 768), 8 anchors per chunk.  The chunks'
+per-layer K/V are precomputed offline on the GPU, each chunk alone, and kept in
+pinned host memory; every step streams them back layer by layer as the method
+prescribes.
+
+A step is one fused prefill: probe, critical-layer profiling, top-N, 32 layers
+of selective recompute with the next layers' K/V copied on a side stream, LM
+head, first token on the host.  value = context tokens per second = C / step
+time.  e2e repeats the step through the same public API with the token ids
+copied from pinned host memory and the logits and first token copied back.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the path has no exchange step); value = all ranks' context tokens / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import qcfdata as qd  # noqa: E402
+
+METRIC = "fused-prefill context tokens/s + TTFT ms at 15% recompute vs full prefill"
+UNIT = "context tokens/s"
+WORKLOAD = ("llama3-8b-shaped fused RAG prefill: 10 chunks x 512 + 64 query tokens, critical layer 16, "
+            "15% recompute (N=768), 8 anchors/chunk, chunk K/V streamed from pinned host")
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of `value` over the ranks of the default process group (identity at world 1)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs", 6791.0), "bf16": d.get("bf16_tflops", 1900.8),
+                "bf16_sustained": d.get("bf16_tflops_sustained", 1702.3), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- the workload
+
+def build_workload(device, spec=qd.LLAMA8B, req=qd.LLAMA8B_REQ):
+    from rag_kv_cache_re_gb300 import model as M
+    weights = qd.ModelWeights(spec, device=str(device))
+    dm = M.DeviceModel(weights, device, max_pos=8192)
+    del weights
+    torch.cuda.empty_cache()
+    store = M.ChunkStore(dm, req.crit_layer, req.n_anchor)
+    chunk_ids = list(range(req.n_chunks))
+    for c in chunk_ids:   # offline: each chunk prefilled alone at positions 0..511
+        store.ingest(c, qd.chunk_tokens(c, req.chunk_len, spec.vocab))
+    query = qd.query_tokens(0, req.query_len, spec.vocab)
+    fr = M.FusedRequest(dm, store, chunk_ids, query, req.ratio_bp)
+    return dm, store, fr
+
+
+def gemm_flops(spec, n_rows, ffn_padded):
+    d, D = spec.d_model, spec.head_dim
+    return {"gemm_qkv_rope": 2.0 * n_rows * d * (spec.n_heads + 2 * spec.n_kv_heads) * D,
+            "gemm_o_resid": 2.0 * n_rows * spec.n_heads * D * d,
+            "gemm_gate_up_swiglu": 2.0 * n_rows * d * 2 * ffn_padded,
+            "gemm_down_resid": 2.0 * n_rows * ffn_padded * d}
+
+
+def run_gpu(args):
+    from rag_kv_cache_re_gb300 import qcf as Q
+    world, rank, local = _dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    spec, req = qd.LLAMA8B, qd.LLAMA8B_REQ
+    dm, store, fr = build_workload(device)
+    cs, xs = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def step(e2e=False):
+        fr.run(cs, xs, ids_from_host=e2e)
+        if e2e:
+            with torch.cuda.stream(cs):
+                logits_host.copy_(fr.logits, non_blocking=True)
+
+    logits_host = torch.empty(spec.vocab, dtype=torch.float32).pin_memory()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = Q.qcf_query_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    # ---- timed region: K fused prefills, per-kernel event timing on
+    clocks = ClockSampler(device.index)
+    barrier(world, device)
+    torch.cuda.synchronize()
+    clocks.start()
+    Q.qcf_timing_enable(True)
+    launches0 = Q.qcf_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(cs)
+    for _ in range(args.steps):
+        step()
+    ev1.record(cs)
+    torch.cuda.synchronize()
+    launches = Q.qcf_launch_count() - launches0
+    per_kernel = Q.qcf_timing_read()
+    Q.qcf_timing_enable(False)
+    clk = clocks.stop()
+    barrier(world, device)
+    elapsed_ms = reduce_max_over_ranks(ev0.elapsed_time(ev1), world, device)
+    ms_per_step = elapsed_ms / args.steps
+    C = fr.C
+    value = world * C * args.steps / (elapsed_ms / 1e3)
+
+    # ---- e2e: ids from pinned host, logits + first token back to the host, per step
+    torch.cuda.synchronize()
+    barrier(world, device)
+    e0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(e2e=True)
+        cs.synchronize()
+    e_ms = reduce_max_over_ranks((time.perf_counter() - e0) * 1e3, world, device)
+    kv_bytes = sum(c.K.numel() * 2 + c.V.numel() * 2 for c in fr.chunks)
+    anchor_bytes = sum(c.aK[: req.crit_layer].numel() * 2 + c.aV[: req.crit_layer].numel() * 2 for c in fr.chunks)
+    h2d = int(fr.ids_host.numel() * 4 + kv_bytes + anchor_bytes)
+    d2h = int(spec.vocab * 4 + 4)
+
+    # ---- full prefill TTFT on the same tokens (the baseline the ratio compares with)
+    K_layers = [torch.empty((fr.T, spec.n_kv_heads, spec.head_dim), dtype=torch.bfloat16, device=device)
+                for _ in range(spec.n_layers)]
+    V_layers = [torch.empty_like(K_layers[0]) for _ in range(spec.n_layers)]
+    tok_host = torch.zeros(1, dtype=torch.int32).pin_memory()
+    with torch.cuda.stream(cs):
+        for _ in range(2):
+            Q.qcf_full_prefill(dm, fr.ids, K_layers, V_layers, stream=cs)
+    torch.cuda.synchronize()
+    n_full = max(2, min(5, args.steps))
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(cs)
+    with torch.cuda.stream(cs):
+        for _ in range(n_full):
+            _, _, _, tok = Q.qcf_full_prefill(dm, fr.ids, K_layers, V_layers, stream=cs)
+            tok_host.copy_(tok, non_blocking=True)
+    f1.record(cs)
+    torch.cuda.synchronize()
+    full_ms = reduce_max_over_ranks(f0.elapsed_time(f1) / n_full, world, device)
+
+    # ---- roofline of the dominant kernel (gate/up GEMM with SwiGLU epilogue)
+    peaks = load_peaks()
+    flops = gemm_flops(spec, fr.ns, dm.ffn_padded)
+    total_ms = max(1e-9, sum(v[0] for v in per_kernel.values()))
+    kernels = {name: {"ms_total": round(ms, 4), "launches": cnt, "share": round(ms / total_ms, 4)}
+               for name, (ms, cnt) in per_kernel.items() if cnt > 0}
+    # flop counts per step per GEMM class: 32 recompute layers (832 rows) + 16 probe layers (64 rows)
+    probe_flops = gemm_flops(spec, req.query_len, dm.ffn_padded)
+    step_flops = {k: spec.n_layers * flops[k] + req.crit_layer * probe_flops[k] for k in flops}
+    step_flops["gemm_qkv_rope"] += 2.0 * req.query_len * spec.d_model * spec.n_heads * spec.head_dim  # q_crit
+    for k, f in step_flops.items():
+        if k in kernels:
+            ms = kernels[k]["ms_total"] / args.steps
+            kernels[k]["tflops"] = round(f / (ms * 1e-3) / 1e12, 1)
+    gu = kernels.get("gemm_gate_up_swiglu")
+    gu_avg_ms = gu["ms_total"] / gu["launches"] if gu else float("nan")
+    gu_flops_avg = step_flops["gemm_gate_up_swiglu"] / (gu["launches"] / args.steps) if gu else float("nan")
+    achieved = gu_flops_avg / (gu_avg_ms * 1e-3) / 1e12 if gu else None
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
+                "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_sustained"], 4) if achieved else None, "traffic": None,
+                "kernel": "gemm_gate_up_swiglu (tcgen05, fused SwiGLU epilogue)",
+                "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)"}
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights N(0,0.02), uniform token ids)",
+        "config": {"workload": WORKLOAD, "context_tokens": C, "query_tokens": fr.Q, "recomputed_rows": fr.ns,
+                   "l2": "inputs larger than L2: 16 GB of weights and 671 MB of chunk K/V stream through every step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "ttft_ms": round(ms_per_step, 3), "ttft_full_prefill_ms": round(full_ms, 3),
+        "ttft_ratio_fused_over_full": round(ms_per_step / full_ms, 4),
+        "e2e": {"value": round(world * C * args.steps / (e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ttft_ms": round(e_ms / args.steps, 3)},
+        "gpu_launches": int(launches), "clocks": clk, "roofline": roofline, "kernels": kernels,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(dm, fr, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------- the oracle as CPU baseline
+
+def _oracle_sample(weights_src, spec, req, ns, budget_s):
+    """Times the oracle's fused path pieces on the 8B shapes and extrapolates one request.
+
+    Sample: the critical-layer profile + top-N over the C context keys, one probe
+    layer (64 query rows over the 80-anchor prefix) and one or more recompute
+    layers (832 rows over the 5184-row fused cache), within `budget_s`.
+    """
+    from oracle import qcf_oracle as O
+    om = O.OracleModel(weights_src, cache=False)
+    rng = np.random.default_rng(0)
+    C, Qn = req.chunk_len * req.n_chunks, req.query_len
+    T = C + Qn
+    Kc = rng.standard_normal((T, spec.n_kv_heads, spec.head_dim)).astype(np.float32)
+    Vc = rng.standard_normal((T, spec.n_kv_heads, spec.head_dim)).astype(np.float32)
+    q = (rng.standard_normal((Qn, spec.n_heads, spec.head_dim)) / math.sqrt(spec.head_dim)).astype(np.float32)
+    W = om.layer(0)
+    t0 = time.perf_counter()
+    s = O.profile_scores(q, Kc[:C], 1.0 / math.sqrt(spec.head_dim))
+    O.topn_select(s, O.num_selected(C, req.ratio_bp))
+    t_select = time.perf_counter() - t0
+    nA = req.n_chunks * req.n_anchor
+    xp = rng.standard_normal((Qn, spec.d_model)).astype(np.float32)
+    Kp, Vp = Kc[: nA + Qn].copy(), Vc[: nA + Qn].copy()
+    t0 = time.perf_counter()
+    O.layer_forward(xp, W, spec, C + np.arange(Qn), nA + np.arange(Qn), Kp, Vp)
+    t_probe = time.perf_counter() - t0
+    rows = np.concatenate([np.sort(rng.choice(C, ns - Qn, replace=False)), np.arange(C, T)])
+    x = rng.standard_normal((ns, spec.d_model)).astype(np.float32)
+    layers, t_layer = 0, 0.0
+    while layers < 1 or (t_layer + t_probe + t_select < budget_s * 0.6 and layers < 3):
+        t0 = time.perf_counter()
+        O.layer_forward(x, W, spec, rows, rows, Kc, Vc)
+        t_layer += time.perf_counter() - t0
+        layers += 1
+    ttft = t_select + req.crit_layer * t_probe + spec.n_layers * t_layer / layers
+    sample = (f"oracle on the 8B shapes: profile+top-N over {C} keys, 1 probe layer (64 rows), {layers} recompute "
+              f"layer(s) ({ns} rows over {T} cache rows); TTFT extrapolated to 16 probe + 32 recompute layers")
+    return ttft, sample
+
+
+def cpu_baseline(dm, fr, budget_s=20.0):
+    spec, req = qd.LLAMA8B, qd.LLAMA8B_REQ
+
+    class _Src:   # layer 0 of the device model's weights, unpacked, on the host
+        def __init__(self):
+            self.spec = spec
+
+        def layer(self, l):
+            t = dm.layer_tensors[l]
+            Fp, F, d = dm.ffn_padded, spec.ffn, spec.d_model
+            qw, kw = spec.q_width, spec.kv_width
+            gu = t["w_gu"].view(Fp // 64, 2, 64, d)
+            return {"wq": t["w_qkv"][:qw].cpu(), "wk": t["w_qkv"][qw:qw + kw].cpu(),
+                    "wv": t["w_qkv"][qw + kw:].cpu(), "wo": t["w_o"].cpu(),
+                    "wg": gu[:, 0].reshape(Fp, d)[:F].cpu(), "wu": gu[:, 1].reshape(Fp, d)[:F].cpu(),
+                    "wd": t["w_down"][:, :F].cpu(), "g_attn": t["g_attn"].cpu(), "g_mlp": t["g_mlp"].cpu()}
+
+    ttft, sample = _oracle_sample(_Src(), spec, req, fr.ns, budget_s)
+    cores = os.cpu_count()
+    return {"value": round(fr.C / ttft, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+            "ttft_s_extrapolated": round(ttft, 2), "threads": torch.get_num_threads()}
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores, same metric and workload."""
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    spec, req = qd.LLAMA8B, qd.LLAMA8B_REQ
+    weights = qd.ModelWeights(spec)
+
+    class _Layer0:
+        def __init__(self):
+            self.spec = spec
+
+        def layer(self, l):
+            return weights.layer(0)
+
+    ns = qd.LLAMA8B_REQ.query_len + (req.ratio_bp * req.chunk_len * req.n_chunks + 9999) // 10000
+    budget = max(5.0, 60.0 / max(1, args.steps + args.warmup))
+    times, sample = [], ""
+    for i in range(args.warmup + args.steps):
+        ttft, sample = _oracle_sample(_Layer0(), spec, req, ns, budget)
+        if i >= args.warmup:
+            times.append(ttft)
+    ttft = statistics.mean(times)
+    C = req.chunk_len * req.n_chunks
+    v = C / ttft
+    out = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ttft * 1e3, 1), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "context_tokens": C},
+           "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["qcf", "reference"], default="qcf")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,332 @@
+// Location-aware sparse causal attention over the fused KV cache.
+//
+// Recomputed rows arrive sorted by their absolute position.  A CTA takes a block
+// of BR consecutive rows and one KV head g with all G = Hq/Hkv query heads that
+// share it; warp w handles 16 rows of query head g*G + (w % G).  The CTA streams
+// K/V tiles of 64 keys from 0 up to the largest position of its rows (rows are
+// ascending, so that is its last row's position) through a 2-stage TMA ring; each
+// warp skips tiles beyond its own rows and masks keys j > pos inside the
+// boundary tiles.  Q.K^T and P.V run on warp-level tensor cores (m16n8k16, bf16
+// in, fp32 accumulate); the softmax is online in fp32 registers with quad
+// shuffles for the row max.  Blocks are scheduled longest (highest position)
+// first.
+#include <mutex>
+
+#include "qcf_internal.cuh"
+
+namespace qcf {
+
+constexpr int kKeyTile = 64;
+constexpr int kAttnStages = 2;
+
+template <int D>
+struct AttnCfg {
+  static constexpr int TILE_BYTES = kKeyTile * D * 2;  // one of K or V
+  static constexpr int SMEM_BYTES = kAttnStages * 2 * TILE_BYTES + 256 + 1024;
+  static constexpr bool SW128 = D >= 64;
+};
+
+// Byte offset of element (key, col) in a K or V tile; col % 8 == 0.
+template <int D>
+__device__ __forceinline__ uint32_t tile_off(int key, int col) {
+  if constexpr (D >= 64) {
+    return static_cast<uint32_t>((col >> 6) * (kKeyTile * 128)) + sw128_off(key, (col & 63) >> 3);
+  } else {
+    return static_cast<uint32_t>(key * (D * 2) + col * 2);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                          const __grid_constant__ CUtensorMap tmV,
+                                                          const __nv_bfloat16* __restrict__ q,
+                                                          const int32_t* __restrict__ pos, int n, int T, int Hq,
+                                                          int Hkv, int G, int BR, float scale_log2,
+                                                          __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                          unsigned int* status, int check) {
+  using Cfg = AttnCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kAttnStages * 2 * Cfg::TILE_BYTES);
+  uint64_t* empty = full + kAttnStages;
+
+  const int nwarps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_blocks = (n + BR - 1) / BR;
+  const int rb = n_blocks - 1 - static_cast<int>(blockIdx.x);
+  const int g = blockIdx.y;
+  const int row0 = rb * BR;
+  const int row_end = min(n, row0 + BR);
+  const int kmax = pos[row_end - 1];
+  const int n_tiles = kmax / kKeyTile + 1;
+
+  const int hh = warp % G, rg = warp / G;
+  const int h = g * G + hh;
+  const int wrow0 = row0 + rg * 16;
+  const int r_lo = wrow0 + (lane >> 2), r_hi = r_lo + 8;
+  const int p_lo = r_lo < row_end ? pos[r_lo] : -1;
+  const int p_hi = r_hi < row_end ? pos[r_hi] : -1;
+  const int warp_kmax = wrow0 < row_end ? pos[min(row_end, wrow0 + 16) - 1] : -1;
+
+  if (check && threadIdx.x == 0) {
+    for (int r = row0; r < row_end; ++r) {
+      const int p = pos[r];
+      if (p < 0 || p >= T || (r > 0 && pos[r - 1] >= p)) {
+        flag_status(status, QCF_DEV_BAD_INDEX);
+        break;
+      }
+    }
+  }
+
+  // Q fragments (A operand of m16n8k16) straight from global memory.
+  const int qc = (lane & 3) * 2;
+  uint32_t qf[D / 16][4];
+  {
+    const size_t row_stride = static_cast<size_t>(Hq) * D;
+    const __nv_bfloat16* qlo = q + static_cast<size_t>(r_lo) * row_stride + static_cast<size_t>(h) * D;
+    const __nv_bfloat16* qhi = q + static_cast<size_t>(r_hi) * row_stride + static_cast<size_t>(h) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int k = ks * 16 + qc;
+      qf[ks][0] = r_lo < row_end ? *reinterpret_cast<const uint32_t*>(qlo + k) : 0u;
+      qf[ks][1] = r_hi < row_end ? *reinterpret_cast<const uint32_t*>(qhi + k) : 0u;
+      qf[ks][2] = r_lo < row_end ? *reinterpret_cast<const uint32_t*>(qlo + k + 8) : 0u;
+      qf[ks][3] = r_hi < row_end ? *reinterpret_cast<const uint32_t*>(qhi + k + 8) : 0u;
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAttnStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nwarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  constexpr int boxes = D >= 64 ? D / 64 : 1;
+  constexpr int box_cols = D >= 64 ? 64 : D;
+  auto issue = [&](int t) {
+    const int s = t % kAttnStages;
+    uint8_t* kb = smem + s * 2 * Cfg::TILE_BYTES;
+    uint8_t* vb = kb + Cfg::TILE_BYTES;
+    mbar_arrive_expect_tx(&full[s], 2 * Cfg::TILE_BYTES);
+#pragma unroll
+    for (int b = 0; b < boxes; ++b) {
+      tma_load_2d(kb + b * kKeyTile * box_cols * 2, &tmK, &full[s], g * D + b * box_cols, t * kKeyTile);
+      tma_load_2d(vb + b * kKeyTile * box_cols * 2, &tmV, &full[s], g * D + b * box_cols, t * kKeyTile);
+    }
+  };
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    for (int t = 0; t < kAttnStages && t < n_tiles; ++t) issue(t);
+  }
+
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  float oacc[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+
+  bool ok = true;
+  for (int t = 0; t < n_tiles; ++t) {
+    const int s = t % kAttnStages;
+    const uint32_t par = (t / kAttnStages) & 1;
+    if (!mbar_wait(&full[s], par)) {
+      flag_status(status, QCF_DEV_TIMEOUT);
+      ok = false;
+      break;
+    }
+    const int j0 = t * kKeyTile;
+    if (j0 <= warp_kmax) {
+      const uint32_t kaddr = smem_u32(smem + s * 2 * Cfg::TILE_BYTES);
+      const uint32_t vaddr = kaddr + Cfg::TILE_BYTES;
+      float sc[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+      const int mi = lane >> 3, mr = lane & 7;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kaddr + tile_off<D>(np * 16 + (mi >> 1) * 8 + mr, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
+          mma_bf16_16816(sc[2 * np], qf[ks], b0, b1);
+          mma_bf16_16816(sc[2 * np + 1], qf[ks], b2, b3);
+        }
+      }
+      // scale into log2 units, causal mask by true position, online softmax
+      float tmax_lo = -INFINITY, tmax_hi = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = j0 + nt * 8 + qc + (e & 1);
+          const int p = e < 2 ? p_lo : p_hi;
+          const float x = key <= p ? sc[nt][e] * scale_log2 : -INFINITY;
+          sc[nt][e] = x;
+          if (e < 2) tmax_lo = fmaxf(tmax_lo, x); else tmax_hi = fmaxf(tmax_hi, x);
+        }
+      }
+      tmax_lo = fmaxf(tmax_lo, __shfl_xor_sync(0xffffffffu, tmax_lo, 1));
+      tmax_lo = fmaxf(tmax_lo, __shfl_xor_sync(0xffffffffu, tmax_lo, 2));
+      tmax_hi = fmaxf(tmax_hi, __shfl_xor_sync(0xffffffffu, tmax_hi, 1));
+      tmax_hi = fmaxf(tmax_hi, __shfl_xor_sync(0xffffffffu, tmax_hi, 2));
+      const float mn_lo = fmaxf(m_lo, tmax_lo), mn_hi = fmaxf(m_hi, tmax_hi);
+      const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+      const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+      const float alpha_lo = exp2f(m_lo - base_lo), alpha_hi = exp2f(m_hi - base_hi);
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      float rs_lo = 0.f, rs_hi = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        sc[nt][0] = exp2f(sc[nt][0] - base_lo);
+        sc[nt][1] = exp2f(sc[nt][1] - base_lo);
+        sc[nt][2] = exp2f(sc[nt][2] - base_hi);
+        sc[nt][3] = exp2f(sc[nt][3] - base_hi);
+        rs_lo += sc[nt][0] + sc[nt][1];
+        rs_hi += sc[nt][2] + sc[nt][3];
+      }
+      l_lo = l_lo * alpha_lo + rs_lo;
+      l_hi = l_hi * alpha_hi + rs_hi;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        oacc[i][0] *= alpha_lo;
+        oacc[i][1] *= alpha_lo;
+        oacc[i][2] *= alpha_hi;
+        oacc[i][3] *= alpha_hi;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
+        pa[1] = pack_bf16x2(sc[2 * kk][2], sc[2 * kk][3]);
+        pa[2] = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+        pa[3] = pack_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vaddr + tile_off<D>(kk * 16 + (mi & 1) * 8 + mr, dp * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
+          mma_bf16_16816(oacc[2 * dp], pa, b0, b1);
+          mma_bf16_16816(oacc[2 * dp + 1], pa, b2, b3);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (warp == 0) {
+      if (lane == 0 && t + kAttnStages < n_tiles) {
+        if (!mbar_wait(&empty[s], par)) {
+          flag_status(status, QCF_DEV_TIMEOUT);
+          ok = false;
+        } else {
+          issue(t + kAttnStages);
+        }
+      }
+      __syncwarp();   // reconverge warp 0 before its next warp-wide MMA
+    }
+    if (!ok) break;
+  }
+  // On a timeout every warp gives up at its next wait (nothing more is issued);
+  // the CTA then exits without writing.  No barrier follows, so warps that
+  // finished normally cannot be stranded.
+  if (!ok) return;
+
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
+  const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
+  const size_t ostride = static_cast<size_t>(Hq) * D;
+  if (r_lo < row_end) {
+    __nv_bfloat16* op = o + static_cast<size_t>(r_lo) * ostride + static_cast<size_t>(h) * D;
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt)
+      *reinterpret_cast<uint32_t*>(op + dt * 8 + qc) = pack_bf16x2(oacc[dt][0] * inv_lo, oacc[dt][1] * inv_lo);
+    if (lse && (lane & 3) == 0) lse[static_cast<size_t>(r_lo) * Hq + h] = (m_lo + log2f(l_lo)) * 0.69314718055994531f;
+  }
+  if (r_hi < row_end) {
+    __nv_bfloat16* op = o + static_cast<size_t>(r_hi) * ostride + static_cast<size_t>(h) * D;
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt)
+      *reinterpret_cast<uint32_t*>(op + dt * 8 + qc) = pack_bf16x2(oacc[dt][2] * inv_hi, oacc[dt][3] * inv_hi);
+    if (lse && (lane & 3) == 0) lse[static_cast<size_t>(r_hi) * Hq + h] = (m_hi + log2f(l_hi)) * 0.69314718055994531f;
+  }
+}
+
+size_t attn_workspace_size(int, int, int, int, int) { return 0; }
+
+template <int D>
+static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,
+                                const __nv_bfloat16* V, int T, int Hq, int Hkv, float scale, __nv_bfloat16* o,
+                                float* lse, cudaStream_t st) {
+  using Cfg = AttnCfg<D>;
+  const int G = Hq / Hkv;
+  const int BR = 16 * (G >= 8 ? 1 : 8 / G);
+  const int warps = G * (BR / 16);
+  CUtensorMap tk, tv;
+  const uint64_t width = static_cast<uint64_t>(Hkv) * D;
+  const uint32_t box_cols = D >= 64 ? 64 : D;
+  const CUtensorMapSwizzle sw = Cfg::SW128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!encode_tmap_2d(&tk, K, width, T, width * 2, box_cols, kKeyTile, sw) ||
+      !encode_tmap_2d(&tv, V, width, T, width * 2, box_cols, kKeyTile, sw))
+    return set_error(QCF_ERR_CUDA, "sparse_causal_attn: tensor map encoding failed");
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  });
+  if (attr != cudaSuccess) return cuda_error(attr, "sparse_causal_attn: smem attribute");
+  dim3 grid((n + BR - 1) / BR, Hkv);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  LaunchScope ls(KC_ATTN, st);
+  sparse_attn_kernel<D><<<grid, warps * 32, Cfg::SMEM_BYTES, st>>>(tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o,
+                                                                    lse, device_status_ptr(), check_enabled() ? 1 : 0);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? QCF_OK : cuda_error(e, "sparse_causal_attn: launch");
+}
+
+qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K, const __nv_bfloat16* V,
+                       int T, int Hq, int Hkv, int D, float scale, __nv_bfloat16* o, float* lse, void* ws,
+                       size_t ws_bytes, cudaStream_t st) {
+  (void)ws;
+  (void)ws_bytes;
+  if (n <= 0) return QCF_OK;
+  switch (D) {
+    case 16: return attn_launch_d<16>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, st);
+    case 64: return attn_launch_d<64>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, st);
+    case 128: return attn_launch_d<128>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, st);
+    default: return set_error(QCF_ERR_SHAPE, "sparse_causal_attn: head dim %d unsupported", D);
+  }
+}
+
+}  // namespace qcf
+
+using namespace qcf;
+
+extern "C" {
+
+size_t qcf_sparse_causal_attn_workspace_size(int n, int T, int Hq, int Hkv, int D) {
+  return attn_workspace_size(n, T, Hq, Hkv, D);
+}
+
+qcf_status qcf_sparse_causal_attn(const qcf_bf16* q, const int32_t* pos, int n, const qcf_bf16* K, const qcf_bf16* V,
+                                  int T, int Hq, int Hkv, int D, float scale, qcf_bf16* o, float* lse, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  if (!q || !pos || !K || !V || !o) return set_error(QCF_ERR_INVALID_ARG, "qcf_sparse_causal_attn: NULL pointer");
+  if (n < 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hq / Hkv > 8 || (D != 16 && D != 64 && D != 128))
+    return set_error(QCF_ERR_SHAPE, "qcf_sparse_causal_attn: n=%d T=%d Hq=%d Hkv=%d D=%d", n, T, Hq, Hkv, D);
+  if (take_fault(4) || !aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(o))
+    return set_error(QCF_ERR_ALIGN, "qcf_sparse_causal_attn: pointers must be 16-byte aligned");
+  if (take_fault(1)) return set_error(QCF_ERR_INVALID_ARG, "qcf_sparse_causal_attn: injected invalid index table");
+  if (ws_bytes < qcf_sparse_causal_attn_workspace_size(n, T, Hq, Hkv, D))
+    return set_error(QCF_ERR_WORKSPACE, "qcf_sparse_causal_attn: workspace too small");
+  return attn_launch(reinterpret_cast<const __nv_bfloat16*>(q), pos, n, reinterpret_cast<const __nv_bfloat16*>(K),
+                     reinterpret_cast<const __nv_bfloat16*>(V), T, Hq, Hkv, D, scale,
+                     reinterpret_cast<__nv_bfloat16*>(o), lse, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

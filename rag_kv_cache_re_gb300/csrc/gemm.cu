@@ -1,0 +1,592 @@
+// Dense GEMM on 5th-generation tensor cores: out = A * W^T with A [M][K] and
+// W [N][K] bf16 (both K-major), fp32 accumulators in tensor memory (TMEM).
+//
+// Persistent, warp-specialised CTA of 6 warps, one CTA per SM:
+//   warp 0   TMA producer: 128x64 A tile and BNx64 W tile per stage (128-byte swizzle)
+//   warp 1   TMEM allocator and single-thread tcgen05.mma issuer (M=128, N=BN, K=16 steps)
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (one row per thread), fused op, store
+// The accumulator is double-buffered in TMEM so the epilogue of one tile overlaps
+// the main loop of the next.  Work units are (m tile, n tile, k split); consecutive
+// units walk the m tiles of one weight tile so concurrently running CTAs share it
+// through L2.  With k splits > 1 every unit writes an fp32 partial to the
+// workspace and the last unit of a tile (counted with an atomic) sums the
+// partials in split order -- deterministic -- and runs the epilogue.
+//
+// Fused epilogues:
+//   STORE_BF16  out[m][n] = acc
+//   ADD_F32     out[m][n] += acc                      (residual stream, fp32)
+//   QKV_ROPE    columns are [q heads | k heads | v heads] of width D: q and k are
+//               rotated by RoPE at rope_pos[m]; q goes to q_out[m], k/v are written
+//               into the cache at row cache_row[m]
+//   SWIGLU      W rows come in blocks of 64 gate rows then 64 up rows;
+//               out[m][f] = silu(gate) * up
+#include <mutex>
+
+#include "qcf_internal.cuh"
+
+namespace qcf {
+
+constexpr int kBM = 128, kBK = 64;
+constexpr int kGemmThreads = 192;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier over the 4 epilogue warps that also ORs a predicate across them.
+__device__ __forceinline__ int epi_bar_or(int v) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n barrier.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"(v)
+      : "memory");
+  return static_cast<int>(out);
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    d[i] = u;
+  }
+}
+
+// Loads 32 accumulator columns [32c, 32c+32) of this thread's row, either from
+// TMEM (direct) or as the in-order sum of the split-K partials in the workspace.
+struct ChunkLoader {
+  uint32_t taddr;       // TMEM address of (row quarter, column 0) of the accumulator
+  const float* part;    // first partial of this tile's row, or nullptr for TMEM
+  int splits;
+  int part_stride;      // floats between consecutive splits' partials
+  __device__ __forceinline__ void operator()(int c, float* v) const {
+    if (part == nullptr) {
+      tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(part + c * 32 + i));
+        v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+      }
+      for (int s = 1; s < splits; ++s) {
+        const float* p = part + static_cast<size_t>(s) * part_stride;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(p + c * 32 + i));
+          v[i] += t.x; v[i + 1] += t.y; v[i + 2] += t.z; v[i + 3] += t.w;
+        }
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ void rope_pair32(float* lo, float* hi, const float* cs, const float* sn) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float a = lo[i], b = hi[i];
+    lo[i] = a * cs[i] - b * sn[i];
+    hi[i] = b * cs[i] + a * sn[i];
+  }
+}
+
+__device__ __forceinline__ void load_f32x(const float* src, float* v, int n) {
+  for (int i = 0; i < n; i += 4) {
+    const float4 t = *reinterpret_cast<const float4*>(src + i);
+    v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+  }
+}
+
+// Epilogue of one tile for the calling thread's row.  `row` < M is checked here.
+template <int BN, int EPI, int HD>
+__device__ __forceinline__ void tile_epilogue(const ChunkLoader& ld, const EpiParams& ep, int row, int M, int n0) {
+  const bool live = row < M;
+  if constexpr (EPI == EPI_STORE_BF16) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ep.out);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      ld(c, v);
+      if (live) store_bf16x32(out + static_cast<size_t>(row) * ep.ldo + n0 + c * 32, v);
+    }
+  } else if constexpr (EPI == EPI_ADD_F32) {
+    float* out = static_cast<float*>(ep.out);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      ld(c, v);
+      if (live) {
+        float4* o = reinterpret_cast<float4*>(out + static_cast<size_t>(row) * ep.ldo + n0 + c * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 t = o[i];
+          t.x += v[4 * i]; t.y += v[4 * i + 1]; t.z += v[4 * i + 2]; t.w += v[4 * i + 3];
+          o[i] = t;
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ep.out);
+    const int f0 = n0 / 2;
+#pragma unroll 1
+    for (int blk = 0; blk < BN / 128; ++blk) {
+#pragma unroll 1
+      for (int j = 0; j < 2; ++j) {
+        float g[32], u[32];
+        ld(blk * 4 + j, g);
+        ld(blk * 4 + 2 + j, u);
+        if (live) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+          store_bf16x32(out + static_cast<size_t>(row) * ep.ldo + f0 + blk * 64 + j * 32, g);
+        }
+      }
+    }
+  } else {  // EPI_QKV_ROPE
+    static_assert(HD == 16 || HD == 64 || HD == 128, "head dim");
+    static_assert(BN % HD == 0, "tile must hold whole heads");
+    const int qw = ep.Hq * HD, kw = ep.Hkv * HD;
+    int p = 0, crow = 0;
+    bool kv_ok = true;
+    if (live) {
+      p = ep.rope_pos[row];
+      crow = ep.cache_row ? ep.cache_row[row] : 0;
+      if (static_cast<unsigned>(p) >= static_cast<unsigned>(ep.max_pos)) {
+        flag_status(ep.status, QCF_DEV_BAD_INDEX);
+        p = 0;
+      }
+      if (static_cast<unsigned>(crow) >= static_cast<unsigned>(ep.T)) {
+        flag_status(ep.status, QCF_DEV_BAD_INDEX);
+        kv_ok = false;
+      }
+    }
+    const float* cs_row = ep.cos_t + static_cast<size_t>(p) * (HD / 2);
+    const float* sn_row = ep.sin_t + static_cast<size_t>(p) * (HD / 2);
+#pragma unroll 1
+    for (int h = 0; h < BN / HD; ++h) {
+      const int col = n0 + h * HD;  // first global column of this head
+      __nv_bfloat16* dst = nullptr;
+      bool rotate = true;
+      const bool dst_is_q = col < qw;
+      if (col < qw) {
+        dst = ep.q_out + static_cast<size_t>(row) * qw + col;
+      } else if (col < qw + kw) {
+        dst = ep.k_cache + static_cast<size_t>(crow) * kw + (col - qw);
+      } else {
+        dst = ep.v_cache + static_cast<size_t>(crow) * kw + (col - qw - kw);
+        rotate = false;
+      }
+      if constexpr (HD >= 64) {
+        constexpr int dist = HD / 64;  // chunks between element k and k + D/2
+#pragma unroll 1
+        for (int j = 0; j < dist; ++j) {
+          float lo[32], hi[32];
+          const int c_lo = h * (HD / 32) + j;
+          ld(c_lo, lo);
+          ld(c_lo + dist, hi);
+          if (live && (dst_is_q || kv_ok)) {
+            if (rotate) {
+              float cs[32], sn[32];
+              load_f32x(cs_row + j * 32, cs, 32);
+              load_f32x(sn_row + j * 32, sn, 32);
+              rope_pair32(lo, hi, cs, sn);
+            }
+            store_bf16x32(dst + j * 32, lo);
+            store_bf16x32(dst + HD / 2 + j * 32, hi);
+          }
+        }
+      } else {  // HD == 16: one chunk holds two heads; handle them when h is even
+        if (h & 1) continue;
+        float v[32];
+        ld(h / 2, v);
+        if (live) {
+          float cs[8], sn[8];
+          load_f32x(cs_row, cs, 8);
+          load_f32x(sn_row, sn, 8);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int colh = col + hh * 16;
+            if (colh >= qw && !kv_ok) continue;
+            bool rot = true;
+            __nv_bfloat16* d2;
+            if (colh < qw) {
+              d2 = ep.q_out + static_cast<size_t>(row) * qw + colh;
+            } else if (colh < qw + kw) {
+              d2 = ep.k_cache + static_cast<size_t>(crow) * kw + (colh - qw);
+            } else {
+              d2 = ep.v_cache + static_cast<size_t>(crow) * kw + (colh - qw - kw);
+              rot = false;
+            }
+            float o[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float a = v[hh * 16 + i], b = v[hh * 16 + 8 + i];
+              o[i] = rot ? a * cs[i] - b * sn[i] : a;
+              o[8 + i] = rot ? b * cs[i] + a * sn[i] : b;
+            }
+            uint4* dd = reinterpret_cast<uint4*>(d2);
+            uint4 u0, u1;
+            u0.x = pack_bf16x2(o[0], o[1]); u0.y = pack_bf16x2(o[2], o[3]);
+            u0.z = pack_bf16x2(o[4], o[5]); u0.w = pack_bf16x2(o[6], o[7]);
+            u1.x = pack_bf16x2(o[8], o[9]); u1.y = pack_bf16x2(o[10], o[11]);
+            u1.z = pack_bf16x2(o[12], o[13]); u1.w = pack_bf16x2(o[14], o[15]);
+            dd[0] = u0;
+            dd[1] = u1;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int BN, int EPI, int HD>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
+                        int N, int K, int splits, const EpiParams ep, float* __restrict__ ws_part,
+                        unsigned int* __restrict__ ws_cnt, unsigned int* status) {
+  using Cfg = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+  uint64_t* empty = full + Cfg::STAGES;
+  uint64_t* tfull = empty + Cfg::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = (M + kBM - 1) / kBM;
+  const int tiles_n = N / BN;
+  const int kb_total = K / kBK;
+  const int units = tiles_m * tiles_n * splits;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto decode = [&](int u, int& mt, int& nt, int& sp) {
+    mt = u % tiles_m;
+    const int r = u / tiles_m;
+    sp = r % splits;
+    nt = r / splits;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        int mt, nt, sp;
+        decode(u, mt, nt, sp);
+        const int kb0 = static_cast<int>(static_cast<long long>(kb_total) * sp / splits);
+        const int kb1 = static_cast<int>(static_cast<long long>(kb_total) * (sp + 1) / splits);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+            flag_status(status, QCF_DEV_TIMEOUT);
+            ok = false;
+            break;
+          }
+          uint8_t* a_s = smem + stage * Cfg::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+          tma_load_2d(a_s, &tmA, &full[stage], kb * kBK, mt * kBM);
+          tma_load_2d(a_s + Cfg::A_BYTES, &tmB, &full[stage], kb * kBK, nt * BN);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+        int mt, nt, sp;
+        decode(u, mt, nt, sp);
+        const int kb0 = static_cast<int>(static_cast<long long>(kb_total) * sp / splits);
+        const int kb1 = static_cast<int>(static_cast<long long>(kb_total) * (sp + 1) / splits);
+        const int acc = local & 1;
+        if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1u)) {
+          flag_status(status, QCF_DEV_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            flag_status(status, QCF_DEV_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + Cfg::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            umma_f16(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                     (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int local = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+      int mt, nt, sp;
+      decode(u, mt, nt, sp);
+      const int acc = local & 1;
+      const bool got = mbar_wait(&tfull[acc], (local >> 1) & 1);
+      if (!got) flag_status(status, QCF_DEV_TIMEOUT);
+      if (splits > 1) {
+        // the split-K path has epilogue-wide barriers: abort only together
+        if (epi_bar_or(!got)) break;
+      } else if (!got) {
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
+      const int row = mt * kBM + row_in_tile;
+      const int n0 = nt * BN;
+      if (splits == 1) {
+        ChunkLoader ld{taddr, nullptr, 1, 0};
+        tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else {
+        const int tile = nt * tiles_m + mt;
+        const int stride = kBM * BN;
+        float* mine = ws_part + (static_cast<size_t>(tile) * splits + sp) * stride + static_cast<size_t>(row_in_tile) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
+          float4* d = reinterpret_cast<float4*>(mine + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        __threadfence();
+        epi_bar();
+        if (threadIdx.x == 64) {
+          const unsigned int prev = atomicAdd(&ws_cnt[tile], 1u);
+          const int last = prev == static_cast<unsigned int>(splits - 1);
+          if (last) ws_cnt[tile] = 0u;
+          *s_last = last;
+        }
+        epi_bar();
+        const int last = *s_last;
+        epi_bar();
+        if (last) {
+          __threadfence();
+          ChunkLoader ld{0u, ws_part + static_cast<size_t>(tile) * splits * stride + static_cast<size_t>(row_in_tile) * BN,
+                         splits, stride};
+          tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+struct GemmPlan {
+  int BN;
+  int splits;
+  int tiles;
+};
+
+static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
+  const int sms = num_sms();
+  const int tiles_m = (M + kBM - 1) / kBM;
+  const int kb = K / kBK;
+  GemmPlan best{64, 1, tiles_m * (N / 64)};
+  double best_score = -1.0;
+  const int cands[3] = {256, 128, 64};
+  for (int bn : cands) {
+    if (N % bn) continue;
+    if (epi == EPI_SWIGLU && bn % 128) continue;
+    if (epi == EPI_QKV_ROPE && bn % head_dim) continue;
+    const int tiles = tiles_m * (N / bn);
+    for (int s = 1; s <= 4; ++s) {
+      if (s > 1 && kb / s < 16) break;
+      const int units = tiles * s;
+      const int waves = (units + sms - 1) / sms;
+      const double eff = static_cast<double>(units) / (static_cast<double>(waves) * sms);
+      const double bn_factor = bn == 256 ? 1.0 : (bn == 128 ? 0.9 : 0.75);
+      const double split_factor = s == 1 ? 1.0 : 0.93;
+      const double score = eff * bn_factor * split_factor;
+      if (score > best_score + 1e-9) {
+        best_score = score;
+        best = GemmPlan{bn, s, tiles};
+      }
+    }
+  }
+  return best;
+}
+
+size_t gemm_workspace_size(int M, int N, int K) {
+  // the largest requirement over every epilogue's plan
+  size_t need = 0;
+  const EpiKind kinds[4] = {EPI_STORE_BF16, EPI_ADD_F32, EPI_QKV_ROPE, EPI_SWIGLU};
+  for (EpiKind e : kinds) {
+    for (int hd : {16, 64, 128}) {
+      if (e != EPI_QKV_ROPE && hd != 16) continue;
+      if (M <= 0 || N <= 0 || K <= 0 || N % 64 || K % 64) continue;
+      GemmPlan p = plan_gemm(M, N, K, e, hd);
+      if (p.splits > 1) {
+        const size_t b = align_up(static_cast<size_t>(p.tiles) * p.splits * kBM * p.BN * sizeof(float), 256) +
+                         align_up(static_cast<size_t>(p.tiles) * sizeof(unsigned int), 256);
+        need = b > need ? b : need;
+      }
+    }
+  }
+  return need + 256;
+}
+
+template <int BN, int EPI, int HD>
+static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int splits,
+                             const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st, int units) {
+  using Cfg = GemmCfg<BN>;
+  auto kern = gemm_tcgen05_kernel<BN, EPI, HD>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return cuda_error(attr_err, "gemm: shared memory attribute");
+  const int grid = units < num_sms() ? units : num_sms();
+  kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, st>>>(ta, tb, M, N, K, splits, ep, part, cnt, device_status_ptr());
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? QCF_OK : cuda_error(e, "gemm: launch");
+}
+
+template <int BN>
+static qcf_status dispatch_epi(EpiKind epi, int hd, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+                               int splits, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
+                               int units) {
+  switch (epi) {
+    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+    case EPI_ADD_F32: return launch_cfg<BN, EPI_ADD_F32, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+    case EPI_SWIGLU:
+      if constexpr (BN >= 128) return launch_cfg<BN, EPI_SWIGLU, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+      break;
+    case EPI_QKV_ROPE:
+      if (hd == 16) return launch_cfg<BN, EPI_QKV_ROPE, 16>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+      if (hd == 64) return launch_cfg<BN, EPI_QKV_ROPE, 64>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+      if constexpr (BN >= 128)
+        if (hd == 128) return launch_cfg<BN, EPI_QKV_ROPE, 128>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+      break;
+  }
+  return set_error(QCF_ERR_UNSUPPORTED, "gemm: no kernel for epilogue %d, BN %d, head dim %d", epi, BN, hd);
+}
+
+qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const __nv_bfloat16* W, int N,
+                       const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc) {
+  if (M <= 0) return QCF_OK;
+  if (K % kBK || N % 64 || K <= 0 || N <= 0) return set_error(QCF_ERR_SHAPE, "gemm: K=%d N=%d (K%%64, N%%64 required)", K, N);
+  const int hd = epi == EPI_QKV_ROPE ? ep.D : 16;
+  GemmPlan p = plan_gemm(M, N, K, epi, hd);
+  float* part = nullptr;
+  unsigned int* cnt = nullptr;
+  if (p.splits > 1) {
+    const size_t pb = align_up(static_cast<size_t>(p.tiles) * p.splits * kBM * p.BN * sizeof(float), 256);
+    const size_t cb = align_up(static_cast<size_t>(p.tiles) * sizeof(unsigned int), 256);
+    if (!ws || ws_bytes < pb + cb) return set_error(QCF_ERR_WORKSPACE, "gemm: workspace %zu < %zu", ws_bytes, pb + cb);
+    part = static_cast<float*>(ws);
+    cnt = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + pb);
+    cudaError_t e = cudaMemsetAsync(cnt, 0, p.tiles * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return cuda_error(e, "gemm: counter reset");
+  }
+  CUtensorMap ta, tb;
+  if (!encode_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tb, W, K, N, static_cast<uint64_t>(K) * 2, kBK, p.BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return set_error(QCF_ERR_CUDA, "gemm: tensor map encoding failed");
+  const int units = p.tiles * p.splits;
+  LaunchScope ls(kc, st);
+  switch (p.BN) {
+    case 256: return dispatch_epi<256>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
+    case 128: return dispatch_epi<128>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
+    default: return dispatch_epi<64>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
+  }
+}
+
+}  // namespace qcf
+
+using namespace qcf;
+
+extern "C" {
+
+size_t qcf_linear_workspace_size(int M, int N, int K) { return gemm_workspace_size(M, N, K); }
+
+qcf_status qcf_linear(const qcf_bf16* A, int M, int K, const qcf_bf16* W, int N, int epilogue, void* out, void* ws,
+                      size_t ws_bytes, void* stream) {
+  if (!A || !W || !out) return set_error(QCF_ERR_INVALID_ARG, "qcf_linear: NULL pointer");
+  if (epilogue != QCF_EPI_STORE_BF16 && epilogue != QCF_EPI_ADD_F32)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_linear: unknown epilogue %d", epilogue);
+  if (M < 0 || K <= 0 || N <= 0 || K % 64 || N % 64)
+    return set_error(QCF_ERR_SHAPE, "qcf_linear: M=%d K=%d N=%d (K, N multiples of 64)", M, K, N);
+  if (take_fault(4) || !aligned16(A) || !aligned16(W) || !aligned16(out))
+    return set_error(QCF_ERR_ALIGN, "qcf_linear: pointers must be 16-byte aligned");
+  if (take_fault(2)) return set_error(QCF_ERR_WORKSPACE, "qcf_linear: injected short workspace");
+  EpiParams ep{};
+  ep.out = out;
+  ep.ldo = N;
+  return gemm_launch(epilogue == QCF_EPI_STORE_BF16 ? EPI_STORE_BF16 : EPI_ADD_F32,
+                     reinterpret_cast<const __nv_bfloat16*>(A), M, K, reinterpret_cast<const __nv_bfloat16*>(W), N, ep,
+                     ws, ws_bytes, static_cast<cudaStream_t>(stream), KC_GEMM_OTHER);
+}
+
+}  // extern "C"

@@ -1,0 +1,558 @@
+// Decoder layer forward for recomputed rows, full prefill, and the per-request
+// fused-prefill driver (probe -> profile -> top-N -> pipelined per-layer recompute).
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "qcf_internal.cuh"
+
+namespace qcf {
+
+// ------------------------------------------------------------------ workspace carving
+
+struct Carve {
+  uint8_t* base;
+  size_t cap;
+  size_t used = 0;
+  bool ok = true;
+  template <typename T>
+  T* take(size_t count) {
+    const size_t off = align_up(used, 256);
+    const size_t bytes = align_up(count * sizeof(T), 256);
+    used = off + bytes;
+    if (!base || used > cap) {
+      ok = false;
+      return nullptr;
+    }
+    return reinterpret_cast<T*>(base + off);
+  }
+};
+
+static size_t gemm_ws_layer(const qcf_dims& d, int n) {
+  const int D = d.head_dim;
+  size_t w = gemm_workspace_size(n, (d.n_heads + 2 * d.n_kv_heads) * D, d.d_model);
+  w = std::max(w, gemm_workspace_size(n, d.d_model, d.n_heads * D));
+  w = std::max(w, gemm_workspace_size(n, 2 * d.ffn_padded, d.d_model));
+  w = std::max(w, gemm_workspace_size(n, d.d_model, d.ffn_padded));
+  return w;
+}
+
+struct LayerBufs {
+  __nv_bfloat16* h;
+  __nv_bfloat16* q;
+  __nv_bfloat16* o;
+  __nv_bfloat16* act;
+  void* gemm_ws;
+  size_t gemm_ws_bytes;
+};
+
+static size_t layer_ws_bytes(const qcf_dims& d, int n, int T) {
+  Carve c{nullptr, 0};
+  c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.d_model);
+  c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.n_heads * d.head_dim);
+  c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.n_heads * d.head_dim);
+  c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.ffn_padded);
+  c.take<uint8_t>(gemm_ws_layer(d, n));
+  c.take<uint8_t>(attn_workspace_size(n, T, d.n_heads, d.n_kv_heads, d.head_dim));
+  return c.used;
+}
+
+static bool carve_layer(Carve& c, const qcf_dims& d, int n, int T, LayerBufs* b) {
+  b->h = c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.d_model);
+  b->q = c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.n_heads * d.head_dim);
+  b->o = c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.n_heads * d.head_dim);
+  b->act = c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.ffn_padded);
+  b->gemm_ws_bytes = gemm_ws_layer(d, n);
+  b->gemm_ws = c.take<uint8_t>(b->gemm_ws_bytes);
+  c.take<uint8_t>(attn_workspace_size(n, T, d.n_heads, d.n_kv_heads, d.head_dim));
+  return c.ok;
+}
+
+static qcf_status check_dims(const qcf_dims& d, const char* who) {
+  const int D = d.head_dim;
+  if (d.n_layers <= 0 || d.d_model <= 0 || d.n_heads <= 0 || d.n_kv_heads <= 0 || d.n_heads % d.n_kv_heads ||
+      d.n_heads / d.n_kv_heads > 8 || (D != 16 && D != 64 && D != 128) || d.d_model % 64 || (d.n_heads * D) % 64 ||
+      d.ffn <= 0 || d.ffn_padded < d.ffn || d.ffn_padded % 64 || d.vocab <= 0 || d.d_model > 12288)
+    return set_error(QCF_ERR_SHAPE,
+                     "%s: unsupported dims (L=%d d=%d Hq=%d Hkv=%d D=%d ffn=%d ffn_padded=%d vocab=%d); need D in "
+                     "{16,64,128}, d%%64==0, Hq*D%%64==0, ffn_padded%%64==0, Hq/Hkv<=8",
+                     who, d.n_layers, d.d_model, d.n_heads, d.n_kv_heads, D, d.ffn, d.ffn_padded, d.vocab);
+  return QCF_OK;
+}
+
+static qcf_status check_model(const qcf_model* m, const char* who) {
+  if (!m || !m->layers || !m->embed || !m->lm_head || !m->g_final || !m->rope.cos || !m->rope.sin)
+    return set_error(QCF_ERR_INVALID_ARG, "%s: model has NULL pointers", who);
+  qcf_status s = check_dims(m->dims, who);
+  if (s != QCF_OK) return s;
+  if (m->rope.head_dim != m->dims.head_dim) return set_error(QCF_ERR_SHAPE, "%s: RoPE table head dim mismatch", who);
+  return QCF_OK;
+}
+
+// One decoder layer on rows x (validated by the caller).
+static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, const int32_t* rope_pos,
+                                     const int32_t* cache_row, int n, __nv_bfloat16* Kc, __nv_bfloat16* Vc, int T,
+                                     const LayerBufs& b, cudaStream_t st) {
+  const qcf_dims& d = m->dims;
+  const qcf_layer_weights& w = m->layers[layer];
+  const int D = d.head_dim, Hq = d.n_heads, Hkv = d.n_kv_heads;
+  cudaError_t e = launch_rmsnorm(x, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, b.h, st);
+  if (e != cudaSuccess) return cuda_error(e, "layer: rmsnorm");
+  EpiParams ep{};
+  ep.q_out = b.q;
+  ep.k_cache = Kc;
+  ep.v_cache = Vc;
+  ep.rope_pos = rope_pos;
+  ep.cache_row = cache_row;
+  ep.cos_t = m->rope.cos;
+  ep.sin_t = m->rope.sin;
+  ep.Hq = Hq;
+  ep.Hkv = Hkv;
+  ep.D = D;
+  ep.T = T;
+  ep.max_pos = m->rope.max_pos;
+  ep.status = device_status_ptr();
+  qcf_status s = gemm_launch(EPI_QKV_ROPE, b.h, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
+                             (Hq + 2 * Hkv) * D, ep, b.gemm_ws, b.gemm_ws_bytes, st, KC_GEMM_QKV);
+  if (s != QCF_OK) return s;
+  s = attn_launch(b.q, cache_row, n, Kc, Vc, T, Hq, Hkv, D, 1.0f / sqrtf(static_cast<float>(D)), b.o, nullptr, nullptr,
+                  0, st);
+  if (s != QCF_OK) return s;
+  EpiParams eo{};
+  eo.out = x;
+  eo.ldo = d.d_model;
+  s = gemm_launch(EPI_ADD_F32, b.o, n, Hq * D, reinterpret_cast<const __nv_bfloat16*>(w.w_o), d.d_model, eo, b.gemm_ws,
+                  b.gemm_ws_bytes, st, KC_GEMM_O);
+  if (s != QCF_OK) return s;
+  e = launch_rmsnorm(x, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_mlp), d.eps, b.h, st);
+  if (e != cudaSuccess) return cuda_error(e, "layer: rmsnorm");
+  EpiParams eg{};
+  eg.out = b.act;
+  eg.ldo = d.ffn_padded;
+  s = gemm_launch(EPI_SWIGLU, b.h, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_gu), 2 * d.ffn_padded, eg,
+                  b.gemm_ws, b.gemm_ws_bytes, st, KC_GEMM_GU);
+  if (s != QCF_OK) return s;
+  EpiParams edn{};
+  edn.out = x;
+  edn.ldo = d.d_model;
+  return gemm_launch(EPI_ADD_F32, b.act, n, d.ffn_padded, reinterpret_cast<const __nv_bfloat16*>(w.w_down), d.d_model,
+                     edn, b.gemm_ws, b.gemm_ws_bytes, st, KC_GEMM_DOWN);
+}
+
+// ------------------------------------------------------------------ small helper kernels
+
+// out[i] = start + i
+__global__ void iota_kernel(int32_t* out, int n, int start) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = start + i;
+}
+
+// rows[i] = sel[i] for i < N, then the query rows C, C+1, ...
+__global__ void make_rows_kernel(const int32_t* __restrict__ sel, int N, int C, int n, int32_t* __restrict__ rows) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) rows[i] = i < N ? sel[i] : C + (i - N);
+}
+
+constexpr int kMaxReqChunks = 512;
+struct ChunkOffsets {
+  int n_chunks;
+  int off[kMaxReqChunks];
+};
+
+// Probe KV prefix for one layer: anchor rows of every chunk from the staging
+// buffer [chunk][layer][anchor][Hkv*D] into probe cache rows chunk*A + a, keys
+// re-rotated by the chunk's offset, values copied.  One thread per (row, head,
+// group of 8 rotation pairs).
+__global__ void anchor_assemble_kernel(const __nv_bfloat16* __restrict__ stK, const __nv_bfloat16* __restrict__ stV,
+                                       int layer, int n_layers_staged, int A, int Hkv, int D,
+                                       const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+                                       const ChunkOffsets co, __nv_bfloat16* __restrict__ pK,
+                                       __nv_bfloat16* __restrict__ pV) {
+  const int half = D / 2, groups = half / 8;
+  const int per_row = Hkv * groups;
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int rows = co.n_chunks * A;
+  if (tid >= rows * per_row) return;
+  const int row = tid / per_row;
+  const int rem = tid - row * per_row;
+  const int h = rem / groups, k0 = (rem - h * groups) * 8;
+  const int c = row / A, a = row - c * A;
+  const size_t HD = static_cast<size_t>(Hkv) * D;
+  const size_t src = ((static_cast<size_t>(c) * n_layers_staged + layer) * A + a) * HD + static_cast<size_t>(h) * D;
+  const size_t dst = static_cast<size_t>(row) * HD + static_cast<size_t>(h) * D;
+  const int delta = co.off[c];
+  const __nv_bfloat162* ka = reinterpret_cast<const __nv_bfloat162*>(stK + src + k0);
+  const __nv_bfloat162* kb = reinterpret_cast<const __nv_bfloat162*>(stK + src + half + k0);
+  const float* cs = cos_t + static_cast<size_t>(delta) * half + k0;
+  const float* sn = sin_t + static_cast<size_t>(delta) * half + k0;
+  __nv_bfloat162 o1[4], o2[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 av = __bfloat1622float2(ka[i]), bv = __bfloat1622float2(kb[i]);
+    o1[i] = __floats2bfloat162_rn(av.x * cs[2 * i] - bv.x * sn[2 * i], av.y * cs[2 * i + 1] - bv.y * sn[2 * i + 1]);
+    o2[i] = __floats2bfloat162_rn(bv.x * cs[2 * i] + av.x * sn[2 * i], bv.y * cs[2 * i + 1] + av.y * sn[2 * i + 1]);
+  }
+  *reinterpret_cast<uint4*>(pK + dst + k0) = *reinterpret_cast<uint4*>(o1);
+  *reinterpret_cast<uint4*>(pK + dst + half + k0) = *reinterpret_cast<uint4*>(o2);
+  *reinterpret_cast<uint4*>(pV + dst + k0) = *reinterpret_cast<const uint4*>(stV + src + k0);
+  *reinterpret_cast<uint4*>(pV + dst + half + k0) = *reinterpret_cast<const uint4*>(stV + src + half + k0);
+}
+
+// ------------------------------------------------------------------ request plan
+
+struct RequestLayout {
+  int C, Q, T, N, ns, nA, crit;
+  LayerBufs lb;          // sized for max(ns rows over T, Q rows over nA+Q)
+  float* x;              // [ns][d]
+  int32_t* rows;         // [ns]
+  int32_t* probe_pos;    // [Q] absolute positions C..T-1
+  int32_t* probe_row;    // [Q] probe cache rows nA..nA+Q-1
+  __nv_bfloat16* stK;    // [n_chunks][crit][A][HD]
+  __nv_bfloat16* stV;
+  __nv_bfloat16* pK;     // [nA+Q][HD]
+  __nv_bfloat16* pV;
+  __nv_bfloat16* q_crit; // [Q][Hq*D]
+  float* scores;         // [C]
+  int32_t* sel;          // [N]
+  void* prof_ws;
+  size_t prof_ws_bytes;
+  void* lm_ws;
+};
+
+static bool carve_request(Carve& c, const qcf_dims& d, int C, int Q, int nA, int N, int n_chunks, int crit,
+                          int n_anchor, RequestLayout* r) {
+  const int T = C + Q, ns = N + Q;
+  const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim;
+  r->C = C; r->Q = Q; r->T = T; r->N = N; r->ns = ns; r->nA = nA; r->crit = crit;
+  const int nmax = ns > Q ? ns : Q;
+  r->lb.h = c.take<__nv_bfloat16>(static_cast<size_t>(nmax) * d.d_model);
+  r->lb.q = c.take<__nv_bfloat16>(static_cast<size_t>(nmax) * d.n_heads * d.head_dim);
+  r->lb.o = c.take<__nv_bfloat16>(static_cast<size_t>(nmax) * d.n_heads * d.head_dim);
+  r->lb.act = c.take<__nv_bfloat16>(static_cast<size_t>(nmax) * d.ffn_padded);
+  r->lb.gemm_ws_bytes = std::max(gemm_ws_layer(d, ns), gemm_ws_layer(d, Q));
+  r->lb.gemm_ws = c.take<uint8_t>(r->lb.gemm_ws_bytes);
+  r->x = c.take<float>(static_cast<size_t>(nmax) * d.d_model);
+  r->rows = c.take<int32_t>(ns);
+  r->probe_pos = c.take<int32_t>(Q);
+  r->probe_row = c.take<int32_t>(Q);
+  const size_t staged = static_cast<size_t>(n_chunks) * (crit > 0 ? crit : 1) * (n_anchor > 0 ? n_anchor : 1) * HD;
+  r->stK = c.take<__nv_bfloat16>(staged);
+  r->stV = c.take<__nv_bfloat16>(staged);
+  r->pK = c.take<__nv_bfloat16>(static_cast<size_t>(nA + Q) * HD);
+  r->pV = c.take<__nv_bfloat16>(static_cast<size_t>(nA + Q) * HD);
+  r->q_crit = c.take<__nv_bfloat16>(static_cast<size_t>(Q) * d.n_heads * d.head_dim);
+  r->scores = c.take<float>(C);
+  r->sel = c.take<int32_t>(N > 0 ? N : 1);
+  r->prof_ws_bytes = qcf_profile_scores_workspace_size(Q, C, d.n_heads, d.n_kv_heads, d.head_dim);
+  r->prof_ws = c.take<uint8_t>(r->prof_ws_bytes);
+  r->lm_ws = c.take<uint8_t>(256);
+  return c.ok;
+}
+
+struct EventPool {
+  std::mutex mu;
+  std::vector<cudaEvent_t> ev;
+  bool get(size_t n, cudaEvent_t** out) {
+    while (ev.size() < n) {
+      cudaEvent_t e;
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+      ev.push_back(e);
+    }
+    *out = ev.data();
+    return true;
+  }
+};
+static EventPool& event_pool() {
+  static EventPool p;
+  return p;
+}
+
+}  // namespace qcf
+
+using namespace qcf;
+
+extern "C" {
+
+size_t qcf_layer_workspace_size(const qcf_dims* dims, int n, int T) {
+  if (!dims || n <= 0 || T <= 0) return 0;
+  return layer_ws_bytes(*dims, n, T);
+}
+
+qcf_status qcf_fused_layer_forward(const qcf_model* m, int layer, float* x, const int32_t* rope_pos,
+                                   const int32_t* cache_row, int n, qcf_bf16* K_cache, qcf_bf16* V_cache, int T,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  qcf_status s = check_model(m, "qcf_fused_layer_forward");
+  if (s != QCF_OK) return s;
+  if (!x || !rope_pos || !cache_row || !K_cache || !V_cache || !ws)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_fused_layer_forward: NULL pointer");
+  if (layer < 0 || layer >= m->dims.n_layers || n < 0 || T <= 0 || n > T)
+    return set_error(QCF_ERR_SHAPE, "qcf_fused_layer_forward: layer=%d n=%d T=%d", layer, n, T);
+  if (m->rope.max_pos < T) return set_error(QCF_ERR_SHAPE, "qcf_fused_layer_forward: RoPE table shorter than T");
+  if (take_fault(4) || !aligned16(x) || !aligned16(K_cache) || !aligned16(V_cache) || !aligned16(ws))
+    return set_error(QCF_ERR_ALIGN, "qcf_fused_layer_forward: alignment");
+  if (take_fault(2) || ws_bytes < layer_ws_bytes(m->dims, n, T))
+    return set_error(QCF_ERR_WORKSPACE, "qcf_fused_layer_forward: workspace %zu < %zu", ws_bytes,
+                     layer_ws_bytes(m->dims, n, T));
+  if (n == 0) return QCF_OK;
+  Carve c{static_cast<uint8_t*>(ws), ws_bytes};
+  LayerBufs b;
+  if (!carve_layer(c, m->dims, n, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_fused_layer_forward: workspace");
+  return layer_forward_impl(m, layer, x, rope_pos, cache_row, n, reinterpret_cast<__nv_bfloat16*>(K_cache),
+                            reinterpret_cast<__nv_bfloat16*>(V_cache), T, b, static_cast<cudaStream_t>(stream));
+}
+
+size_t qcf_full_prefill_workspace_size(const qcf_dims* dims, int T) {
+  if (!dims || T <= 0) return 0;
+  Carve c{nullptr, 0};
+  c.take<float>(static_cast<size_t>(T) * dims->d_model);
+  c.take<int32_t>(T);
+  c.take<uint8_t>(256);
+  c.take<uint8_t>(layer_ws_bytes(*dims, T, T));
+  return c.used;
+}
+
+qcf_status qcf_full_prefill(const qcf_model* m, const int32_t* ids, int T, qcf_bf16* const* K_layers,
+                            qcf_bf16* const* V_layers, float* last_logits, int32_t* first_token, void* ws,
+                            size_t ws_bytes, void* stream) {
+  qcf_status s = check_model(m, "qcf_full_prefill");
+  if (s != QCF_OK) return s;
+  if (!ids || !K_layers || !V_layers || !last_logits || !first_token || !ws)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_full_prefill: NULL pointer");
+  if (T <= 0 || m->rope.max_pos < T) return set_error(QCF_ERR_SHAPE, "qcf_full_prefill: T=%d (RoPE table %d)", T, m->rope.max_pos);
+  for (int l = 0; l < m->dims.n_layers; ++l)
+    if (!K_layers[l] || !V_layers[l] || !aligned16(K_layers[l]) || !aligned16(V_layers[l]))
+      return set_error(QCF_ERR_ALIGN, "qcf_full_prefill: layer %d cache pointer NULL or misaligned", l);
+  if (take_fault(2) || ws_bytes < qcf_full_prefill_workspace_size(&m->dims, T))
+    return set_error(QCF_ERR_WORKSPACE, "qcf_full_prefill: workspace too small");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c{static_cast<uint8_t*>(ws), ws_bytes};
+  float* x = c.take<float>(static_cast<size_t>(T) * m->dims.d_model);
+  int32_t* pos = c.take<int32_t>(T);
+  void* lm_ws = c.take<uint8_t>(256);
+  LayerBufs b;
+  if (!carve_layer(c, m->dims, T, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_full_prefill: workspace");
+  cudaError_t e = launch_embed(reinterpret_cast<const __nv_bfloat16*>(m->embed), m->dims.vocab, m->dims.d_model, ids,
+                               nullptr, 0, T, x, st);
+  if (e != cudaSuccess) return cuda_error(e, "qcf_full_prefill: embed");
+  {
+    LaunchScope ls(KC_MISC, st);
+    iota_kernel<<<(T + 255) / 256, 256, 0, st>>>(pos, T, 0);
+  }
+  for (int l = 0; l < m->dims.n_layers; ++l) {
+    s = layer_forward_impl(m, l, x, pos, pos, T, reinterpret_cast<__nv_bfloat16*>(K_layers[l]),
+                           reinterpret_cast<__nv_bfloat16*>(V_layers[l]), T, b, st);
+    if (s != QCF_OK) return s;
+  }
+  e = launch_lm_head(m, x + static_cast<size_t>(T - 1) * m->dims.d_model, last_logits, first_token, lm_ws, st);
+  return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_full_prefill: lm head");
+}
+
+size_t qcf_request_workspace_size(const qcf_dims* dims, int C, int Q, int n_anchor_total, int N) {
+  if (!dims || C <= 0 || Q <= 0 || N < 0 || N > C || n_anchor_total < 0) return 0;
+  // staging holds every chunk's anchors for the probe layers; bound it by the total anchor count
+  Carve c{nullptr, 0};
+  RequestLayout r;
+  const int crit = dims->n_layers;  // upper bound on probe layers
+  carve_request(c, *dims, C, Q, n_anchor_total, N, 1, crit, n_anchor_total > 0 ? n_anchor_total : 1, &r);
+  return c.used;
+}
+
+qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, void* ws,
+                               size_t ws_bytes, void* compute_stream, void* copy_stream) {
+  qcf_status s = check_model(m, "qcf_request_prefill");
+  if (s != QCF_OK) return s;
+  if (!r || !out || !ws || !r->chunk_len || !r->chunk_K_host || !r->chunk_V_host || !r->ids)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill: NULL pointer");
+  if (!out->K_layers || !out->V_layers || !out->last_logits || !out->first_token)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill: outputs need K/V layers, logits and first token");
+  const qcf_dims& d = m->dims;
+  const int L = d.n_layers;
+  if (r->n_chunks <= 0 || r->n_chunks > kMaxReqChunks || r->query_len <= 0 || r->crit_layer < 0 ||
+      r->crit_layer >= L || r->ratio_bp < 0 || r->ratio_bp > 10000 || r->n_anchor < 0)
+    return set_error(QCF_ERR_SHAPE, "qcf_request_prefill: n_chunks=%d query_len=%d crit=%d ratio_bp=%d n_anchor=%d",
+                     r->n_chunks, r->query_len, r->crit_layer, r->ratio_bp, r->n_anchor);
+  std::vector<int32_t> seg_start(r->n_chunks + 1, 0), seg_delta(r->n_chunks, 0);
+  ChunkOffsets co;
+  co.n_chunks = r->n_chunks;
+  for (int c = 0; c < r->n_chunks; ++c) {
+    const int len = r->chunk_len[c];
+    if (len <= 0 || len < r->n_anchor || !r->chunk_K_host[c] || !r->chunk_V_host[c])
+      return set_error(QCF_ERR_SHAPE, "qcf_request_prefill: chunk %d length %d / host pointers", c, len);
+    seg_delta[c] = seg_start[c];
+    co.off[c] = seg_start[c];
+    seg_start[c + 1] = seg_start[c] + len;
+  }
+  const int C = seg_start[r->n_chunks], Q = r->query_len, T = C + Q;
+  int N = 0;
+  qcf_num_selected(C, r->ratio_bp, &N);
+  const int crit = r->crit_layer;
+  const int A = r->n_anchor;
+  const int nA = (crit > 0) ? A * r->n_chunks : 0;
+  if (nA > 0 && (!r->anchor_K_host || !r->anchor_V_host))
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill: anchor stores are NULL");
+  if (m->rope.max_pos < T) return set_error(QCF_ERR_SHAPE, "qcf_request_prefill: RoPE table %d shorter than T=%d", m->rope.max_pos, T);
+  for (int l = 0; l < L; ++l)
+    if (!out->K_layers[l] || !out->V_layers[l] || !aligned16(out->K_layers[l]) || !aligned16(out->V_layers[l]))
+      return set_error(QCF_ERR_ALIGN, "qcf_request_prefill: fused cache of layer %d NULL or misaligned", l);
+  if (take_fault(4) || !aligned16(ws)) return set_error(QCF_ERR_ALIGN, "qcf_request_prefill: workspace misaligned");
+  if (take_fault(1)) return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill: injected invalid index table");
+  Carve cv{static_cast<uint8_t*>(ws), ws_bytes};
+  RequestLayout rl;
+  if (take_fault(2) || !carve_request(cv, d, C, Q, nA, N, r->n_chunks, crit, A, &rl))
+    return set_error(QCF_ERR_WORKSPACE, "qcf_request_prefill: workspace %zu too small (need %zu)", ws_bytes, cv.used);
+  float* scores = out->scores ? out->scores : rl.scores;
+  int32_t* sel = out->sel ? out->sel : rl.sel;
+  __nv_bfloat16* q_crit = out->q_crit ? reinterpret_cast<__nv_bfloat16*>(out->q_crit) : rl.q_crit;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+  cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+  const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim;
+  const size_t eb = sizeof(qcf_bf16);
+
+  EventPool& pool = event_pool();
+  std::lock_guard<std::mutex> lk(pool.mu);
+  cudaEvent_t* ev = nullptr;
+  if (!pool.get(static_cast<size_t>(L) + 3, &ev)) return set_error(QCF_ERR_CUDA, "qcf_request_prefill: event create");
+  cudaEvent_t ev_start = ev[0], ev_anchor = ev[1], ev_crit = ev[2];
+  cudaEvent_t* ev_layer = ev + 3;
+
+  cudaError_t e = cudaEventRecord(ev_start, cs);
+  if (e != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record start");
+  if ((e = cudaStreamWaitEvent(xs, ev_start, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: copy wait");
+
+  // ---- copy stream: anchors of the probe layers, the critical layer's keys, then every layer in order
+  if (take_fault(3)) return set_error(QCF_ERR_CUDA, "qcf_request_prefill: injected host-to-device copy failure");
+  for (int c = 0; c < r->n_chunks && nA > 0; ++c) {
+    const size_t n_el = static_cast<size_t>(crit) * A * HD;
+    if ((e = cudaMemcpyAsync(rl.stK + c * n_el, r->anchor_K_host[c], n_el * eb, cudaMemcpyHostToDevice, xs)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(rl.stV + c * n_el, r->anchor_V_host[c], n_el * eb, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: anchor copy");
+  }
+  if ((e = cudaEventRecord(ev_anchor, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
+  auto copy_layer = [&](int l, bool keys, bool values) -> cudaError_t {
+    for (int c = 0; c < r->n_chunks; ++c) {
+      const int len = r->chunk_len[c];
+      const size_t n_el = static_cast<size_t>(len) * HD;
+      const size_t src_off = static_cast<size_t>(l) * n_el;
+      const size_t dst_off = static_cast<size_t>(seg_start[c]) * HD;
+      cudaError_t ce;
+      if (keys && (ce = cudaMemcpyAsync(out->K_layers[l] + dst_off, r->chunk_K_host[c] + src_off, n_el * eb,
+                                        cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+        return ce;
+      if (values && (ce = cudaMemcpyAsync(out->V_layers[l] + dst_off, r->chunk_V_host[c] + src_off, n_el * eb,
+                                          cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+        return ce;
+    }
+    return cudaSuccess;
+  };
+  if ((e = copy_layer(crit, true, false)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: critical-layer copy");
+  if ((e = cudaEventRecord(ev_crit, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
+  for (int l = 0; l < L; ++l) {
+    if ((e = copy_layer(l, l != crit, true)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: layer copy");
+    if ((e = cudaEventRecord(ev_layer[l], xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
+  }
+
+  // ---- compute stream
+  const __nv_bfloat16* embed = reinterpret_cast<const __nv_bfloat16*>(m->embed);
+  // probe: query rows at positions C..T-1 with the anchors as KV prefix (probe cache rows 0..nA-1)
+  if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, nullptr, C, Q, rl.x, cs)) != cudaSuccess)
+    return cuda_error(e, "qcf_request_prefill: embed");
+  {
+    LaunchScope ls(KC_MISC, cs);
+    iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_pos, Q, C);
+  }
+  {
+    LaunchScope ls(KC_MISC, cs);
+    iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_row, Q, nA);
+  }
+  if (crit > 0) {
+    if ((e = cudaStreamWaitEvent(cs, ev_anchor, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+    for (int l = 0; l < crit; ++l) {
+      if (nA > 0) {
+        const int threads = nA * d.n_kv_heads * (d.head_dim / 16);
+        LaunchScope ls(KC_ROPE, cs);
+        anchor_assemble_kernel<<<(threads + 255) / 256, 256, 0, cs>>>(rl.stK, rl.stV, l, crit, A, d.n_kv_heads,
+                                                                      d.head_dim, m->rope.cos, m->rope.sin, co, rl.pK,
+                                                                      rl.pV);
+      }
+      s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK, rl.pV, nA + Q, rl.lb, cs);
+      if (s != QCF_OK) return s;
+    }
+  }
+  // critical layer: q = RoPE(RMSNorm(x) W_q) only
+  {
+    const qcf_layer_weights& w = m->layers[crit];
+    if ((e = launch_rmsnorm(rl.x, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, rl.lb.h, cs)) !=
+        cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: rmsnorm");
+    EpiParams ep{};
+    ep.q_out = q_crit;
+    ep.rope_pos = rl.probe_pos;
+    ep.cache_row = nullptr;
+    ep.cos_t = m->rope.cos;
+    ep.sin_t = m->rope.sin;
+    ep.Hq = d.n_heads;
+    ep.Hkv = d.n_kv_heads;
+    ep.D = d.head_dim;
+    ep.T = 1;
+    ep.max_pos = m->rope.max_pos;
+    ep.status = device_status_ptr();
+    s = gemm_launch(EPI_QKV_ROPE, rl.lb.h, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
+                    d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_QKV);
+    if (s != QCF_OK) return s;
+  }
+  // profile the re-rotated critical-layer keys and select
+  if ((e = cudaStreamWaitEvent(cs, ev_crit, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+  __nv_bfloat16* Kcrit = reinterpret_cast<__nv_bfloat16*>(out->K_layers[crit]);
+  if ((e = launch_reposition(Kcrit, Kcrit, C, d.n_kv_heads, d.head_dim, seg_start.data(), seg_delta.data(), r->n_chunks,
+                             &m->rope, cs)) != cudaSuccess)
+    return cuda_error(e, "qcf_request_prefill: reposition");
+  s = qcf_profile_scores(reinterpret_cast<const qcf_bf16*>(q_crit), reinterpret_cast<const qcf_bf16*>(Kcrit), Q, C,
+                         d.n_heads, d.n_kv_heads, d.head_dim, 1.0f / sqrtf(static_cast<float>(d.head_dim)), scores,
+                         rl.prof_ws, rl.prof_ws_bytes, cs);
+  if (s != QCF_OK) return s;
+  if (N > 0) {
+    if (r->forced_sel) {
+      if ((e = cudaMemcpyAsync(sel, r->forced_sel, N * sizeof(int32_t), cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
+        return cuda_error(e, "qcf_request_prefill: forced selection");
+    } else {
+      s = qcf_topn_select(scores, C, N, sel, cs);
+      if (s != QCF_OK) return s;
+    }
+  }
+  const int ns = N + Q;
+  {
+    LaunchScope ls(KC_MISC, cs);
+    make_rows_kernel<<<(ns + 255) / 256, 256, 0, cs>>>(sel, N, C, ns, rl.rows);
+  }
+  // pipelined per-layer recompute of the selected rows and the query
+  if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, rl.rows, 0, ns, rl.x, cs)) != cudaSuccess)
+    return cuda_error(e, "qcf_request_prefill: embed");
+  for (int l = 0; l < L; ++l) {
+    if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+    __nv_bfloat16* Kl = reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]);
+    __nv_bfloat16* Vl = reinterpret_cast<__nv_bfloat16*>(out->V_layers[l]);
+    if (l != crit) {
+      if ((e = launch_reposition(Kl, Kl, C, d.n_kv_heads, d.head_dim, seg_start.data(), seg_delta.data(), r->n_chunks,
+                                 &m->rope, cs)) != cudaSuccess)
+        return cuda_error(e, "qcf_request_prefill: reposition");
+    }
+    s = layer_forward_impl(m, l, rl.x, rl.rows, rl.rows, ns, Kl, Vl, T, rl.lb, cs);
+    if (s != QCF_OK) return s;
+  }
+  if ((e = launch_lm_head(m, rl.x + static_cast<size_t>(ns - 1) * d.d_model, out->last_logits, out->first_token,
+                          rl.lm_ws, cs)) != cudaSuccess)
+    return cuda_error(e, "qcf_request_prefill: lm head");
+  if (out->x_rows &&
+      (e = cudaMemcpyAsync(out->x_rows, rl.x, static_cast<size_t>(ns) * d.d_model * sizeof(float),
+                           cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
+    return cuda_error(e, "qcf_request_prefill: copy rows");
+  if (out->first_token_host &&
+      (e = cudaMemcpyAsync(out->first_token_host, out->first_token, sizeof(int32_t), cudaMemcpyDeviceToHost, cs)) !=
+          cudaSuccess)
+    return cuda_error(e, "qcf_request_prefill: first token copy");
+  return QCF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,224 @@
+"""Parity of every qcf_* kernel entry point with the CPU oracle (GPU).
+
+Inputs come from qcdata's seeded generators; expected values from oracle/ only.
+Sizes span several tiles with ragged tails; full-size sweep points are checked
+through properties that hold at any size.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import qcfdata as qd
+from oracle import qcf_oracle as O
+from _parity import assert_close, assert_same_selection
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def Q():
+    from rag_kv_cache_re_gb300 import qcf
+    return qcf
+
+
+DEV = "cuda"
+
+
+def f32(t):
+    return t.float().cpu().numpy()
+
+
+def table(Q, max_pos, D):
+    return Q.RopeTable(max_pos, D, 1e4, DEV)
+
+
+# ----------------------------------------------------------------- RoPE re-rotation
+
+@pytest.mark.parametrize("D,Hkv", [(16, 4), (128, 8)])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_rope_reposition(Q, D, Hkv, inplace):
+    lens = [37, 512, 3, 200]
+    start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    delta = np.array([0, 5000, 131000, 77], np.int32)
+    K = qd.normal_bf16((int(start[-1]), Hkv, D), 1.0, 11, DEV)
+    src = K.clone()
+    dst = K if inplace else torch.empty_like(K)
+    Q.qcf_rope_reposition(K, dst, start, delta, table(Q, 131200, D))
+    torch.cuda.synchronize()
+    ref = np.concatenate([O.rope_reposition(f32(src[start[s]:start[s + 1]]), delta[s], 1e4) for s in range(len(lens))])
+    got = f32(dst)
+    # bf16 output: within one rounding of the exact rotation (fp32 table)
+    assert_close(got, ref, atol=1e-6, rtol=2.0 ** -8, what="reposition")
+    assert_close(got, ref, atol=2e-2, rtol=2e-2, what="reposition (stated tolerance)")
+
+
+# ----------------------------------------------------------------- anchors
+
+@pytest.mark.parametrize("D,Hkv,lens,A", [(16, 4, [32, 32, 32], 2), (128, 8, [512] * 10, 8), (128, 8, [700, 9, 1024], 8)])
+def test_anchor_keynorm_topk(Q, D, Hkv, lens, A):
+    start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    K = qd.normal_bf16((int(start[-1]), Hkv, D), 1.0, 12, DEV)
+    K[5] = K[1]                      # exact norm tie inside chunk 0: lower index wins
+    idx, norms = Q.qcf_anchor_keynorm_topk(K, start, A, want_norms=True)
+    torch.cuda.synchronize()
+    Kh = f32(K)
+    ref_idx = O.keynorm_anchors(Kh, start, A)
+    got = idx.cpu().numpy()
+    for c in range(len(lens)):
+        rows = Kh[start[c]:start[c + 1]].astype(np.float64)
+        nrm = np.sqrt(np.sum(rows.reshape(rows.shape[0], -1) ** 2, axis=1))
+        assert np.all(np.diff(got[c]) > 0), "anchors must be ascending"
+        assert_same_selection(got[c], nrm, A, tie_tol=1e-5 * nrm.max(), what=f"anchors chunk {c}")
+    assert (5 not in got[0]) or (1 in got[0]), "equal norms: the lower index must be taken first"
+    assert ref_idx.shape == got.shape
+    ref_n = np.sqrt(np.sum(Kh.astype(np.float64).reshape(Kh.shape[0], -1) ** 2, axis=1))
+    assert_close(norms.cpu().numpy(), ref_n, atol=1e-4, rtol=1e-5, what="norms")
+
+
+# ----------------------------------------------------------------- profiling
+
+@pytest.mark.parametrize("C,nq,Hq,Hkv,D,scale", [
+    (96, 8, 4, 4, 16, 0.25),       # tiny model shape
+    (300, 64, 32, 8, 128, 1.0),    # ragged tail, sweep distributions
+    (4096, 64, 32, 8, 128, 1.0),   # sweep 4k
+    (5120, 64, 32, 8, 128, 1.0 / math.sqrt(128)),  # 8B request shape
+    (16384, 64, 32, 8, 128, 1.0),  # sweep 16k
+    (2000, 128, 56, 8, 128, 1.0),  # 34B head layout (7 heads per KV head, 4 row groups)
+])
+def test_profile_scores(Q, C, nq, Hq, Hkv, D, scale):
+    t = qd.sweep_tensors(C, n_query=nq, Hq=Hq, Hkv=Hkv, D=D, device=DEV)
+    s = Q.qcf_profile_scores(t["Q"], t["K"], scale)
+    torch.cuda.synchronize()
+    ref = O.profile_scores(f32(t["Q"]), f32(t["K"]), scale)
+    assert_close(s.cpu().numpy(), ref, atol=1e-3, rtol=1e-3, what="scores")
+    assert abs(float(s.double().sum()) - Hq * nq) < 1e-3 * Hq * nq
+
+
+@pytest.mark.parametrize("C", [65536, 131072])
+def test_profile_scores_full_size_properties(Q, C):
+    t = qd.sweep_tensors(C, device=DEV)
+    s = Q.qcf_profile_scores(t["Q"], t["K"], 1.0)
+    torch.cuda.synchronize()
+    v = s.double().cpu().numpy()
+    assert np.all(v >= 0) and np.all(np.isfinite(v))
+    assert abs(v.sum() - 32 * 64) < 1e-3 * 32 * 64
+    # the keys with equal K get equal scores: plant a duplicate key and compare
+    K2 = t["K"].clone()
+    K2[C - 1] = K2[7]
+    s2 = Q.qcf_profile_scores(t["Q"], K2, 1.0).cpu().numpy()
+    assert abs(s2[C - 1] - s2[7]) <= 1e-6 * max(1e-30, abs(s2[7])) + 1e-9
+
+
+# ----------------------------------------------------------------- top-N
+
+@pytest.mark.parametrize("C", [1, 7, 1000, 5120, 20480, 131072])
+def test_topn_select_exact(Q, C):
+    rng = np.random.default_rng(C)
+    for kind in ("ties", "continuous"):
+        if kind == "ties":
+            v = (rng.integers(0, 9, C) * 0.125).astype(np.float32)
+            v[rng.integers(0, C, max(1, C // 10))] = -0.0
+        else:
+            v = rng.random(C, dtype=np.float32) * 2.0
+        s = torch.from_numpy(v).to(DEV)
+        for N in sorted({0, 1, max(0, C // 7), O.num_selected(C, 1500), C - 1, C}):
+            if N < 0:
+                continue
+            got = Q.qcf_topn_select(s, N).cpu().numpy()
+            want = O.topn_select(v.astype(np.float64), N)
+            assert np.array_equal(got, want), f"C={C} N={N} {kind}"
+
+
+# ----------------------------------------------------------------- gather / scatter
+
+def test_gather_and_scatter_exact(Q):
+    src = qd.normal_bf16((1000, 8, 128), 1.0, 13, DEV)
+    idx = torch.tensor(qd.selected_indices(1000, 77, "uniform"), dtype=torch.int32, device=DEV)
+    g = Q.qcf_gather_rows(src, idx)
+    assert torch.equal(g, src[idx.long()])
+    Kc = qd.normal_bf16((1000, 8, 128), 1.0, 14, DEV)
+    Vc = qd.normal_bf16((1000, 8, 128), 1.0, 15, DEV)
+    K0, V0 = Kc.clone(), Vc.clone()
+    kn = qd.normal_bf16((77, 8, 128), 1.0, 16, DEV)
+    vn = qd.normal_bf16((77, 8, 128), 1.0, 17, DEV)
+    Q.qcf_scatter_kv(kn, vn, idx, Kc, Vc)
+    K0[idx.long()] = kn
+    V0[idx.long()] = vn
+    assert torch.equal(Kc, K0) and torch.equal(Vc, V0)
+    assert Q.qcf_query_status() == 0
+
+
+def test_bad_index_sets_status_without_fault(Q):
+    src = qd.normal_bf16((10, 8), 1.0, 18, DEV)
+    idx = torch.tensor([1, 10, 3], dtype=torch.int32, device=DEV)   # 10 is out of range
+    Q.qcf_gather_rows(src, idx)
+    assert Q.qcf_query_status() & 0x2
+    assert Q.qcf_query_status() == 0                                  # read clears
+
+
+# ----------------------------------------------------------------- sparse causal attention
+
+@pytest.mark.parametrize("T,n,Hq,Hkv,D,pattern", [
+    (104, 23, 4, 4, 16, "uniform"),        # tiny fused shape (15 selected + 8 query)
+    (104, 104, 4, 4, 16, "all"),           # tiny full prefill (dense causal)
+    (300, 1, 32, 8, 128, "first"),         # a single row at position 0
+    (1000, 150, 32, 8, 128, "clusters"),
+    (5184, 832, 32, 8, 128, "uniform"),    # 8B request shape: 768 selected + 64 query
+    (2000, 300, 56, 8, 128, "uniform"),    # 34B head layout (G = 7)
+])
+def test_sparse_causal_attn(Q, T, n, Hq, Hkv, D, pattern):
+    if pattern == "all":
+        pos = np.arange(T)
+    elif pattern == "first":
+        pos = np.array([0])
+    else:
+        Cx = T - 64 if T > 600 else T - 8
+        nsel = n - (T - Cx)
+        pos = np.concatenate([qd.selected_indices(Cx, nsel, pattern), np.arange(Cx, T)])
+    pos = pos.astype(np.int32)
+    assert len(pos) == n
+    K = qd.normal_bf16((T, Hkv, D), 1.0, 21, DEV)
+    V = qd.normal_bf16((T, Hkv, D), 1.0, 22, DEV)
+    q = qd.normal_bf16((n, Hq, D), 1.0, 23, DEV)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = Q.qcf_sparse_causal_attn(q, torch.from_numpy(pos).to(DEV), K, V, scale, want_lse=True)
+    torch.cuda.synchronize()
+    ref = O.causal_attention(f32(q), pos, f32(K), f32(V), scale)
+    assert_close(f32(o), ref, atol=2e-2, rtol=2e-2, what="attention output")
+    # lse: natural log of sum_j exp(scale q.k_j) over visible keys
+    qd64, Kd = f32(q).astype(np.float64), f32(K).astype(np.float64)
+    G = Hq // Hkv
+    for r in list(range(0, n, max(1, n // 5)))[:5]:
+        for h in (0, Hq - 1):
+            s = scale * Kd[: pos[r] + 1, h // G] @ qd64[r, h]
+            want = s.max() + np.log(np.exp(s - s.max()).sum())
+            assert abs(float(lse[r, h]) - want) < 1e-3 * max(1.0, abs(want))
+    assert Q.qcf_query_status() == 0
+
+
+# ----------------------------------------------------------------- dense pieces
+
+@pytest.mark.parametrize("M,N,K", [(23, 192, 64), (1, 64, 64), (300, 384, 192), (832, 6144, 4096),
+                                   (64, 4096, 14336), (832, 4096, 14336), (200, 28672, 256)])
+def test_linear_store_and_add(Q, M, N, K):
+    A = qd.normal_bf16((M, K), 1.0, 31, DEV)
+    W = qd.normal_bf16((N, K), 0.02, 32, DEV)
+    ref = (f32(A) @ f32(W).T).astype(np.float64)   # fp32 BLAS: error far below the tolerances used
+    out = Q.qcf_linear(A, W)
+    torch.cuda.synchronize()
+    assert_close(f32(out), ref, atol=1e-3, rtol=2.0 ** -8, what="bf16 out")
+    base = torch.randn((M, N), device=DEV, dtype=torch.float32)
+    b0 = base.cpu().numpy().astype(np.float64)
+    Q.qcf_linear(A, W, out=base, add=True)
+    torch.cuda.synchronize()
+    assert_close(base.cpu().numpy(), b0 + ref, atol=1e-4, rtol=1e-5, what="fp32 residual add")
+
+
+def test_rmsnorm(Q):
+    x = torch.randn((300, 4096), device=DEV) * 3
+    g = qd.normal_bf16((4096,), 1.0, 33, DEV)
+    h = Q.qcf_rmsnorm(x, g, 1e-5)
+    ref = O.rmsnorm(x.cpu().numpy(), f32(g), 1e-5)
+    assert_close(f32(h), ref, atol=1e-6, rtol=2.0 ** -8, what="rmsnorm")
