@@ -191,8 +191,10 @@ def run_gpu(args):
     launches0 = Q.qcf_launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(cs)
+    torch.cuda.nvtx.range_push("qcf_timed")
     for _ in range(args.steps):
         step()
+    torch.cuda.nvtx.range_pop()
     ev1.record(cs)
     torch.cuda.synchronize()
     launches = Q.qcf_launch_count() - launches0

@@ -20,6 +20,7 @@
 //               into the cache at row cache_row[m]
 //   SWIGLU      W rows come in blocks of 64 gate rows then 64 up rows;
 //               out[m][f] = silu(gate) * up
+#include <algorithm>
 #include <mutex>
 
 #include "qcf_internal.cuh"
@@ -448,28 +449,40 @@ struct GemmPlan {
   int tiles;
 };
 
+// Chooses the tile width BN and the number of k splits with a small cost model:
+// time = max(rounds of units x per-unit time, weight bytes / HBM bandwidth of the
+// SMs that are busy).  A unit's main loop runs at the SM's tensor rate (narrower
+// tiles lose some of it to operand traffic); a split adds the fp32 partial it
+// writes and the fixup that reads the partials back.  Small-M GEMMs (the probe's
+// 64 rows) stream weights, so they split K to keep every SM loading; the 832-row
+// recompute GEMMs do not split.
 static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
   const int sms = num_sms();
   const int tiles_m = (M + kBM - 1) / kBM;
   const int kb = K / kBK;
+  const double sm_flops = 14.0e12;   // sustained dense bf16 per SM
+  const double hbm = 6.5e12;         // bytes/s
+  const double part_bw = 80.0e9;     // bytes/s one SM writes and reads its partials at
   GemmPlan best{64, 1, tiles_m * (N / 64)};
-  double best_score = -1.0;
+  double best_t = 1e30;
   const int cands[3] = {256, 128, 64};
   for (int bn : cands) {
     if (N % bn) continue;
     if (epi == EPI_SWIGLU && bn % 128) continue;
     if (epi == EPI_QKV_ROPE && bn % head_dim) continue;
+    const double eff = bn == 256 ? 1.0 : (bn == 128 ? 0.85 : 0.6);
     const int tiles = tiles_m * (N / bn);
-    for (int s = 1; s <= 4; ++s) {
-      if (s > 1 && kb / s < 16) break;
+    for (int s = 1; s <= 8; ++s) {
+      if (s > 1 && kb / s < 8) break;
       const int units = tiles * s;
-      const int waves = (units + sms - 1) / sms;
-      const double eff = static_cast<double>(units) / (static_cast<double>(waves) * sms);
-      const double bn_factor = bn == 256 ? 1.0 : (bn == 128 ? 0.9 : 0.75);
-      const double split_factor = s == 1 ? 1.0 : 0.93;
-      const double score = eff * bn_factor * split_factor;
-      if (score > best_score + 1e-9) {
-        best_score = score;
+      const int rounds = (units + sms - 1) / sms;
+      double t_unit = 2.0 * kBM * bn * (static_cast<double>(K) / s) / (sm_flops * eff) + 1.0e-6;
+      if (s > 1) t_unit += 2.0 * kBM * bn * 4.0 / part_bw + 2.0e-6;
+      const double busy = units < sms ? static_cast<double>(units) / sms : 1.0;
+      const double t_mem = (static_cast<double>(N) * K * 2.0 + static_cast<double>(M) * K * 2.0) / (hbm * busy);
+      const double t = std::max(rounds * t_unit, t_mem);
+      if (t < best_t * 0.98) {
+        best_t = t;
         best = GemmPlan{bn, s, tiles};
       }
     }

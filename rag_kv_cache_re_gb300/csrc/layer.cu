@@ -73,7 +73,7 @@ static qcf_status check_dims(const qcf_dims& d, const char* who) {
   const int D = d.head_dim;
   if (d.n_layers <= 0 || d.d_model <= 0 || d.n_heads <= 0 || d.n_kv_heads <= 0 || d.n_heads % d.n_kv_heads ||
       d.n_heads / d.n_kv_heads > 8 || (D != 16 && D != 64 && D != 128) || d.d_model % 64 || (d.n_heads * D) % 64 ||
-      d.ffn <= 0 || d.ffn_padded < d.ffn || d.ffn_padded % 64 || d.vocab <= 0 || d.d_model > 12288)
+      d.ffn <= 0 || d.ffn_padded < d.ffn || d.ffn_padded % 64 || d.vocab <= 0 || d.d_model > 8192)
     return set_error(QCF_ERR_SHAPE,
                      "%s: unsupported dims (L=%d d=%d Hq=%d Hkv=%d D=%d ffn=%d ffn_padded=%d vocab=%d); need D in "
                      "{16,64,128}, d%%64==0, Hq*D%%64==0, ffn_padded%%64==0, Hq/Hkv<=8",

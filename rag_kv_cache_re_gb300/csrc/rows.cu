@@ -137,31 +137,49 @@ __global__ void embed_rows_kernel(const __nv_bfloat16* __restrict__ embed, int v
   }
 }
 
-// h = x / sqrt(mean(x^2) + eps) * g; one warp per row, fp32 statistics.
-__global__ void rmsnorm_kernel(const float* __restrict__ x, int n, int d, const __nv_bfloat16* __restrict__ g,
-                               float eps, __nv_bfloat16* __restrict__ h) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= n) return;
-  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(warp) * d);
+// h = x / sqrt(mean(x^2) + eps) * g with fp32 statistics.  One CTA of 256 threads
+// per row: the row (d <= 8192) is read once into registers, 4 float4 per thread,
+// so every load of the row is in flight at once.
+constexpr int kNormThreads = 256;
+constexpr int kNormVec = 8;   // float4 per thread: d <= 256 * 4 * 8 = 8192
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __restrict__ x, int n, int d,
+                                                               const __nv_bfloat16* __restrict__ g, float eps,
+                                                               __nv_bfloat16* __restrict__ h) {
+  __shared__ float red[kNormThreads / 32];
+  const int row = blockIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(row) * d);
+  const int nv = d / 4;
+  float4 v[kNormVec];
   float ss = 0.f;
-  for (int i = lane; i < d / 4; i += 32) {
-    const float4 v = xr[i];
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i = threadIdx.x + k * kNormThreads;
+    v[k] = i < nv ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
+  for (int k = 0; k < kNormVec; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+#pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
-  uint2* hr = reinterpret_cast<uint2*>(h + static_cast<int64_t>(warp) * d);
+  if (lane == 0) red[wid] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / static_cast<float>(d) + eps);
+  uint2* hr = reinterpret_cast<uint2*>(h + static_cast<int64_t>(row) * d);
   const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(g);
-  for (int i = lane; i < d / 4; i += 32) {
-    const float4 v = xr[i];
-    const float2 ga = __bfloat1622float2(g2[2 * i]);
-    const float2 gb = __bfloat1622float2(g2[2 * i + 1]);
-    uint2 o;
-    o.x = pack_bf16x2(v.x * inv * ga.x, v.y * inv * ga.y);
-    o.y = pack_bf16x2(v.z * inv * gb.x, v.w * inv * gb.y);
-    hr[i] = o;
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i = threadIdx.x + k * kNormThreads;
+    if (i < nv) {
+      const float2 ga = __bfloat1622float2(g2[2 * i]);
+      const float2 gb = __bfloat1622float2(g2[2 * i + 1]);
+      uint2 o;
+      o.x = pack_bf16x2(v[k].x * inv * ga.x, v[k].y * inv * ga.y);
+      o.y = pack_bf16x2(v[k].z * inv * gb.x, v[k].w * inv * gb.y);
+      hr[i] = o;
+    }
   }
 }
 
@@ -261,7 +279,7 @@ cudaError_t launch_rmsnorm(const float* x, int n, int d, const __nv_bfloat16* g,
                            cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   LaunchScope ls(KC_RMSNORM, st);
-  rmsnorm_kernel<<<(n + 7) / 8, 256, 0, st>>>(x, n, d, g, eps, h);
+  rmsnorm_kernel<<<n, kNormThreads, 0, st>>>(x, n, d, g, eps, h);
   return cudaGetLastError();
 }
 
@@ -366,7 +384,8 @@ qcf_status qcf_scatter_kv(const qcf_bf16* k_new, const qcf_bf16* v_new, const in
 
 qcf_status qcf_rmsnorm(const float* x, int n, int d, const qcf_bf16* g, float eps, qcf_bf16* h, void* stream) {
   if (!x || !g || !h) return set_error(QCF_ERR_INVALID_ARG, "qcf_rmsnorm: NULL pointer");
-  if (n < 0 || d <= 0 || d % 8) return set_error(QCF_ERR_SHAPE, "qcf_rmsnorm: d=%d must be a multiple of 8", d);
+  if (n < 0 || d <= 0 || d % 8 || d > 8192)
+    return set_error(QCF_ERR_SHAPE, "qcf_rmsnorm: d=%d must be a multiple of 8 and at most 8192", d);
   if (!aligned16(x) || !aligned16(g) || !aligned16(h)) return set_error(QCF_ERR_ALIGN, "qcf_rmsnorm: alignment");
   cudaError_t e = launch_rmsnorm(x, n, d, reinterpret_cast<const __nv_bfloat16*>(g), eps,
                                  reinterpret_cast<__nv_bfloat16*>(h), static_cast<cudaStream_t>(stream));

@@ -213,7 +213,10 @@ def test_linear_store_and_add(Q, M, N, K):
     b0 = base.cpu().numpy().astype(np.float64)
     Q.qcf_linear(A, W, out=base, add=True)
     torch.cuda.synchronize()
-    assert_close(base.cpu().numpy(), b0 + ref, atol=1e-4, rtol=1e-5, what="fp32 residual add")
+    # fp32 accumulation: each of the K/16 tensor-core steps may round the running
+    # sum once (2^-23 relative); bound by the result's scale
+    acc_tol = (K / 16) * 2.0 ** -22 * max(1.0, float(np.sqrt(np.mean(ref ** 2))))
+    assert_close(base.cpu().numpy(), b0 + ref, atol=max(1e-5, acc_tol), rtol=1e-5, what="fp32 residual add")
 
 
 def test_rmsnorm(Q):
