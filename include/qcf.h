@@ -149,6 +149,26 @@ size_t qcf_profile_scores_workspace_size(int nq, int C, int Hq, int Hkv, int D);
 qcf_status qcf_profile_scores(const qcf_bf16* q, const qcf_bf16* K, int nq, int C, int Hq, int Hkv, int D,
                               float scale, float* scores, void* ws, size_t ws_bytes, void* stream);
 
+/* qcf_profile_scores with no caller workspace and no allocation of any kind.
+ * The pages have no counterpart: this exists for callers that cannot allocate
+ * device memory at the point of the call -- for example a serving loop that
+ * gave all free device memory to its KV-cache pool at start-up, or code holding
+ * a memory budget fixed in advance that must not call cudaMalloc (which may
+ * also synchronise the device) on the request path.
+ * Scratch is one fixed 8 MiB array in device global memory, present on every
+ * GPU that loads the library for the life of the process.  A shape whose
+ * qcf_profile_scores_workspace_size() exceeds 8 MiB is rejected with
+ * QCF_ERR_WORKSPACE before anything runs; the 8B-shaped request (64 query rows
+ * x 32 heads over 5120 keys) needs under 1 MiB and 131072 keys under 6 MiB.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the one array: calls that overlap on the GPU (different streams, or
+ * host threads without ordering) race and corrupt each other's results.  Every
+ * call rewrites all the scratch it reads, so no clearing is needed.
+ * Arguments, layouts and results are those of qcf_profile_scores. */
+qcf_status qcf_profile_scores_noalloc(const qcf_bf16* q, const qcf_bf16* K, int nq, int C, int Hq, int Hkv, int D,
+                                      float scale, float* scores, void* stream);
+
 /* Top-N selection (QCFuse 2.A: "the Top-N context token indices"): the indices of
  * the N largest scores, ties to the lower index (the order of a stable sort by
  * descending score), written ascending to sel [N].  0 <= N <= C <= 2^24.

@@ -80,6 +80,7 @@ PROTOTYPES = {
     "qcf_rope_reposition": (I, [P, P, I64, I, I, PI32, PI32, I, C.POINTER(RopeTable), P]),
     "qcf_profile_scores_workspace_size": (SZ, [I, I, I, I, I]),
     "qcf_profile_scores": (I, [P, P, I, I, I, I, I, F, P, P, SZ, P]),
+    "qcf_profile_scores_noalloc": (I, [P, P, I, I, I, I, I, F, P, P]),
     "qcf_topn_select": (I, [P, I, I, P, P]),
     "qcf_gather_rows": (I, [P, I64, I, P, I, P, P]),
     "qcf_scatter_kv": (I, [P, P, P, I, I, I, P, P, I, P]),

@@ -13,6 +13,7 @@
 // group are (head-in-group, query row) pairs; a CTA takes up to 256 of them
 // (8 warps x 2 row tiles of 16).
 #include <mutex>
+#include <vector>
 
 #include "qcf_internal.cuh"
 
@@ -363,6 +364,35 @@ static qcf_status profile_launch_d(const __nv_bfloat16* q, const __nv_bfloat16* 
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "profile_scores: launch");
 }
 
+// ------------------------------------------------------------------ fixed scratch for callers that cannot allocate
+//
+// Scratch of qcf_profile_scores_noalloc: one array in device global memory that
+// exists for the life of the process on every GPU that loads this library.  Its
+// contents persist between calls; every call fully rewrites the parts it reads,
+// so nothing in it has to start at zero.
+constexpr size_t kNoAllocScratchBytes = 8u << 20;  // 8 MiB
+static __device__ __align__(256) uint8_t g_profile_scratch[kNoAllocScratchBytes];
+
+// Device address of g_profile_scratch for the current device, looked up once per
+// device (the symbol name is a host-side stand-in, not an address a kernel may use).
+static qcf_status profile_scratch_address(void** out) {
+  static std::mutex mu;
+  static std::vector<void*> per_dev;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "qcf_profile_scores_noalloc: cudaGetDevice");
+  std::lock_guard<std::mutex> lk(mu);
+  if (static_cast<int>(per_dev.size()) <= dev) per_dev.resize(dev + 1, nullptr);
+  if (!per_dev[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_profile_scratch);
+    if (e != cudaSuccess) return cuda_error(e, "qcf_profile_scores_noalloc: cudaGetSymbolAddress");
+    per_dev[dev] = p;
+  }
+  *out = per_dev[dev];
+  return QCF_OK;
+}
+
 }  // namespace qcf
 
 using namespace qcf;
@@ -393,6 +423,32 @@ qcf_status qcf_profile_scores(const qcf_bf16* q, const qcf_bf16* K, int nq, int 
     case 16: return profile_launch_d<16>(qq, kk, nq, C, Hq, Hkv, scale, scores, ws, st);
     case 64: return profile_launch_d<64>(qq, kk, nq, C, Hq, Hkv, scale, scores, ws, st);
     default: return profile_launch_d<128>(qq, kk, nq, C, Hq, Hkv, scale, scores, ws, st);
+  }
+}
+
+qcf_status qcf_profile_scores_noalloc(const qcf_bf16* q, const qcf_bf16* K, int nq, int C, int Hq, int Hkv, int D,
+                                      float scale, float* scores, void* stream) {
+  if (!q || !K || !scores) return set_error(QCF_ERR_INVALID_ARG, "qcf_profile_scores_noalloc: NULL pointer");
+  if (nq <= 0 || C <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || (D != 16 && D != 64 && D != 128))
+    return set_error(QCF_ERR_SHAPE, "qcf_profile_scores_noalloc: nq=%d C=%d Hq=%d Hkv=%d D=%d", nq, C, Hq, Hkv, D);
+  if (!aligned16(q) || !aligned16(K) || !aligned16(scores))
+    return set_error(QCF_ERR_ALIGN, "qcf_profile_scores_noalloc: pointers must be 16-byte aligned");
+  const size_t need = qcf_profile_scores_workspace_size(nq, C, Hq, Hkv, D);
+  if (need > kNoAllocScratchBytes)
+    return set_error(QCF_ERR_WORKSPACE,
+                     "qcf_profile_scores_noalloc: this shape needs %zu bytes of scratch, more than the fixed %zu; "
+                     "use qcf_profile_scores with a caller workspace",
+                     need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  qcf_status st = profile_scratch_address(&scratch);
+  if (st != QCF_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* qq = reinterpret_cast<const __nv_bfloat16*>(q);
+  const __nv_bfloat16* kk = reinterpret_cast<const __nv_bfloat16*>(K);
+  switch (D) {
+    case 16: return profile_launch_d<16>(qq, kk, nq, C, Hq, Hkv, scale, scores, scratch, cs);
+    case 64: return profile_launch_d<64>(qq, kk, nq, C, Hq, Hkv, scale, scores, scratch, cs);
+    default: return profile_launch_d<128>(qq, kk, nq, C, Hq, Hkv, scale, scores, scratch, cs);
   }
 }
 
