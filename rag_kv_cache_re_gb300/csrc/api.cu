@@ -76,7 +76,7 @@ static const char* kClassNames[KC_COUNT] = {
     "rope_reposition", "anchor_keynorm_topk", "profile_scores", "topn_select", "gather_rows",
     "scatter_kv",      "sparse_causal_attn",  "attn_combine",   "gemm_qkv_rope", "gemm_o_resid",
     "gemm_gate_up_swiglu", "gemm_down_resid", "gemm_other",     "rmsnorm",     "embed_rows",
-    "lm_head_argmax",  "misc"};
+    "lm_head_argmax",  "misc",         "probe_gemm",     "probe_attn"};
 
 struct TimingState {
   std::mutex mu;

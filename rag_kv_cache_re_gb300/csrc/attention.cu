@@ -43,7 +43,9 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
                                                           const int32_t* __restrict__ pos, int n, int T, int Hq,
                                                           int Hkv, int G, int BR, float scale_log2,
                                                           __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                                                          unsigned int* status, int check) {
+                                                          int split_tiles, int max_splits, float* __restrict__ part_o,
+                                                          float2* __restrict__ part_ml, unsigned int* status,
+                                                          int check) {
   using Cfg = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -54,12 +56,19 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
   const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_blocks = (n + BR - 1) / BR;
-  const int rb = n_blocks - 1 - static_cast<int>(blockIdx.x);
+  const int rb = n_blocks - 1 - static_cast<int>(blockIdx.x) / max_splits;
+  const int sp = static_cast<int>(blockIdx.x) % max_splits;
   const int g = blockIdx.y;
   const int row0 = rb * BR;
   const int row_end = min(n, row0 + BR);
   const int kmax = pos[row_end - 1];
-  const int n_tiles = kmax / kKeyTile + 1;
+  const int n_tiles_all = kmax / kKeyTile + 1;
+  // key tiles [t_begin, n_tiles) of this split; a block whose keys fit in one split
+  // writes its output directly, longer blocks write partial sums for the combine
+  const int t_begin = sp * split_tiles;
+  if (t_begin >= n_tiles_all) return;
+  const int n_tiles = min(n_tiles_all, t_begin + split_tiles);
+  const int n_split = min(max_splits, (n_tiles_all + split_tiles - 1) / split_tiles);
 
   const int hh = warp % G, rg = warp / G;
   const int h = g * G + hh;
@@ -108,7 +117,7 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
   constexpr int boxes = D >= 64 ? D / 64 : 1;
   constexpr int box_cols = D >= 64 ? 64 : D;
   auto issue = [&](int t) {
-    const int s = t % kAttnStages;
+    const int s = (t - t_begin) % kAttnStages;
     uint8_t* kb = smem + s * 2 * Cfg::TILE_BYTES;
     uint8_t* vb = kb + Cfg::TILE_BYTES;
     mbar_arrive_expect_tx(&full[s], 2 * Cfg::TILE_BYTES);
@@ -121,7 +130,7 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    for (int t = 0; t < kAttnStages && t < n_tiles; ++t) issue(t);
+    for (int t = t_begin; t < t_begin + kAttnStages && t < n_tiles; ++t) issue(t);
   }
 
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
@@ -130,9 +139,9 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
   for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
   bool ok = true;
-  for (int t = 0; t < n_tiles; ++t) {
-    const int s = t % kAttnStages;
-    const uint32_t par = (t / kAttnStages) & 1;
+  for (int t = t_begin; t < n_tiles; ++t) {
+    const int s = (t - t_begin) % kAttnStages;
+    const uint32_t par = ((t - t_begin) / kAttnStages) & 1;
     if (!mbar_wait(&full[s], par)) {
       flag_status(status, QCF_DEV_TIMEOUT);
       ok = false;
@@ -238,6 +247,24 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  if (n_split > 1) {   // unnormalised partial: O, running max (log2 units) and sum
+    const size_t pstride = static_cast<size_t>(n) * Hq;
+    if (r_lo < row_end) {
+      float* po = part_o + (static_cast<size_t>(sp) * pstride + static_cast<size_t>(r_lo) * Hq + h) * D;
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt)
+        *reinterpret_cast<float2*>(po + dt * 8 + qc) = make_float2(oacc[dt][0], oacc[dt][1]);
+      if ((lane & 3) == 0) part_ml[static_cast<size_t>(sp) * pstride + static_cast<size_t>(r_lo) * Hq + h] = make_float2(m_lo, l_lo);
+    }
+    if (r_hi < row_end) {
+      float* po = part_o + (static_cast<size_t>(sp) * pstride + static_cast<size_t>(r_hi) * Hq + h) * D;
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt)
+        *reinterpret_cast<float2*>(po + dt * 8 + qc) = make_float2(oacc[dt][2], oacc[dt][3]);
+      if ((lane & 3) == 0) part_ml[static_cast<size_t>(sp) * pstride + static_cast<size_t>(r_hi) * Hq + h] = make_float2(m_hi, l_hi);
+    }
+    return;
+  }
   const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
   const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
   const size_t ostride = static_cast<size_t>(Hq) * D;
@@ -257,16 +284,97 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
   }
 }
 
-size_t attn_workspace_size(int, int, int, int, int) { return 0; }
+// Merges the key-range partials of rows whose block was split: one warp per
+// (row, head), splits summed in order (deterministic).
+template <int D>
+__global__ void attn_combine_kernel(const int32_t* __restrict__ pos, int n, int Hq, int BR, int split_tiles,
+                                    int max_splits, const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                                    __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= n * Hq) return;
+  const int row = w / Hq, h = w - row * Hq;
+  const int rb = row / BR;
+  const int row_end = min(n, rb * BR + BR);
+  const int n_tiles_all = pos[row_end - 1] / kKeyTile + 1;
+  const int n_split = min(max_splits, (n_tiles_all + split_tiles - 1) / split_tiles);
+  if (n_split <= 1) return;
+  const size_t pstride = static_cast<size_t>(n) * Hq;
+  float M = -INFINITY;
+  for (int s = 0; s < n_split; ++s) M = fmaxf(M, part_ml[s * pstride + static_cast<size_t>(row) * Hq + h].x);
+  constexpr int PER = (D + 31) / 32;   // elements d = lane + 32 i, d < D
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float L = 0.f;
+  for (int s = 0; s < n_split; ++s) {
+    const float2 ml = part_ml[s * pstride + static_cast<size_t>(row) * Hq + h];
+    if (!(ml.y > 0.f)) continue;
+    const float f = exp2f(ml.x - M);
+    L += ml.y * f;
+    const float* po = part_o + (s * pstride + static_cast<size_t>(row) * Hq + h) * D;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (lane + 32 * i < D) acc[i] += po[lane + 32 * i] * f;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* op = o + (static_cast<size_t>(row) * Hq + h) * D;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (lane + 32 * i < D) op[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+  if (lse && lane == 0) lse[static_cast<size_t>(row) * Hq + h] = (M + log2f(L)) * 0.69314718055994531f;
+}
+
+struct AttnPlan {
+  int G, BR, n_blocks, split_tiles, max_splits;
+};
+
+// Long row blocks are split over key ranges only when the grid is too small to
+// balance by itself (the fused path: few rows, the query block sees every key).
+static AttnPlan plan_attn(int n, int T, int Hq, int Hkv) {
+  AttnPlan p;
+  p.G = Hq / Hkv;
+  p.BR = 16 * (p.G >= 8 ? 1 : 8 / p.G);
+  p.n_blocks = (n + p.BR - 1) / p.BR;
+  const int max_tiles = (T + kKeyTile - 1) / kKeyTile;
+  p.split_tiles = max_tiles;
+  p.max_splits = 1;
+  if (p.n_blocks * Hkv < 4 * num_sms() && max_tiles > 16) {
+    p.max_splits = 4;
+    p.split_tiles = (max_tiles + p.max_splits - 1) / p.max_splits;
+    if (p.split_tiles < 8) p.split_tiles = 8;
+    p.max_splits = (max_tiles + p.split_tiles - 1) / p.split_tiles;
+  }
+  return p;
+}
+
+size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D) {
+  if (n <= 0 || T <= 0 || Hkv <= 0 || Hq % Hkv) return 0;
+  const AttnPlan p = plan_attn(n, T, Hq, Hkv);
+  if (p.max_splits <= 1) return 0;
+  return align_up(static_cast<size_t>(p.max_splits) * n * Hq * D * sizeof(float), 256) +
+         align_up(static_cast<size_t>(p.max_splits) * n * Hq * sizeof(float2), 256);
+}
 
 template <int D>
 static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,
                                 const __nv_bfloat16* V, int T, int Hq, int Hkv, float scale, __nv_bfloat16* o,
-                                float* lse, cudaStream_t st) {
+                                float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc) {
   using Cfg = AttnCfg<D>;
-  const int G = Hq / Hkv;
-  const int BR = 16 * (G >= 8 ? 1 : 8 / G);
+  const AttnPlan plan = plan_attn(n, T, Hq, Hkv);
+  const int G = plan.G;
+  const int BR = plan.BR;
   const int warps = G * (BR / 16);
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  if (plan.max_splits > 1) {
+    const size_t ob = align_up(static_cast<size_t>(plan.max_splits) * n * Hq * D * sizeof(float), 256);
+    if (!ws || ws_bytes < attn_workspace_size(n, T, Hq, Hkv, D))
+      return set_error(QCF_ERR_WORKSPACE, "sparse_causal_attn: workspace %zu < %zu", ws_bytes,
+                       attn_workspace_size(n, T, Hq, Hkv, D));
+    part_o = static_cast<float*>(ws);
+    part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + ob);
+  }
   CUtensorMap tk, tv;
   const uint64_t width = static_cast<uint64_t>(Hkv) * D;
   const uint32_t box_cols = D >= 64 ? 64 : D;
@@ -280,25 +388,32 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
     attr = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   });
   if (attr != cudaSuccess) return cuda_error(attr, "sparse_causal_attn: smem attribute");
-  dim3 grid((n + BR - 1) / BR, Hkv);
+  dim3 grid(plan.n_blocks * plan.max_splits, Hkv);
   const float scale_log2 = scale * 1.4426950408889634f;
-  LaunchScope ls(KC_ATTN, st);
-  sparse_attn_kernel<D><<<grid, warps * 32, Cfg::SMEM_BYTES, st>>>(tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o,
-                                                                    lse, device_status_ptr(), check_enabled() ? 1 : 0);
+  {
+    LaunchScope ls(kc, st);
+    sparse_attn_kernel<D><<<grid, warps * 32, Cfg::SMEM_BYTES, st>>>(
+        tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o, lse, plan.split_tiles, plan.max_splits, part_o, part_ml,
+        device_status_ptr(), check_enabled() ? 1 : 0);
+  }
+  if (plan.max_splits > 1) {
+    LaunchScope ls(kc == KC_ATTN ? KC_ATTN_COMBINE : kc, st);
+    const int warps_total = n * Hq;
+    attn_combine_kernel<D><<<(warps_total + 7) / 8, 256, 0, st>>>(pos, n, Hq, BR, plan.split_tiles, plan.max_splits, part_o,
+                                                                  part_ml, o, lse);
+  }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "sparse_causal_attn: launch");
 }
 
 qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K, const __nv_bfloat16* V,
                        int T, int Hq, int Hkv, int D, float scale, __nv_bfloat16* o, float* lse, void* ws,
-                       size_t ws_bytes, cudaStream_t st) {
-  (void)ws;
-  (void)ws_bytes;
+                       size_t ws_bytes, cudaStream_t st, KernelClass kc) {
   if (n <= 0) return QCF_OK;
   switch (D) {
-    case 16: return attn_launch_d<16>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, st);
-    case 64: return attn_launch_d<64>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, st);
-    case 128: return attn_launch_d<128>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, st);
+    case 16: return attn_launch_d<16>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc);
+    case 64: return attn_launch_d<64>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc);
+    case 128: return attn_launch_d<128>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc);
     default: return set_error(QCF_ERR_SHAPE, "sparse_causal_attn: head dim %d unsupported", D);
   }
 }

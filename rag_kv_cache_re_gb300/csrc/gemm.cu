@@ -37,7 +37,8 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+  static constexpr int EPI_BYTES = 4 * 32 * 33 * 4;   // one 32x32 fp32 transpose tile per epilogue warp
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -110,8 +111,10 @@ __device__ __forceinline__ void load_f32x(const float* src, float* v, int n) {
 }
 
 // Epilogue of one tile for the calling thread's row.  `row` < M is checked here.
+// `tile` is this warp's 32x33 fp32 staging area in shared memory.
 template <int BN, int EPI, int HD>
-__device__ __forceinline__ void tile_epilogue(const ChunkLoader& ld, const EpiParams& ep, int row, int M, int n0) {
+__device__ __forceinline__ void tile_epilogue(const ChunkLoader& ld, const EpiParams& ep, int row, int M, int n0,
+                                              float* tile) {
   const bool live = row < M;
   if constexpr (EPI == EPI_STORE_BF16) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ep.out);
@@ -122,20 +125,51 @@ __device__ __forceinline__ void tile_epilogue(const ChunkLoader& ld, const EpiPa
       if (live) store_bf16x32(out + static_cast<size_t>(row) * ep.ldo + n0 + c * 32, v);
     }
   } else if constexpr (EPI == EPI_ADD_F32) {
+    // The accumulator arrives one row per thread; the residual x is read and
+    // written with 4 full 128-byte row segments per warp instruction by passing
+    // each 32x32 chunk through shared memory.  x of the next chunk is loaded
+    // ahead while the current one is transposed and added.
+    const int lane = threadIdx.x & 31;
+    const int row0 = row - lane;                 // first row of this warp's 32
+    const int rr = lane >> 3, cq = (lane & 7) * 4;
     float* out = static_cast<float*>(ep.out);
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    auto xptr = [&](int c, int i) {
+      return reinterpret_cast<float4*>(out + static_cast<size_t>(row0 + i * 4 + rr) * ep.ldo + n0 + c * 32 + cq);
+    };
+    auto row_ok = [&](int i) { return row0 + i * 4 + rr < M; };
+    float4 xa[8], xb[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (row_ok(i)) xa[i] = *xptr(0, i);
+    auto add_store = [&](int c, const float4* xr) {
       float v[32];
       ld(c, v);
-      if (live) {
-        float4* o = reinterpret_cast<float4*>(out + static_cast<size_t>(row) * ep.ldo + n0 + c * 32);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float4 t = o[i];
-          t.x += v[4 * i]; t.y += v[4 * i + 1]; t.z += v[4 * i + 2]; t.w += v[4 * i + 3];
-          o[i] = t;
+      for (int j = 0; j < 32; ++j) tile[lane * 33 + j] = v[j];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float* tr = tile + (i * 4 + rr) * 33 + cq;
+        if (row_ok(i)) {
+          float4 t = xr[i];
+          t.x += tr[0]; t.y += tr[1]; t.z += tr[2]; t.w += tr[3];
+          *xptr(c, i) = t;
         }
       }
+      __syncwarp();
+    };
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; c += 2) {   // BN / 32 is even
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (row_ok(i)) xb[i] = *xptr(c + 1, i);
+      add_store(c, xa);
+      if (c + 2 < BN / 32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (row_ok(i)) xa[i] = *xptr(c + 2, i);
+      }
+      add_store(c + 1, xb);
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ep.out);
@@ -266,6 +300,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* epi_tiles = reinterpret_cast<float*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES + 1024);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_m = (M + kBM - 1) / kBM;
@@ -375,6 +410,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    float* my_tile = epi_tiles + (warp - 2) * (32 * 33);
     int local = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
       int mt, nt, sp;
@@ -394,7 +430,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int n0 = nt * BN;
       if (splits == 1) {
         ChunkLoader ld{taddr, nullptr, 1, 0};
-        tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0);
+        tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -428,7 +464,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __threadfence();
           ChunkLoader ld{0u, ws_part + static_cast<size_t>(tile) * splits * stride + static_cast<size_t>(row_in_tile) * BN,
                          splits, stride};
-          tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0);
+          tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
         }
       }
     }
@@ -449,38 +485,42 @@ struct GemmPlan {
   int tiles;
 };
 
-// Chooses the tile width BN and the number of k splits with a small cost model:
-// time = max(rounds of units x per-unit time, weight bytes / HBM bandwidth of the
-// SMs that are busy).  A unit's main loop runs at the SM's tensor rate (narrower
-// tiles lose some of it to operand traffic); a split adds the fp32 partial it
-// writes and the fixup that reads the partials back.  Small-M GEMMs (the probe's
-// 64 rows) stream weights, so they split K to keep every SM loading; the 832-row
-// recompute GEMMs do not split.
+// Chooses the tile width BN and the number of k splits from measurements on GB300:
+//  * M > 128 (the recompute GEMMs): tensor-bound; the widest tile (BN = 256) and
+//    no k split were fastest on every 8B layer shape (splits write fp32 partials
+//    whose traffic and fixup cost more than the waves they fill).
+//  * M <= 128 (the probe's query rows): weight-bound; one busy SM streams about
+//    45 GB/s of weights through the TMA ring, so time ~ rounds x bytes per unit /
+//    45 GB/s, plus ~10 us and the partial traffic when K is split.
 static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
   const int sms = num_sms();
   const int tiles_m = (M + kBM - 1) / kBM;
   const int kb = K / kBK;
-  const double sm_flops = 14.0e12;   // sustained dense bf16 per SM
-  const double hbm = 6.5e12;         // bytes/s
-  const double part_bw = 80.0e9;     // bytes/s one SM writes and reads its partials at
+  auto valid = [&](int bn) {
+    if (N % bn) return false;
+    if (epi == EPI_SWIGLU && bn % 128) return false;
+    if (epi == EPI_QKV_ROPE && bn % head_dim) return false;
+    return true;
+  };
+  const int cands[3] = {256, 128, 64};
+  if (tiles_m >= 2) {
+    for (int bn : cands)
+      if (valid(bn)) return GemmPlan{bn, 1, tiles_m * (N / bn)};
+  }
   GemmPlan best{64, 1, tiles_m * (N / 64)};
   double best_t = 1e30;
-  const int cands[3] = {256, 128, 64};
   for (int bn : cands) {
-    if (N % bn) continue;
-    if (epi == EPI_SWIGLU && bn % 128) continue;
-    if (epi == EPI_QKV_ROPE && bn % head_dim) continue;
-    const double eff = bn == 256 ? 1.0 : (bn == 128 ? 0.85 : 0.6);
+    if (!valid(bn)) continue;
+    const double stream = bn == 64 ? 28.0e9 : 45.0e9;   // bytes/s one SM pulls with this tile's ring
     const int tiles = tiles_m * (N / bn);
     for (int s = 1; s <= 8; ++s) {
-      if (s > 1 && kb / s < 8) break;
+      if (s > 1 && kb / s < 4) break;
       const int units = tiles * s;
       const int rounds = (units + sms - 1) / sms;
-      double t_unit = 2.0 * kBM * bn * (static_cast<double>(K) / s) / (sm_flops * eff) + 1.0e-6;
-      if (s > 1) t_unit += 2.0 * kBM * bn * 4.0 / part_bw + 2.0e-6;
-      const double busy = units < sms ? static_cast<double>(units) / sms : 1.0;
-      const double t_mem = (static_cast<double>(N) * K * 2.0 + static_cast<double>(M) * K * 2.0) / (hbm * busy);
-      const double t = std::max(rounds * t_unit, t_mem);
+      const double unit_bytes = static_cast<double>(bn) * (static_cast<double>(K) / s) * 2.0;
+      const double unit_flops = 2.0 * kBM * bn * (static_cast<double>(K) / s);
+      double t = rounds * std::max(unit_bytes / stream, unit_flops / 11.0e12 + 1.0e-6);
+      if (s > 1) t += 10.0e-6 + units * (kBM * bn * 4.0 * 2.0) / 1.5e12;
       if (t < best_t * 0.98) {
         best_t = t;
         best = GemmPlan{bn, s, tiles};

@@ -45,6 +45,8 @@ struct LayerBufs {
   __nv_bfloat16* act;
   void* gemm_ws;
   size_t gemm_ws_bytes;
+  void* attn_ws;
+  size_t attn_ws_bytes;
 };
 
 static size_t layer_ws_bytes(const qcf_dims& d, int n, int T) {
@@ -65,7 +67,8 @@ static bool carve_layer(Carve& c, const qcf_dims& d, int n, int T, LayerBufs* b)
   b->act = c.take<__nv_bfloat16>(static_cast<size_t>(n) * d.ffn_padded);
   b->gemm_ws_bytes = gemm_ws_layer(d, n);
   b->gemm_ws = c.take<uint8_t>(b->gemm_ws_bytes);
-  c.take<uint8_t>(attn_workspace_size(n, T, d.n_heads, d.n_kv_heads, d.head_dim));
+  b->attn_ws_bytes = attn_workspace_size(n, T, d.n_heads, d.n_kv_heads, d.head_dim);
+  b->attn_ws = c.take<uint8_t>(b->attn_ws_bytes);
   return c.ok;
 }
 
@@ -91,9 +94,11 @@ static qcf_status check_model(const qcf_model* m, const char* who) {
 }
 
 // One decoder layer on rows x (validated by the caller).
+// `probe` only selects the timing classes (the probe's 64-row GEMMs are weight-bound
+// and are accounted apart from the recompute GEMMs).
 static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, const int32_t* rope_pos,
                                      const int32_t* cache_row, int n, __nv_bfloat16* Kc, __nv_bfloat16* Vc, int T,
-                                     const LayerBufs& b, cudaStream_t st) {
+                                     const LayerBufs& b, cudaStream_t st, bool probe = false) {
   const qcf_dims& d = m->dims;
   const qcf_layer_weights& w = m->layers[layer];
   const int D = d.head_dim, Hq = d.n_heads, Hkv = d.n_kv_heads;
@@ -114,16 +119,16 @@ static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, co
   ep.max_pos = m->rope.max_pos;
   ep.status = device_status_ptr();
   qcf_status s = gemm_launch(EPI_QKV_ROPE, b.h, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
-                             (Hq + 2 * Hkv) * D, ep, b.gemm_ws, b.gemm_ws_bytes, st, KC_GEMM_QKV);
+                             (Hq + 2 * Hkv) * D, ep, b.gemm_ws, b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_QKV);
   if (s != QCF_OK) return s;
-  s = attn_launch(b.q, cache_row, n, Kc, Vc, T, Hq, Hkv, D, 1.0f / sqrtf(static_cast<float>(D)), b.o, nullptr, nullptr,
-                  0, st);
+  s = attn_launch(b.q, cache_row, n, Kc, Vc, T, Hq, Hkv, D, 1.0f / sqrtf(static_cast<float>(D)), b.o, nullptr, b.attn_ws,
+                  b.attn_ws_bytes, st, probe ? KC_ATTN_PROBE : KC_ATTN);
   if (s != QCF_OK) return s;
   EpiParams eo{};
   eo.out = x;
   eo.ldo = d.d_model;
   s = gemm_launch(EPI_ADD_F32, b.o, n, Hq * D, reinterpret_cast<const __nv_bfloat16*>(w.w_o), d.d_model, eo, b.gemm_ws,
-                  b.gemm_ws_bytes, st, KC_GEMM_O);
+                  b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_O);
   if (s != QCF_OK) return s;
   e = launch_rmsnorm(x, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_mlp), d.eps, b.h, st);
   if (e != cudaSuccess) return cuda_error(e, "layer: rmsnorm");
@@ -131,13 +136,13 @@ static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, co
   eg.out = b.act;
   eg.ldo = d.ffn_padded;
   s = gemm_launch(EPI_SWIGLU, b.h, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_gu), 2 * d.ffn_padded, eg,
-                  b.gemm_ws, b.gemm_ws_bytes, st, KC_GEMM_GU);
+                  b.gemm_ws, b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_GU);
   if (s != QCF_OK) return s;
   EpiParams edn{};
   edn.out = x;
   edn.ldo = d.d_model;
   return gemm_launch(EPI_ADD_F32, b.act, n, d.ffn_padded, reinterpret_cast<const __nv_bfloat16*>(w.w_down), d.d_model,
-                     edn, b.gemm_ws, b.gemm_ws_bytes, st, KC_GEMM_DOWN);
+                     edn, b.gemm_ws, b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_DOWN);
 }
 
 // ------------------------------------------------------------------ small helper kernels
@@ -232,6 +237,9 @@ static bool carve_request(Carve& c, const qcf_dims& d, int C, int Q, int nA, int
   r->lb.act = c.take<__nv_bfloat16>(static_cast<size_t>(nmax) * d.ffn_padded);
   r->lb.gemm_ws_bytes = std::max(gemm_ws_layer(d, ns), gemm_ws_layer(d, Q));
   r->lb.gemm_ws = c.take<uint8_t>(r->lb.gemm_ws_bytes);
+  r->lb.attn_ws_bytes = std::max(attn_workspace_size(ns, T, d.n_heads, d.n_kv_heads, d.head_dim),
+                                 attn_workspace_size(Q, nA + Q, d.n_heads, d.n_kv_heads, d.head_dim));
+  r->lb.attn_ws = c.take<uint8_t>(r->lb.attn_ws_bytes);
   r->x = c.take<float>(static_cast<size_t>(nmax) * d.d_model);
   r->rows = c.take<int32_t>(ns);
   r->probe_pos = c.take<int32_t>(Q);
@@ -476,7 +484,7 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
                                                                       d.head_dim, m->rope.cos, m->rope.sin, co, rl.pK,
                                                                       rl.pV);
       }
-      s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK, rl.pV, nA + Q, rl.lb, cs);
+      s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK, rl.pV, nA + Q, rl.lb, cs, true);
       if (s != QCF_OK) return s;
     }
   }
@@ -499,7 +507,7 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
     ep.max_pos = m->rope.max_pos;
     ep.status = device_status_ptr();
     s = gemm_launch(EPI_QKV_ROPE, rl.lb.h, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
-                    d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_QKV);
+                    d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_PROBE);
     if (s != QCF_OK) return s;
   }
   // profile the re-rotated critical-layer keys and select

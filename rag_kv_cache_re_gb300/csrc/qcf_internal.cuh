@@ -30,7 +30,7 @@ unsigned int* device_status_ptr();
 enum KernelClass {
   KC_ROPE = 0, KC_ANCHOR, KC_PROFILE, KC_TOPN, KC_GATHER, KC_SCATTER, KC_ATTN, KC_ATTN_COMBINE,
   KC_GEMM_QKV, KC_GEMM_O, KC_GEMM_GU, KC_GEMM_DOWN, KC_GEMM_OTHER, KC_RMSNORM, KC_EMBED,
-  KC_LMHEAD, KC_MISC, KC_COUNT
+  KC_LMHEAD, KC_MISC, KC_GEMM_PROBE, KC_ATTN_PROBE, KC_COUNT
 };
 struct LaunchScope {
   LaunchScope(KernelClass kc, cudaStream_t s);
@@ -88,7 +88,7 @@ cudaError_t launch_reposition(const __nv_bfloat16* src, __nv_bfloat16* dst, int6
 size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D);
 qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,
                        const __nv_bfloat16* V, int T, int Hq, int Hkv, int D, float scale, __nv_bfloat16* o,
-                       float* lse, void* ws, size_t ws_bytes, cudaStream_t st);
+                       float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc = KC_ATTN);
 
 // ------------------------------------------------------------------ device side
 
