@@ -420,6 +420,78 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# ----------------------------------------------------------------- kernel sweep (profile + top-N, attention)
+
+# Exponential ceiling of the profile kernel: 152 SMs x 16 MUFU.EX2 per SM per clock
+# (4 per sub-partition) x the 2070 MHz maximum SM clock.
+EXP_PEAK_PER_S = 152 * 16 * 2.07e9
+
+
+def run_sweep(args):
+    """Times profile+top-N and sparse causal attention on the kernel-sweep shapes
+    (context 4k..128k, 64 query rows, 32 Q / 8 KV heads, head dim 128, 5..50 %
+    selected, uniform or clustered), L2 flushed before every timed launch."""
+    from rag_kv_cache_re_gb300 import qcf as Q
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    Hq, Hkv, D = qd.SWEEP_HEADS
+    nq = qd.SWEEP_QUERY
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    reps = max(3, args.steps)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.median(ms)
+
+    for C in qd.SWEEP_CONTEXTS:
+        t = qd.sweep_tensors(C + nq, n_query=nq, device=str(device))
+        K, V, q = t["K"], t["V"], t["Q"]
+        Kc = K[:C]
+        ms_prof = timed(lambda: Q.qcf_profile_scores(q, Kc, 1.0))
+        scores = Q.qcf_profile_scores(q, Kc, 1.0)
+        kbytes = C * Hkv * D * 2
+        exps = 2.0 * nq * Hq * C
+        for frac_bp in qd.SWEEP_FRACTIONS_BP:
+            N = (frac_bp * C + 9999) // 10000
+            ms_topn = timed(lambda: Q.qcf_topn_select(scores, N))
+            for pattern in ("uniform", "clusters"):
+                pos = np.concatenate([qd.selected_indices(C, N, pattern), np.arange(C, C + nq)]).astype(np.int32)
+                pos_d = torch.from_numpy(pos).to(device)
+                qa = qd.normal_bf16((len(pos), Hq, D), 1.0 / math.sqrt(D), 9, str(device))
+                ms_attn = timed(lambda: Q.qcf_sparse_causal_attn(qa, pos_d, K, V, 1.0))
+                aflops = 4.0 * Hq * D * float(np.sum(pos.astype(np.float64) + 1))
+                abytes = 2.0 * (C + nq) * Hkv * D * 2
+                print(json.dumps({
+                    "sweep": {"context": C, "selected_bp": frac_bp, "pattern": pattern, "N": int(N), "query_rows": nq},
+                    "profile_topn_ms": round(ms_prof + ms_topn, 4), "profile_ms": round(ms_prof, 4),
+                    "topn_ms": round(ms_topn, 4),
+                    "profile_roofline": {"bound": "alu", "achieved": round(exps / (ms_prof * 1e-3) / 1e12, 3),
+                                         "peak": round(EXP_PEAK_PER_S / 1e12, 3), "unit": "T exp/s",
+                                         "frac": round(exps / (ms_prof * 1e-3) / EXP_PEAK_PER_S, 4),
+                                         "hbm_gbs": round(kbytes / (ms_prof * 1e-3) / 1e9, 1),
+                                         "hbm_frac": round(kbytes / (ms_prof * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+                    "attn_ms": round(ms_attn, 4),
+                    "attn_roofline": {"bound": "tensor", "achieved": round(aflops / (ms_attn * 1e-3) / 1e12, 1),
+                                      "peak": peaks["bf16"], "unit": "TFLOP/s",
+                                      "frac": round(aflops / (ms_attn * 1e-3) / 1e12 / peaks["bf16"], 4),
+                                      "hbm_gbs": round(abytes / (ms_attn * 1e-3) / 1e9, 1)},
+                    "l2": "flushed (256 MB write) before every timed launch"}), flush=True)
+                del qa, pos_d
+        del t, K, V, q, scores
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -428,11 +500,14 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["qcf", "reference"], default="qcf")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time the kernel-sweep shapes instead of the request")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_gpu(args)
 

@@ -161,21 +161,21 @@ def causal_attention(q: np.ndarray, bound: np.ndarray, K: np.ndarray, V: np.ndar
     n, Hq, D = q.shape
     T, Hkv, _ = K.shape
     G = Hq // Hkv
-    head_map = np.arange(Hq) // G
-    Kh = K.astype(F64)[:, head_map, :].transpose(1, 2, 0)   # [Hq][D][T]
-    Vh = V.astype(F64)[:, head_map, :].transpose(1, 0, 2)   # [Hq][T][D]
     keys = np.arange(T)
     out = np.empty((n, Hq, D), dtype=F32)
-    for r0 in range(0, n, block):
-        r1 = min(n, r0 + block)
-        qb = q[r0:r1].astype(F64).transpose(1, 0, 2)         # [Hq][b][D]
-        s = np.matmul(qb, Kh) * scale                          # [Hq][b][T]
-        hidden = keys[None, None, :] > np.asarray(bound[r0:r1])[None, :, None]
-        s = np.where(hidden, -np.inf, s)
-        m = s.max(axis=-1, keepdims=True)
-        p = np.exp(s - m)
-        p /= p.sum(axis=-1, keepdims=True)
-        out[r0:r1] = np.matmul(p, Vh).transpose(1, 0, 2).astype(F32)
+    for g in range(Hkv):                      # one KV head at a time keeps memory at O(T*D)
+        Kg = K[:, g, :].astype(F64)           # [T][D]
+        Vg = V[:, g, :].astype(F64)
+        for h in range(g * G, (g + 1) * G):
+            for r0 in range(0, n, block):
+                r1 = min(n, r0 + block)
+                s = (q[r0:r1, h, :].astype(F64) @ Kg.T) * scale          # [b][T]
+                hidden = keys[None, :] > np.asarray(bound[r0:r1])[:, None]
+                s = np.where(hidden, -np.inf, s)
+                m = s.max(axis=-1, keepdims=True)
+                p = np.exp(s - m)
+                p /= p.sum(axis=-1, keepdims=True)
+                out[r0:r1, h, :] = (p @ Vg).astype(F32)
     return out
 
 

@@ -66,28 +66,36 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
   }
 }
 
+// fp32 partial tiles in the workspace are stored column-quad-major: element
+// (row, col) of a 128 x BN slot sits at ((col / 4) * 128 + row) * 4 + col % 4, so
+// a warp (32 consecutive rows) moving one float4 each touches 512 contiguous bytes.
+__device__ __forceinline__ size_t part_idx(int row, int quad) {
+  return (static_cast<size_t>(quad) * kBM + row) * 4;
+}
+
 // Loads 32 accumulator columns [32c, 32c+32) of this thread's row, either from
 // TMEM (direct) or as the in-order sum of the split-K partials in the workspace.
 struct ChunkLoader {
   uint32_t taddr;       // TMEM address of (row quarter, column 0) of the accumulator
-  const float* part;    // first partial of this tile's row, or nullptr for TMEM
+  const float* part;    // the tile's first partial slot, or nullptr for TMEM
   int splits;
-  int part_stride;      // floats between consecutive splits' partials
+  int part_stride;      // floats between consecutive splits' slots
+  int row;              // row within the tile
   __device__ __forceinline__ void operator()(int c, float* v) const {
     if (part == nullptr) {
       tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 t = __ldcg(reinterpret_cast<const float4*>(part + c * 32 + i));
-        v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+      for (int q = 0; q < 8; ++q) {
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(part + part_idx(row, c * 8 + q)));
+        v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
       }
       for (int s = 1; s < splits; ++s) {
         const float* p = part + static_cast<size_t>(s) * part_stride;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 t = __ldcg(reinterpret_cast<const float4*>(p + c * 32 + i));
-          v[i] += t.x; v[i + 1] += t.y; v[i + 2] += t.z; v[i + 3] += t.w;
+        for (int q = 0; q < 8; ++q) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(p + part_idx(row, c * 8 + q)));
+          v[4 * q] += t.x; v[4 * q + 1] += t.y; v[4 * q + 2] += t.z; v[4 * q + 3] += t.w;
         }
       }
     }
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row = mt * kBM + row_in_tile;
       const int n0 = nt * BN;
       if (splits == 1) {
-        ChunkLoader ld{taddr, nullptr, 1, 0};
+        ChunkLoader ld{taddr, nullptr, 1, 0, row_in_tile};
         tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
         tc_fence_before();
         __syncwarp();
@@ -437,14 +445,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else {
         const int tile = nt * tiles_m + mt;
         const int stride = kBM * BN;
-        float* mine = ws_part + (static_cast<size_t>(tile) * splits + sp) * stride + static_cast<size_t>(row_in_tile) * BN;
+        float* mine = ws_part + (static_cast<size_t>(tile) * splits + sp) * stride;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
-          float4* d = reinterpret_cast<float4*>(mine + c * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(mine + part_idx(row_in_tile, c * 8 + q)) =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
         tc_fence_before();
         __syncwarp();
@@ -462,8 +471,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         epi_bar();
         if (last) {
           __threadfence();
-          ChunkLoader ld{0u, ws_part + static_cast<size_t>(tile) * splits * stride + static_cast<size_t>(row_in_tile) * BN,
-                         splits, stride};
+          ChunkLoader ld{0u, ws_part + static_cast<size_t>(tile) * splits * stride, splits, stride, row_in_tile};
           tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
         }
       }
@@ -504,6 +512,11 @@ static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
   };
   const int cands[3] = {256, 128, 64};
   if (tiles_m >= 2) {
+    // Widest tile, whole k range.  Measured on the 8B recompute shapes: uniform
+    // k splits (lockstep or stream-K) lost to the plain persistent grid because the
+    // split epilogue (fenced partial write, last-CTA fixup) outlasts a short k
+    // slice's main loop, and stream-K ranges break the m tiles' shared walk over
+    // a weight tile (L2 reuse).
     for (int bn : cands)
       if (valid(bn)) return GemmPlan{bn, 1, tiles_m * (N / bn)};
   }

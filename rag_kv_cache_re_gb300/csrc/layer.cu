@@ -454,10 +454,19 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
     }
     return cudaSuccess;
   };
+  // Each layer's chunk keys are re-rotated to their offsets on the copy stream right
+  // after they land, so the rotation overlaps the recompute of earlier layers.
+  auto rotate_layer = [&](int l) -> cudaError_t {
+    __nv_bfloat16* Kl = reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]);
+    return launch_reposition(Kl, Kl, C, d.n_kv_heads, d.head_dim, seg_start.data(), seg_delta.data(), r->n_chunks,
+                             &m->rope, xs);
+  };
   if ((e = copy_layer(crit, true, false)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: critical-layer copy");
+  if ((e = rotate_layer(crit)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: reposition");
   if ((e = cudaEventRecord(ev_crit, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
   for (int l = 0; l < L; ++l) {
     if ((e = copy_layer(l, l != crit, true)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: layer copy");
+    if (l != crit && (e = rotate_layer(l)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: reposition");
     if ((e = cudaEventRecord(ev_layer[l], xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
   }
 
@@ -513,9 +522,6 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
   // profile the re-rotated critical-layer keys and select
   if ((e = cudaStreamWaitEvent(cs, ev_crit, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
   __nv_bfloat16* Kcrit = reinterpret_cast<__nv_bfloat16*>(out->K_layers[crit]);
-  if ((e = launch_reposition(Kcrit, Kcrit, C, d.n_kv_heads, d.head_dim, seg_start.data(), seg_delta.data(), r->n_chunks,
-                             &m->rope, cs)) != cudaSuccess)
-    return cuda_error(e, "qcf_request_prefill: reposition");
   s = qcf_profile_scores(reinterpret_cast<const qcf_bf16*>(q_crit), reinterpret_cast<const qcf_bf16*>(Kcrit), Q, C,
                          d.n_heads, d.n_kv_heads, d.head_dim, 1.0f / sqrtf(static_cast<float>(d.head_dim)), scores,
                          rl.prof_ws, rl.prof_ws_bytes, cs);
@@ -541,11 +547,6 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
     if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
     __nv_bfloat16* Kl = reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]);
     __nv_bfloat16* Vl = reinterpret_cast<__nv_bfloat16*>(out->V_layers[l]);
-    if (l != crit) {
-      if ((e = launch_reposition(Kl, Kl, C, d.n_kv_heads, d.head_dim, seg_start.data(), seg_delta.data(), r->n_chunks,
-                                 &m->rope, cs)) != cudaSuccess)
-        return cuda_error(e, "qcf_request_prefill: reposition");
-    }
     s = layer_forward_impl(m, l, rl.x, rl.rows, rl.rows, ns, Kl, Vl, T, rl.lb, cs);
     if (s != QCF_OK) return s;
   }

@@ -129,6 +129,7 @@ class FusedRequest:
         self.model, self.store = model, store
         chunks = [store.chunks[int(c)] for c in chunk_ids]
         self.chunks = chunks
+        self.chunk_ids = [int(c) for c in chunk_ids]
         lens = [len(c.tokens) for c in chunks]
         self.C = int(sum(lens))
         self.Q = len(query_ids)

@@ -200,7 +200,7 @@ def test_sparse_causal_attn(Q, T, n, Hq, Hkv, D, pattern):
 
 # ----------------------------------------------------------------- dense pieces
 
-@pytest.mark.parametrize("M,N,K", [(23, 192, 64), (1, 64, 64), (300, 384, 192), (832, 6144, 4096),
+@pytest.mark.parametrize("M,N,K", [(23, 192, 64), (1, 64, 64), (300, 384, 192), (832, 6144, 4096), (832, 4096, 4096), (832, 28672, 4096),
                                    (64, 4096, 14336), (832, 4096, 14336), (200, 28672, 256)])
 def test_linear_store_and_add(Q, M, N, K):
     A = qd.normal_bf16((M, K), 1.0, 31, DEV)
