@@ -205,9 +205,11 @@ qcf_status qcf_sparse_causal_attn(const qcf_bf16* q, const int32_t* pos, int n, 
  * layout) on tcgen05 tensor cores with TMEM accumulators.
  *   epilogue QCF_EPI_STORE_BF16: out is bf16 [M][N]
  *   epilogue QCF_EPI_ADD_F32:    out is fp32 [M][N] and receives out += A W^T
+ *   | QCF_LINEAR_W_KN:           W is stored [K][N] instead (out = A * W)
  * K % 64 == 0, N % 64 == 0. */
 #define QCF_EPI_STORE_BF16 0
 #define QCF_EPI_ADD_F32 1
+#define QCF_LINEAR_W_KN 0x10
 size_t qcf_linear_workspace_size(int M, int N, int K);
 qcf_status qcf_linear(const qcf_bf16* A, int M, int K, const qcf_bf16* W, int N, int epilogue, void* out,
                       void* ws, size_t ws_bytes, void* stream);

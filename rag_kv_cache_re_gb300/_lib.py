@@ -18,6 +18,7 @@ QCF_DEV_TIMEOUT = 0x1
 QCF_DEV_BAD_INDEX = 0x2
 QCF_EPI_STORE_BF16 = 0
 QCF_EPI_ADD_F32 = 1
+QCF_LINEAR_W_KN = 0x10
 
 
 class QcfError(RuntimeError):

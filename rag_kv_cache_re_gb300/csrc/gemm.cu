@@ -293,7 +293,7 @@ __device__ __forceinline__ void tile_epilogue(const ChunkLoader& ld, const EpiPa
   }
 }
 
-template <int BN, int EPI, int HD>
+template <int BN, int EPI, int HD, bool BMN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
                         int N, int K, int splits, const EpiParams ep, float* __restrict__ ws_part,
@@ -364,7 +364,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* a_s = smem + stage * Cfg::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
           tma_load_2d(a_s, &tmA, &full[stage], kb * kBK, mt * kBM);
-          tma_load_2d(a_s + Cfg::A_BYTES, &tmB, &full[stage], kb * kBK, nt * BN);
+          if constexpr (BMN) {   // W stored [K][N]: BN/64 boxes of 64 K rows x 64 N columns
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(a_s + Cfg::A_BYTES + j * (kBK * 128), &tmB, &full[stage], nt * BN + j * 64, kb * kBK);
+          } else {
+            tma_load_2d(a_s + Cfg::A_BYTES, &tmB, &full[stage], kb * kBK, nt * BN);
+          }
           if (++stage == Cfg::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -374,7 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, BMN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -402,8 +408,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t b_addr = a_addr + Cfg::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            umma_f16(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
-                     (kb > kb0 || kk > 0) ? 1u : 0u);
+            // K-major: 16 K elements are 32 bytes along the swizzled row; MN-major:
+            // 16 K indices are two 1024-byte atoms
+            const uint64_t bdesc = BMN ? sdesc_mnmajor_sw128(b_addr + kk * 2048, kBK * 128)
+                                       : sdesc_kmajor_sw128(b_addr + kk * 32);
+            umma_f16(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32), bdesc, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == Cfg::STAGES) {
@@ -562,11 +571,11 @@ size_t gemm_workspace_size(int M, int N, int K) {
   return need + 256;
 }
 
-template <int BN, int EPI, int HD>
+template <int BN, int EPI, int HD, bool BMN = false>
 static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int splits,
                              const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st, int units) {
   using Cfg = GemmCfg<BN>;
-  auto kern = gemm_tcgen05_kernel<BN, EPI, HD>;
+  auto kern = gemm_tcgen05_kernel<BN, EPI, HD, BMN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -580,11 +589,24 @@ static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M
 }
 
 template <int BN>
+static qcf_status dispatch_kn(EpiKind epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+                              int splits, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
+                              int units) {
+  if constexpr (BN >= 64) {
+    if (epi == EPI_STORE_BF16)
+      return launch_cfg<BN, EPI_STORE_BF16, 0, true>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+    if (epi == EPI_ADD_F32)
+      return launch_cfg<BN, EPI_ADD_F32, 0, true>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+  }
+  return set_error(QCF_ERR_UNSUPPORTED, "gemm: [K][N] weights support the store and add epilogues only");
+}
+
+template <int BN>
 static qcf_status dispatch_epi(EpiKind epi, int hd, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
                                int splits, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
                                int units) {
   switch (epi) {
-    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0, false>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
     case EPI_ADD_F32: return launch_cfg<BN, EPI_ADD_F32, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
     case EPI_SWIGLU:
       if constexpr (BN >= 128) return launch_cfg<BN, EPI_SWIGLU, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
@@ -600,7 +622,7 @@ static qcf_status dispatch_epi(EpiKind epi, int hd, const CUtensorMap& ta, const
 }
 
 qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const __nv_bfloat16* W, int N,
-                       const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc) {
+                       const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc, bool w_kn) {
   if (M <= 0) return QCF_OK;
   if (K % kBK || N % 64 || K <= 0 || N <= 0) return set_error(QCF_ERR_SHAPE, "gemm: K=%d N=%d (K%%64, N%%64 required)", K, N);
   const int hd = epi == EPI_QKV_ROPE ? ep.D : 16;
@@ -617,11 +639,19 @@ qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const 
     if (e != cudaSuccess) return cuda_error(e, "gemm: counter reset");
   }
   CUtensorMap ta, tb;
-  if (!encode_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_2d(&tb, W, K, N, static_cast<uint64_t>(K) * 2, kBK, p.BN, CU_TENSOR_MAP_SWIZZLE_128B))
+  const bool tb_ok = w_kn ? encode_tmap_2d(&tb, W, N, K, static_cast<uint64_t>(N) * 2, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B)
+                          : encode_tmap_2d(&tb, W, K, N, static_cast<uint64_t>(K) * 2, kBK, p.BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!encode_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) || !tb_ok)
     return set_error(QCF_ERR_CUDA, "gemm: tensor map encoding failed");
   const int units = p.tiles * p.splits;
   LaunchScope ls(kc, st);
+  if (w_kn) {
+    switch (p.BN) {
+      case 256: return dispatch_kn<256>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
+      case 128: return dispatch_kn<128>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
+      default: return dispatch_kn<64>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
+    }
+  }
   switch (p.BN) {
     case 256: return dispatch_epi<256>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
     case 128: return dispatch_epi<128>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
@@ -640,6 +670,8 @@ size_t qcf_linear_workspace_size(int M, int N, int K) { return gemm_workspace_si
 qcf_status qcf_linear(const qcf_bf16* A, int M, int K, const qcf_bf16* W, int N, int epilogue, void* out, void* ws,
                       size_t ws_bytes, void* stream) {
   if (!A || !W || !out) return set_error(QCF_ERR_INVALID_ARG, "qcf_linear: NULL pointer");
+  const bool w_kn = (epilogue & QCF_LINEAR_W_KN) != 0;
+  epilogue &= ~QCF_LINEAR_W_KN;
   if (epilogue != QCF_EPI_STORE_BF16 && epilogue != QCF_EPI_ADD_F32)
     return set_error(QCF_ERR_INVALID_ARG, "qcf_linear: unknown epilogue %d", epilogue);
   if (M < 0 || K <= 0 || N <= 0 || K % 64 || N % 64)
@@ -652,7 +684,7 @@ qcf_status qcf_linear(const qcf_bf16* A, int M, int K, const qcf_bf16* W, int N,
   ep.ldo = N;
   return gemm_launch(epilogue == QCF_EPI_STORE_BF16 ? EPI_STORE_BF16 : EPI_ADD_F32,
                      reinterpret_cast<const __nv_bfloat16*>(A), M, K, reinterpret_cast<const __nv_bfloat16*>(W), N, ep,
-                     ws, ws_bytes, static_cast<cudaStream_t>(stream), KC_GEMM_OTHER);
+                     ws, ws_bytes, static_cast<cudaStream_t>(stream), KC_GEMM_OTHER, w_kn);
 }
 
 }  // extern "C"

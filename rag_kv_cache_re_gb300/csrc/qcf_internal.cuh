@@ -73,7 +73,8 @@ struct EpiParams {
 };
 size_t gemm_workspace_size(int M, int N, int K);
 qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const __nv_bfloat16* W, int N,
-                       const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc);
+                       const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc,
+                       bool w_kn = false);
 
 // Row kernels (rows.cu).
 cudaError_t launch_embed(const __nv_bfloat16* embed, int vocab, int d, const int32_t* ids, const int32_t* rows,
@@ -215,11 +216,26 @@ __host__ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_ad
   d |= static_cast<uint64_t>(2u) << 61;
   return d;
 }
+// Shared-memory matrix descriptor for an MN-major bf16 operand (the N or M index
+// contiguous) written by TMA with 128-byte swizzle: each 1024-byte atom holds 8
+// consecutive K indices x 64 MN elements; `mn_block_bytes` apart sit the next 64
+// MN elements (leading byte offset), 1024 bytes apart the next 8 K indices
+// (stride byte offset).
+__host__ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t smem_addr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
-// B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 (17-22), M >> 4 (24-28).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// B bf16 (10-12 = 1), A K-major (bit 15 = 0), B K-major or MN-major (bit 16),
+// N >> 3 (17-22), M >> 4 (24-28).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // ---- warp-level MMA (m16n8k16, bf16 in, fp32 accumulate) and ldmatrix

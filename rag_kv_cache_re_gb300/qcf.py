@@ -189,19 +189,20 @@ def qcf_sparse_causal_attn(q, pos, K, V, scale: float, want_lse: bool = False, s
 
 
 def qcf_linear(A: torch.Tensor, W: torch.Tensor, out: Optional[torch.Tensor] = None, add: bool = False,
-               stream=None) -> torch.Tensor:
-    """out = A W^T (bf16 out), or out += A W^T for an fp32 `out` when add=True."""
+               w_kn: bool = False, stream=None) -> torch.Tensor:
+    """out = A W^T (bf16 out), or out += A W^T for an fp32 `out` when add=True.
+    With w_kn, W is stored [K][N] and out = A W."""
     _need_cuda(A, W)
     M, K = A.shape
-    N = W.shape[0]
+    N = W.shape[1] if w_kn else W.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32 if add else torch.bfloat16, device=A.device)
         if add:
             out.zero_()
     nb = _lib.lib().qcf_linear_workspace_size(M, N, K)
     ws = workspace(nb, A.device)
-    call("qcf_linear", _ptr(A), M, K, _ptr(W), N, _lib.QCF_EPI_ADD_F32 if add else _lib.QCF_EPI_STORE_BF16,
-         _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    epi = (_lib.QCF_EPI_ADD_F32 if add else _lib.QCF_EPI_STORE_BF16) | (_lib.QCF_LINEAR_W_KN if w_kn else 0)
+    call("qcf_linear", _ptr(A), M, K, _ptr(W), N, epi, _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
     return out
 
 

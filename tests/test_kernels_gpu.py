@@ -219,6 +219,22 @@ def test_linear_store_and_add(Q, M, N, K):
     assert_close(base.cpu().numpy(), b0 + ref, atol=max(1e-5, acc_tol), rtol=1e-5, what="fp32 residual add")
 
 
+@pytest.mark.parametrize("M,N,K", [(23, 64, 64), (300, 384, 192), (832, 4096, 4096), (64, 4096, 14336)])
+def test_linear_weights_stored_k_by_n(Q, M, N, K):
+    # W kept [K][N] (N contiguous): the tensor cores read it as an MN-major operand
+    A = qd.normal_bf16((M, K), 1.0, 34, DEV)
+    Wkn = qd.normal_bf16((K, N), 0.02, 35, DEV)
+    ref = (f32(A) @ f32(Wkn)).astype(np.float64)
+    out = Q.qcf_linear(A, Wkn, w_kn=True)
+    torch.cuda.synchronize()
+    assert_close(f32(out), ref, atol=1e-3, rtol=2.0 ** -8, what="bf16 out, W [K][N]")
+    base = torch.zeros((M, N), device=DEV, dtype=torch.float32)
+    Q.qcf_linear(A, Wkn, out=base, add=True, w_kn=True)
+    torch.cuda.synchronize()
+    acc_tol = (K / 16) * 2.0 ** -22 * max(1.0, float(np.sqrt(np.mean(ref ** 2))))
+    assert_close(base.cpu().numpy(), ref, atol=max(1e-5, acc_tol), rtol=1e-5, what="fp32 add, W [K][N]")
+
+
 def test_rmsnorm(Q):
     x = torch.randn((300, 4096), device=DEV) * 3
     g = qd.normal_bf16((4096,), 1.0, 33, DEV)
