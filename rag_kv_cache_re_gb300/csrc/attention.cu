@@ -284,6 +284,295 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
   }
 }
 
+// ------------------------------------------------------------------ tensor-core (tcgen05) variant, D = 128
+//
+// One CTA = 128 score rows: BRp = floor(128 / G) consecutive recomputed rows x the
+// G query heads of one KV head (row rho = p * G + hh).  Six warps:
+//   warp 0    TMA: K and V tiles of 64 keys (two 64-column boxes each, 128B swizzle), 2 stages
+//   warp 1    TMEM allocation; one thread issues S = Q K^T (M=128, N=64, K=128) into a
+//             double-buffered TMEM region and O += P V (M=128, N=128, K=64 keys, V read
+//             MN-major) into the O accumulator, one tile behind
+//   warps 2-5 one score row per thread: causal mask by true position, online softmax
+//             in the exp2 domain, P written to shared memory as bf16 (128B-swizzled
+//             K-major), O rescaled in TMEM only when a row max grows by more than 2^8
+// TMEM columns: S buffers [0, 64) and [64, 128); O [128, 256).
+constexpr int kTcKeys = 64;
+constexpr int kTcThreads = 192;
+constexpr int kTcQBytes = 128 * 128 * 2;       // Q tile: 2 atoms of 128 rows x 64 columns
+constexpr int kTcKVBytes = kTcKeys * 128 * 2;  // one K or V tile: 2 boxes of 64 keys x 64 columns
+constexpr int kTcPBytes = 128 * kTcKeys * 2;   // one P tile: 128 rows x 64 keys
+constexpr int kTcSmem = kTcQBytes + 2 * 2 * kTcKVBytes + 2 * kTcPBytes + 256 + 1024;
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ pos, int n, int T, int Hq,
+                          int Hkv, int G, int BRp, float scale_log2, __nv_bfloat16* __restrict__ o,
+                          float* __restrict__ lse, int split_tiles, int max_splits, float* __restrict__ part_o,
+                          float2* __restrict__ part_ml, unsigned int* status, int check) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* qbuf = smem;
+  uint8_t* kvbuf = smem + kTcQBytes;                       // stage s: K at s*2*KV, V at s*2*KV + KV
+  uint8_t* pbuf = kvbuf + 2 * 2 * kTcKVBytes;              // buffer b at b*P
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(pbuf + 2 * kTcPBytes);
+  uint64_t* kv_empty = kv_full + 2;
+  uint64_t* s_full = kv_empty + 2;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* q_ready = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_blocks = (n + BRp - 1) / BRp;
+  const int rb = n_blocks - 1 - static_cast<int>(blockIdx.x) / max_splits;
+  const int sp = static_cast<int>(blockIdx.x) % max_splits;
+  const int g = blockIdx.y;
+  const int row0 = rb * BRp;
+  const int row_end = min(n, row0 + BRp);
+  const int n_tiles_all = pos[row_end - 1] / kTcKeys + 1;
+  const int t_begin = sp * split_tiles;
+  if (t_begin >= n_tiles_all) return;
+  const int t_end = min(n_tiles_all, t_begin + split_tiles);
+  const int n_split = min(max_splits, (n_tiles_all + split_tiles - 1) / split_tiles);
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&kv_full[b], 1);
+      mbar_init(&kv_empty[b], 1);
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], 4);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&pv_done[b], 1);
+    }
+    mbar_init(q_ready, 4);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      for (int t = t_begin; t < t_end; ++t) {
+        const int i = t - t_begin, b = i & 1;
+        if (!mbar_wait(&kv_empty[b], ((i >> 1) & 1) ^ 1u)) {
+          flag_status(status, QCF_DEV_TIMEOUT);
+          break;
+        }
+        uint8_t* kb = kvbuf + b * 2 * kTcKVBytes;
+        uint8_t* vb = kb + kTcKVBytes;
+        mbar_arrive_expect_tx(&kv_full[b], 2 * kTcKVBytes);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          tma_load_2d(kb + h2 * (kTcKeys * 128), &tmK, &kv_full[b], g * D + h2 * 64, t * kTcKeys);
+          tma_load_2d(vb + h2 * (kTcKeys * 128), &tmV, &kv_full[b], g * D + h2 * 64, t * kTcKeys);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTcKeys, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      const uint32_t q_addr = smem_u32(qbuf);
+      bool ok = mbar_wait(q_ready, 0);
+      if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
+      tc_fence_after();
+      auto issue_pv = [&](int i) -> bool {   // O += P_i V_i
+        const int b = i & 1;
+        if (!mbar_wait(&p_full[b], (i >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(pbuf + b * kTcPBytes);
+        const uint32_t v_addr = smem_u32(kvbuf + b * 2 * kTcKVBytes + kTcKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTcKeys / 16; ++kk)
+          umma_f16(tmem_base + 128, sdesc_kmajor_sw128(p_addr + kk * 32), sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcKeys * 128),
+                   idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[b]);
+        umma_commit(&kv_empty[b]);
+        return true;
+      };
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        const int i = t - t_begin, b = i & 1;
+        if (!mbar_wait(&kv_full[b], (i >> 1) & 1) || !mbar_wait(&s_empty[b], ((i >> 1) & 1) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(kvbuf + b * 2 * kTcKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_q = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          const uint32_t off_k = (kk >> 2) * (kTcKeys * 128) + (kk & 3) * 32;
+          umma_f16(tmem_base + b * kTcKeys, sdesc_kmajor_sw128(q_addr + off_q), sdesc_kmajor_sw128(k_addr + off_k), idesc_s,
+                   kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[b]);
+        if (i > 0 && !issue_pv(i - 1)) ok = false;
+      }
+      if (ok && t_end > t_begin && !issue_pv(t_end - 1 - t_begin)) ok = false;
+      if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
+    }
+  } else {
+    // ---- softmax warps: thread = score row
+    const int quarter = warp & 3;
+    const int rho = quarter * 32 + lane;
+    const int p_local = rho / G, hh = rho - p_local * G;
+    const int r = row0 + p_local;
+    const bool valid = p_local < BRp && r < row_end;
+    const int prow = valid ? pos[r] : -1;
+    const int h = g * G + hh;
+    if (check && valid && (prow < 0 || prow >= T || (r > 0 && pos[r - 1] >= prow))) flag_status(status, QCF_DEV_BAD_INDEX);
+    // Q row -> shared memory in the 128B-swizzled K-major layout (2 atoms of 64 columns)
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(valid ? r : 0) * Hq + h) * D);
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(qbuf + (ch >> 3) * (128 * 128) + sw128_off(rho, ch & 7)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = t_begin; t < t_end; ++t) {
+      const int i = t - t_begin, b = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (i >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[64];
+      tmem_ld32(tmem_base + lane_base + b * kTcKeys, sv);
+      tmem_ld32(tmem_base + lane_base + b * kTcKeys + 32, sv + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[b]);
+      const int j0 = t * kTcKeys;
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        const float x = (j0 + j <= prow) ? sv[j] * scale_log2 : -INFINITY;
+        sv[j] = x;
+        tmax = fmaxf(tmax, x);
+      }
+      // rescale lazily: keep the old max unless a row's max grew by more than 2^8
+      const bool grow = tmax > m + 8.0f;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float m_new = grow ? tmax : m;
+        if (i > 0) {   // O holds tiles up to i-1: wait for their P.V, then scale the row
+          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float ov[32];
+            tmem_ld32(tmem_base + lane_base + 128 + c * 32, ov);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ov[k] *= f;
+            tmem_st32(tmem_base + lane_base + 128 + c * 32, ov);
+          }
+          l *= f;
+        }
+        m = m_new;
+      }
+      // P buffer b was read by the P.V of tile i-2
+      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((i - 2) >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      float rs = 0.f;
+      uint8_t* prow_smem = pbuf + b * kTcPBytes;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        float pv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float x = sv[ch * 8 + k];
+          pv[k] = (m == -INFINITY || x == -INFINITY) ? 0.f : fast_exp2(x - m);
+          rs += pv[k];
+        }
+        uint4 u;
+        u.x = pack_bf16x2(pv[0], pv[1]);
+        u.y = pack_bf16x2(pv[2], pv[3]);
+        u.z = pack_bf16x2(pv[4], pv[5]);
+        u.w = pack_bf16x2(pv[6], pv[7]);
+        *reinterpret_cast<uint4*>(prow_smem + sw128_off(rho, ch)) = u;
+      }
+      l += rs;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[b]);
+    }
+    if (ok && t_end > t_begin) {
+      const int last = t_end - 1 - t_begin;
+      if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[last & 1], (last >> 1) & 1))) ok = false;
+    }
+    if (!ok) {
+      flag_status(status, QCF_DEV_TIMEOUT);
+    } else {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (n_split > 1) {
+        const size_t pstride = static_cast<size_t>(n) * Hq;
+        float* po = valid ? part_o + (static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h) * D : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(tmem_base + lane_base + 128 + c * 32, ov);
+          if (valid) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+              *reinterpret_cast<float4*>(po + c * 32 + k) = make_float4(ov[k], ov[k + 1], ov[k + 2], ov[k + 3]);
+          }
+        }
+        if (valid) part_ml[static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h] = make_float2(m, l);
+      } else {
+        __nv_bfloat16* op = valid ? o + (static_cast<size_t>(r) * Hq + h) * D : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(tmem_base + lane_base + 128 + c * 32, ov);
+          if (valid) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 8) {
+              uint4 u;
+              u.x = pack_bf16x2(ov[k] * inv, ov[k + 1] * inv);
+              u.y = pack_bf16x2(ov[k + 2] * inv, ov[k + 3] * inv);
+              u.z = pack_bf16x2(ov[k + 4] * inv, ov[k + 5] * inv);
+              u.w = pack_bf16x2(ov[k + 6] * inv, ov[k + 7] * inv);
+              *reinterpret_cast<uint4*>(op + c * 32 + k) = u;
+            }
+          }
+        }
+        if (valid && lse) lse[static_cast<size_t>(r) * Hq + h] = (m + log2f(l)) * 0.69314718055994531f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 256);
+  }
+}
+
 // Merges the key-range partials of rows whose block was split: one warp per
 // (row, head), splits summed in order (deterministic).
 template <int D>
@@ -331,10 +620,11 @@ struct AttnPlan {
 
 // Long row blocks are split over key ranges only when the grid is too small to
 // balance by itself (the fused path: few rows, the query block sees every key).
-static AttnPlan plan_attn(int n, int T, int Hq, int Hkv) {
+static AttnPlan plan_attn(int n, int T, int Hq, int Hkv, int D) {
   AttnPlan p;
   p.G = Hq / Hkv;
-  p.BR = 16 * (p.G >= 8 ? 1 : 8 / p.G);
+  // rows per CTA: the tensor-core kernel (D = 128) fills 128 score rows, the warp-MMA kernel 16 per warp
+  p.BR = D == 128 ? 128 / p.G : 16 * (p.G >= 8 ? 1 : 8 / p.G);
   p.n_blocks = (n + p.BR - 1) / p.BR;
   const int max_tiles = (T + kKeyTile - 1) / kKeyTile;
   p.split_tiles = max_tiles;
@@ -350,7 +640,7 @@ static AttnPlan plan_attn(int n, int T, int Hq, int Hkv) {
 
 size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D) {
   if (n <= 0 || T <= 0 || Hkv <= 0 || Hq % Hkv) return 0;
-  const AttnPlan p = plan_attn(n, T, Hq, Hkv);
+  const AttnPlan p = plan_attn(n, T, Hq, Hkv, D);
   if (p.max_splits <= 1) return 0;
   return align_up(static_cast<size_t>(p.max_splits) * n * Hq * D * sizeof(float), 256) +
          align_up(static_cast<size_t>(p.max_splits) * n * Hq * sizeof(float2), 256);
@@ -361,7 +651,7 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
                                 const __nv_bfloat16* V, int T, int Hq, int Hkv, float scale, __nv_bfloat16* o,
                                 float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc) {
   using Cfg = AttnCfg<D>;
-  const AttnPlan plan = plan_attn(n, T, Hq, Hkv);
+  const AttnPlan plan = plan_attn(n, T, Hq, Hkv, D);
   const int G = plan.G;
   const int BR = plan.BR;
   const int warps = G * (BR / 16);
@@ -390,7 +680,18 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
   if (attr != cudaSuccess) return cuda_error(attr, "sparse_causal_attn: smem attribute");
   dim3 grid(plan.n_blocks * plan.max_splits, Hkv);
   const float scale_log2 = scale * 1.4426950408889634f;
-  {
+  if constexpr (D == 128) {
+    static std::once_flag once_tc;
+    static cudaError_t attr_tc = cudaSuccess;
+    std::call_once(once_tc, [] {
+      attr_tc = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    });
+    if (attr_tc != cudaSuccess) return cuda_error(attr_tc, "sparse_causal_attn: smem attribute");
+    LaunchScope ls(kc, st);
+    sparse_attn_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o, lse,
+                                                              plan.split_tiles, plan.max_splits, part_o, part_ml,
+                                                              device_status_ptr(), check_enabled() ? 1 : 0);
+  } else {
     LaunchScope ls(kc, st);
     sparse_attn_kernel<D><<<grid, warps * 32, Cfg::SMEM_BYTES, st>>>(
         tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o, lse, plan.split_tiles, plan.max_splits, part_o, part_ml,
