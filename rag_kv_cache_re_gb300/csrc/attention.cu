@@ -287,21 +287,34 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
 // ------------------------------------------------------------------ tensor-core (tcgen05) variant, D = 128
 //
 // One CTA = 128 score rows: BRp = floor(128 / G) consecutive recomputed rows x the
-// G query heads of one KV head (row rho = p * G + hh).  Six warps:
-//   warp 0    TMA: K and V tiles of 64 keys (two 64-column boxes each, 128B swizzle), 2 stages
-//   warp 1    TMEM allocation; one thread issues S = Q K^T (M=128, N=64, K=128) into a
-//             double-buffered TMEM region and O += P V (M=128, N=128, K=64 keys, V read
-//             MN-major) into the O accumulator, one tile behind
-//   warps 2-5 one score row per thread: causal mask by true position, online softmax
-//             in the exp2 domain, P written to shared memory as bf16 (128B-swizzled
-//             K-major), O rescaled in TMEM only when a row max grows by more than 2^8
-// TMEM columns: S buffers [0, 64) and [64, 128); O [128, 256).
+// G query heads of one KV head (row rho = p * G + hh).  Eleven warps:
+//   warp 0     TMA producer for K: tiles of 64 keys (two 64-column boxes, 128B swizzle)
+//              into a 4-stage ring; a stage is freed by the Q.K^T that read it
+//   warp 1     TMEM allocation; one thread issues S_i = Q K_i^T (M=128, N=64, K=128)
+//              two tiles ahead of O_s += P_i V_i (M=128, N=128, K=64 keys, V read
+//              MN-major), so a softmax stream finds its next scores already computed
+//   warp 2     TMA producer for V: the same tiling, its own 4-stage ring, freed by P.V
+//   warps 3-10 two softmax streams of four warps; stream s owns the key tiles i = s
+//              (mod 2) of the CTA's range with its own S buffer, P buffer and O
+//              accumulator.  One score row per thread: causal mask by true position
+//              (boundary tiles only), online softmax in the exp2 domain with the scale
+//              folded into one FFMA, P written to shared memory as bf16 (128B-swizzled
+//              K-major), O_s rescaled in TMEM only when a row max grows by more than
+//              2^8.  The streams are independent online softmaxes over disjoint key
+//              sets, merged once at the end (common max, rescale, sum): the algebra of
+//              merging split-KV partials.
+// TMEM columns: S_s at [64 s, 64 s + 64); O_s at [128 + 128 s, 256 + 128 s).
 constexpr int kTcKeys = 64;
-constexpr int kTcThreads = 192;
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 352;
 constexpr int kTcQBytes = 128 * 128 * 2;       // Q tile: 2 atoms of 128 rows x 64 columns
 constexpr int kTcKVBytes = kTcKeys * 128 * 2;  // one K or V tile: 2 boxes of 64 keys x 64 columns
 constexpr int kTcPBytes = 128 * kTcKeys * 2;   // one P tile: 128 rows x 64 keys
-constexpr int kTcSmem = kTcQBytes + 2 * 2 * kTcKVBytes + 2 * kTcPBytes + 256 + 1024;
+constexpr int kTcMlBytes = 2 * 128 * 8;        // per-stream (m, l) of every row, for the merge
+constexpr int kTcSmem = kTcQBytes + 2 * kTcStages * kTcKVBytes + 2 * kTcPBytes + kTcMlBytes + 256 + 1024;
+
+// Barrier 1 over the 256 softmax threads (barrier 0 is __syncthreads).
+__device__ __forceinline__ void softmax_threads_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -310,15 +323,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           float* __restrict__ lse, int split_tiles, int max_splits, float* __restrict__ part_o,
                           float2* __restrict__ part_ml, unsigned int* status, int check) {
   constexpr int D = 128;
+  constexpr unsigned kAll = 0xffffffffu;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* qbuf = smem;
-  uint8_t* kvbuf = smem + kTcQBytes;                       // stage s: K at s*2*KV, V at s*2*KV + KV
-  uint8_t* pbuf = kvbuf + 2 * 2 * kTcKVBytes;              // buffer b at b*P
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(pbuf + 2 * kTcPBytes);
-  uint64_t* kv_empty = kv_full + 2;
-  uint64_t* s_full = kv_empty + 2;
+  uint8_t* kbuf = smem + kTcQBytes;              // stage st at st * KV
+  uint8_t* vbuf = kbuf + kTcStages * kTcKVBytes;
+  uint8_t* pbuf = vbuf + kTcStages * kTcKVBytes;  // stream s at s * P
+  float2* ml_x = reinterpret_cast<float2*>(pbuf + 2 * kTcPBytes);  // [stream][row]
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(pbuf + 2 * kTcPBytes + kTcMlBytes);
+  uint64_t* k_empty = k_full + kTcStages;
+  uint64_t* v_full = k_empty + kTcStages;
+  uint64_t* v_empty = v_full + kTcStages;
+  uint64_t* s_full = v_empty + kTcStages;
   uint64_t* s_empty = s_full + 2;
   uint64_t* p_full = s_empty + 2;
   uint64_t* pv_done = p_full + 2;
@@ -337,21 +355,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (t_begin >= n_tiles_all) return;
   const int t_end = min(n_tiles_all, t_begin + split_tiles);
   const int n_split = min(max_splits, (n_tiles_all + split_tiles - 1) / split_tiles);
+  const int nt = t_end - t_begin;  // >= 1
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&kv_full[b], 1);
-      mbar_init(&kv_empty[b], 1);
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 4);
-      mbar_init(&p_full[b], 4);
-      mbar_init(&pv_done[b], 1);
+    for (int st = 0; st < kTcStages; ++st) {
+      mbar_init(&k_full[st], 1);
+      mbar_init(&k_empty[st], 1);
+      mbar_init(&v_full[st], 1);
+      mbar_init(&v_empty[st], 1);
     }
-    mbar_init(q_ready, 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], 4);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(q_ready, 8);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -359,71 +382,78 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
+    // ---- TMA producers: warp 0 streams K, warp 2 streams V
     if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      for (int t = t_begin; t < t_end; ++t) {
-        const int i = t - t_begin, b = i & 1;
-        if (!mbar_wait(&kv_empty[b], ((i >> 1) & 1) ^ 1u)) {
+      const bool is_k = warp == 0;
+      const CUtensorMap* map = is_k ? &tmK : &tmV;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* ring = is_k ? kbuf : vbuf;
+      tma_prefetch_desc(map);
+      for (int i = 0; i < nt; ++i) {
+        const int st = i % kTcStages;
+        if (!mbar_wait(&empty[st], ((i / kTcStages) & 1) ^ 1u)) {
           flag_status(status, QCF_DEV_TIMEOUT);
           break;
         }
-        uint8_t* kb = kvbuf + b * 2 * kTcKVBytes;
-        uint8_t* vb = kb + kTcKVBytes;
-        mbar_arrive_expect_tx(&kv_full[b], 2 * kTcKVBytes);
+        mbar_arrive_expect_tx(&full[st], kTcKVBytes);
+        uint8_t* dst = ring + st * kTcKVBytes;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          tma_load_2d(kb + h2 * (kTcKeys * 128), &tmK, &kv_full[b], g * D + h2 * 64, t * kTcKeys);
-          tma_load_2d(vb + h2 * (kTcKeys * 128), &tmV, &kv_full[b], g * D + h2 * 64, t * kTcKeys);
-        }
+        for (int h2 = 0; h2 < 2; ++h2)
+          tma_load_2d(dst + h2 * (kTcKeys * 128), map, &full[st], g * D + h2 * 64, (t_begin + i) * kTcKeys);
       }
     }
   } else if (warp == 1) {
+    // ---- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTcKeys, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       const uint32_t q_addr = smem_u32(qbuf);
       bool ok = mbar_wait(q_ready, 0);
-      if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
       tc_fence_after();
-      auto issue_pv = [&](int i) -> bool {   // O += P_i V_i
-        const int b = i & 1;
-        if (!mbar_wait(&p_full[b], (i >> 1) & 1)) return false;
+      auto issue_s = [&](int i) -> bool {  // S_s = Q K_i^T
+        const int st = i % kTcStages, s = i & 1;
+        if (!mbar_wait(&k_full[st], (i / kTcStages) & 1) || !mbar_wait(&s_empty[s], ((i >> 1) & 1) ^ 1u))
+          return false;
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(pbuf + b * kTcPBytes);
-        const uint32_t v_addr = smem_u32(kvbuf + b * 2 * kTcKVBytes + kTcKVBytes);
-#pragma unroll
-        for (int kk = 0; kk < kTcKeys / 16; ++kk)
-          umma_f16(tmem_base + 128, sdesc_kmajor_sw128(p_addr + kk * 32), sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcKeys * 128),
-                   idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[b]);
-        umma_commit(&kv_empty[b]);
-        return true;
-      };
-      for (int t = t_begin; t < t_end && ok; ++t) {
-        const int i = t - t_begin, b = i & 1;
-        if (!mbar_wait(&kv_full[b], (i >> 1) & 1) || !mbar_wait(&s_empty[b], ((i >> 1) & 1) ^ 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(kvbuf + b * 2 * kTcKVBytes);
+        const uint32_t k_addr = smem_u32(kbuf + st * kTcKVBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_q = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
           const uint32_t off_k = (kk >> 2) * (kTcKeys * 128) + (kk & 3) * 32;
-          umma_f16(tmem_base + b * kTcKeys, sdesc_kmajor_sw128(q_addr + off_q), sdesc_kmajor_sw128(k_addr + off_k), idesc_s,
-                   kk > 0 ? 1u : 0u);
+          umma_f16(tmem_base + s * kTcKeys, sdesc_kmajor_sw128(q_addr + off_q), sdesc_kmajor_sw128(k_addr + off_k),
+                   idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[b]);
-        if (i > 0 && !issue_pv(i - 1)) ok = false;
+        umma_commit(&s_full[s]);
+        umma_commit(&k_empty[st]);
+        return true;
+      };
+      auto issue_pv = [&](int i) -> bool {  // O_s += P_i V_i
+        const int st = i % kTcStages, s = i & 1;
+        if (!mbar_wait(&v_full[st], (i / kTcStages) & 1) || !mbar_wait(&p_full[s], (i >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(pbuf + s * kTcPBytes);
+        const uint32_t v_addr = smem_u32(vbuf + st * kTcKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTcKeys / 16; ++kk)
+          umma_f16(tmem_base + 128 + s * 128, sdesc_kmajor_sw128(p_addr + kk * 32),
+                   sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcKeys * 128), idesc_o, (i >= 2 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[s]);
+        umma_commit(&v_empty[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && nt > 1) ok = issue_s(1);
+      for (int i = 0; i < nt && ok; ++i) {
+        if (i + 2 < nt && !issue_s(i + 2)) ok = false;
+        else if (!issue_pv(i)) ok = false;
       }
-      if (ok && t_end > t_begin && !issue_pv(t_end - 1 - t_begin)) ok = false;
       if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
     }
   } else {
-    // ---- softmax warps: thread = score row
+    // ---- softmax streams: thread = score row
+    const int sidx = (warp - 3) >> 2;
     const int quarter = warp & 3;
     const int rho = quarter * 32 + lane;
     const int p_local = rho / G, hh = rho - p_local * G;
@@ -431,49 +461,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool valid = p_local < BRp && r < row_end;
     const int prow = valid ? pos[r] : -1;
     const int h = g * G + hh;
-    if (check && valid && (prow < 0 || prow >= T || (r > 0 && pos[r - 1] >= prow))) flag_status(status, QCF_DEV_BAD_INDEX);
-    // Q row -> shared memory in the 128B-swizzled K-major layout (2 atoms of 64 columns)
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(valid ? r : 0) * Hq + h) * D);
+    if (check && sidx == 0 && valid && (prow < 0 || prow >= T || (r > 0 && pos[r - 1] >= prow)))
+      flag_status(status, QCF_DEV_BAD_INDEX);
+    {  // stream s stores the 64-column atom s of its Q row, 128B-swizzled K-major
+      const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(valid ? r : 0) * Hq + h) * D) + sidx * 8;
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int ch = 0; ch < 8; ++ch) {
         const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(qbuf + (ch >> 3) * (128 * 128) + sw128_off(rho, ch & 7)) = v;
+        *reinterpret_cast<uint4*>(qbuf + sidx * (128 * 128) + sw128_off(rho, ch)) = v;
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_tm = tmem_base + lane_base + sidx * kTcKeys;
+    const uint32_t o_tm = tmem_base + lane_base + 128 + sidx * 128;
+    uint8_t* p_smem = pbuf + sidx * kTcPBytes;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int t = t_begin; t < t_end; ++t) {
-      const int i = t - t_begin, b = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (i >> 1) & 1))) {
+    int k = 0;  // tiles this stream has finished
+    for (int i = sidx; i < nt; i += 2, ++k) {
+      if (!__all_sync(kAll, mbar_wait(&s_full[sidx], k & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
       float sv[64];
-      tmem_ld32(tmem_base + lane_base + b * kTcKeys, sv);
-      tmem_ld32(tmem_base + lane_base + b * kTcKeys + 32, sv + 32);
+      tmem_ld64(s_tm, sv);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[b]);
-      const int j0 = t * kTcKeys;
-      float tmax = -INFINITY;
+      if (lane == 0) mbar_arrive(&s_empty[sidx]);
+      const int j0 = (t_begin + i) * kTcKeys;
+      if (j0 + kTcKeys - 1 > prow) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float x = (j0 + j <= prow) ? sv[j] * scale_log2 : -INFINITY;
-        sv[j] = x;
-        tmax = fmaxf(tmax, x);
+        for (int j = 0; j < 64; ++j)
+          if (j0 + j > prow) sv[j] = -INFINITY;
       }
+      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+      for (int j = 4; j < 64; j += 4) {
+        mx0 = fmaxf(mx0, sv[j]);
+        mx1 = fmaxf(mx1, sv[j + 1]);
+        mx2 = fmaxf(mx2, sv[j + 2]);
+        mx3 = fmaxf(mx3, sv[j + 3]);
+      }
+      const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
       // rescale lazily: keep the old max unless a row's max grew by more than 2^8
       const bool grow = tmax > m + 8.0f;
-      if (__any_sync(0xffffffffu, grow)) {
+      if (__any_sync(kAll, grow)) {
         const float m_new = grow ? tmax : m;
-        if (i > 0) {   // O holds tiles up to i-1: wait for their P.V, then scale the row
-          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1))) {
+        if (k > 0) {  // O_s holds this stream's tiles so far: wait for the last P.V, then scale
+          if (!__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) {
             ok = false;
             break;
           }
@@ -482,86 +521,89 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float ov[32];
-            tmem_ld32(tmem_base + lane_base + 128 + c * 32, ov);
+            tmem_ld32(o_tm + c * 32, ov);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) ov[k] *= f;
-            tmem_st32(tmem_base + lane_base + 128 + c * 32, ov);
+            for (int e = 0; e < 32; ++e) ov[e] *= f;
+            tmem_st32(o_tm + c * 32, ov);
           }
           l *= f;
         }
         m = m_new;
       }
-      // P buffer b was read by the P.V of tile i-2
-      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((i - 2) >> 1) & 1))) {
+      // this stream's P buffer was read by its previous P.V
+      if (k > 0 && !__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) {
         ok = false;
         break;
       }
-      float rs = 0.f;
-      uint8_t* prow_smem = pbuf + b * kTcPBytes;
+      const float nm = (m == -INFINITY) ? 0.f : -m;  // m = -inf only when every key so far is masked
+      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         float pv[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float x = sv[ch * 8 + k];
-          pv[k] = (m == -INFINITY || x == -INFINITY) ? 0.f : fast_exp2(x - m);
-          rs += pv[k];
-        }
+        for (int e = 0; e < 8; ++e) pv[e] = fast_exp2(fmaf(sv[ch * 8 + e], scale_log2, nm));
+        rs0 += pv[0] + pv[4];
+        rs1 += pv[1] + pv[5];
+        rs2 += pv[2] + pv[6];
+        rs3 += pv[3] + pv[7];
         uint4 u;
         u.x = pack_bf16x2(pv[0], pv[1]);
         u.y = pack_bf16x2(pv[2], pv[3]);
         u.z = pack_bf16x2(pv[4], pv[5]);
         u.w = pack_bf16x2(pv[6], pv[7]);
-        *reinterpret_cast<uint4*>(prow_smem + sw128_off(rho, ch)) = u;
+        *reinterpret_cast<uint4*>(p_smem + sw128_off(rho, ch)) = u;
       }
-      l += rs;
+      l += (rs0 + rs1) + (rs2 + rs3);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[b]);
+      if (lane == 0) mbar_arrive(&p_full[sidx]);
     }
-    if (ok && t_end > t_begin) {
-      const int last = t_end - 1 - t_begin;
-      if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[last & 1], (last >> 1) & 1))) ok = false;
-    }
-    if (!ok) {
-      flag_status(status, QCF_DEV_TIMEOUT);
-    } else {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      if (n_split > 1) {
-        const size_t pstride = static_cast<size_t>(n) * Hq;
-        float* po = valid ? part_o + (static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h) * D : nullptr;
+    if (ok && k > 0 && !__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) ok = false;
+    if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
+    // ---- merge the two streams; stream s writes output columns [64 s, 64 s + 64)
+    ml_x[sidx * 128 + rho] = ok ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
+    softmax_threads_sync();
+    tc_fence_after();
+    const float2 a0 = ml_x[rho], a1 = ml_x[128 + rho];
+    const float M = fmaxf(a0.x, a1.x);
+    const float f0 = a0.x == -INFINITY ? 0.f : fast_exp2(a0.x - M);
+    const float f1 = a1.x == -INFINITY ? 0.f : fast_exp2(a1.x - M);
+    const float L = a0.y * f0 + a1.y * f1;
+    if (ok) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const size_t pstride = static_cast<size_t>(n) * Hq;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld32(tmem_base + lane_base + 128 + c * 32, ov);
-          if (valid) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c0 = sidx * 64 + cc * 32;
+        float o0[32], o1[32];
+        tmem_ld32(tmem_base + lane_base + 128 + c0, o0);
+        tmem_ld32(tmem_base + lane_base + 256 + c0, o1);
 #pragma unroll
-            for (int k = 0; k < 32; k += 4)
-              *reinterpret_cast<float4*>(po + c * 32 + k) = make_float4(ov[k], ov[k + 1], ov[k + 2], ov[k + 3]);
+        for (int e = 0; e < 32; ++e) o0[e] = (f0 != 0.f ? o0[e] * f0 : 0.f) + (f1 != 0.f ? o1[e] * f1 : 0.f);
+        if (!valid) continue;
+        if (n_split > 1) {
+          float* po = part_o + (static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h) * D + c0;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(po + e) = make_float4(o0[e], o0[e + 1], o0[e + 2], o0[e + 3]);
+        } else {
+          __nv_bfloat16* op = o + (static_cast<size_t>(r) * Hq + h) * D + c0;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 u;
+            u.x = pack_bf16x2(o0[e] * inv, o0[e + 1] * inv);
+            u.y = pack_bf16x2(o0[e + 2] * inv, o0[e + 3] * inv);
+            u.z = pack_bf16x2(o0[e + 4] * inv, o0[e + 5] * inv);
+            u.w = pack_bf16x2(o0[e + 6] * inv, o0[e + 7] * inv);
+            *reinterpret_cast<uint4*>(op + e) = u;
           }
         }
-        if (valid) part_ml[static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h] = make_float2(m, l);
-      } else {
-        __nv_bfloat16* op = valid ? o + (static_cast<size_t>(r) * Hq + h) * D : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld32(tmem_base + lane_base + 128 + c * 32, ov);
-          if (valid) {
-#pragma unroll
-            for (int k = 0; k < 32; k += 8) {
-              uint4 u;
-              u.x = pack_bf16x2(ov[k] * inv, ov[k + 1] * inv);
-              u.y = pack_bf16x2(ov[k + 2] * inv, ov[k + 3] * inv);
-              u.z = pack_bf16x2(ov[k + 4] * inv, ov[k + 5] * inv);
-              u.w = pack_bf16x2(ov[k + 6] * inv, ov[k + 7] * inv);
-              *reinterpret_cast<uint4*>(op + c * 32 + k) = u;
-            }
-          }
-        }
-        if (valid && lse) lse[static_cast<size_t>(r) * Hq + h] = (m + log2f(l)) * 0.69314718055994531f;
+      }
+      if (valid && sidx == 0) {
+        if (n_split > 1)
+          part_ml[static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h] = make_float2(M, L);
+        else if (lse)
+          lse[static_cast<size_t>(r) * Hq + h] = (M + log2f(L)) * 0.69314718055994531f;
       }
     }
   }
@@ -569,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 256);
+    tmem_dealloc(tmem_base, 512);
   }
 }
 
