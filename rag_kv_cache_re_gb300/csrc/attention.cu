@@ -290,28 +290,37 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
 // G query heads of one KV head (row rho = p * G + hh).  Eleven warps:
 //   warp 0     TMA producer for K: tiles of 64 keys (two 64-column boxes, 128B swizzle)
 //              into a 4-stage ring; a stage is freed by the Q.K^T that read it
-//   warp 1     TMEM allocation; one thread issues S_i = Q K_i^T (M=128, N=64, K=128)
-//              two tiles ahead of O_s += P_i V_i (M=128, N=128, K=64 keys, V read
-//              MN-major), so a softmax stream finds its next scores already computed
+//   warp 1     TMEM allocation; one thread issues the tensor-core work in groups:
+//              group g = { S_{g+2} = Q K_{g+2}^T (M=128, N=64, K=128),
+//                          O_s += P_g V_g (M=128, N=128, K=64 keys; P read from TMEM,
+//                          V MN-major from shared memory) },
+//              after S_0 and S_1.  Every dependency of group g lands on one mbarrier,
+//              so the issuing thread waits once per tile: a barrier read stalls the
+//              issuing thread for longer than the tensor core needs for one of these
+//              small MMAs, so fewer reads keep the tensor pipe fed.
 //   warp 2     TMA producer for V: the same tiling, its own 4-stage ring, freed by P.V
 //   warps 3-10 two softmax streams of four warps; stream s owns the key tiles i = s
-//              (mod 2) of the CTA's range with its own S buffer, P buffer and O
-//              accumulator.  One score row per thread: causal mask by true position
+//              (mod 2) of the CTA's range with its own S buffer, two P buffers and an
+//              O accumulator.  One score row per thread: causal mask by true position
 //              (boundary tiles only), online softmax in the exp2 domain with the scale
-//              folded into one FFMA, P written to shared memory as bf16 (128B-swizzled
-//              K-major), O_s rescaled in TMEM only when a row max grows by more than
-//              2^8.  The streams are independent online softmaxes over disjoint key
-//              sets, merged once at the end (common max, rescale, sum): the algebra of
-//              merging split-KV partials.
-// TMEM columns: S_s at [64 s, 64 s + 64); O_s at [128 + 128 s, 256 + 128 s).
+//              folded into one FFMA, P stored to TMEM as packed bf16 pairs, O_s rescaled
+//              in TMEM only when a row max grows by more than 2^8.  The streams are
+//              independent online softmaxes over disjoint key sets, merged once at the
+//              end (common max, rescale, sum): the algebra of merging split-KV partials.
+// Group g's barrier go[g % 8] completes when: K_{g+2} has landed (or there is none), V_g
+// has landed, and the four warps of stream g % 2 have read S_g and written P_g.
+// TMEM columns: S_s at [64 s, 64 s + 64); O_s at [128 + 128 s, 256 + 128 s);
+// P_{s,b} at [384 + 64 s + 32 b, 416 + 64 s + 32 b) (64 bf16 keys in 32 columns).
 constexpr int kTcKeys = 64;
 constexpr int kTcStages = 4;
+constexpr int kTcGo = 8;                       // group barriers in flight
 constexpr int kTcThreads = 352;
 constexpr int kTcQBytes = 128 * 128 * 2;       // Q tile: 2 atoms of 128 rows x 64 columns
 constexpr int kTcKVBytes = kTcKeys * 128 * 2;  // one K or V tile: 2 boxes of 64 keys x 64 columns
-constexpr int kTcPBytes = 128 * kTcKeys * 2;   // one P tile: 128 rows x 64 keys
 constexpr int kTcMlBytes = 2 * 128 * 8;        // per-stream (m, l) of every row, for the merge
-constexpr int kTcSmem = kTcQBytes + 2 * kTcStages * kTcKVBytes + 2 * kTcPBytes + kTcMlBytes + 256 + 1024;
+constexpr int kTcSmem = kTcQBytes + 2 * kTcStages * kTcKVBytes + kTcMlBytes + 256 + 1024;
+constexpr uint32_t kTcPCol = 384;              // first TMEM column of the P buffers
+constexpr uint32_t kTcGoCount = 10;            // K producer + V producer + 4 (S read) + 4 (P written)
 
 // Barrier 1 over the 256 softmax threads (barrier 0 is __syncthreads).
 __device__ __forceinline__ void softmax_threads_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -328,19 +337,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* qbuf = smem;
-  uint8_t* kbuf = smem + kTcQBytes;              // stage st at st * KV
+  uint8_t* kbuf = smem + kTcQBytes;  // stage st at st * KV
   uint8_t* vbuf = kbuf + kTcStages * kTcKVBytes;
-  uint8_t* pbuf = vbuf + kTcStages * kTcKVBytes;  // stream s at s * P
-  float2* ml_x = reinterpret_cast<float2*>(pbuf + 2 * kTcPBytes);  // [stream][row]
-  uint64_t* k_full = reinterpret_cast<uint64_t*>(pbuf + 2 * kTcPBytes + kTcMlBytes);
-  uint64_t* k_empty = k_full + kTcStages;
-  uint64_t* v_full = k_empty + kTcStages;
-  uint64_t* v_empty = v_full + kTcStages;
-  uint64_t* s_full = v_empty + kTcStages;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* pv_done = p_full + 2;
-  uint64_t* q_ready = pv_done + 2;
+  float2* ml_x = reinterpret_cast<float2*>(vbuf + kTcStages * kTcKVBytes);  // [stream][row]
+  uint64_t* go = reinterpret_cast<uint64_t*>(vbuf + kTcStages * kTcKVBytes + kTcMlBytes);
+  uint64_t* k_init = go + kTcGo;          // K_0 and K_1, read by S_0 and S_1
+  uint64_t* k_empty = k_init + 2;
+  uint64_t* v_empty = k_empty + kTcStages;
+  uint64_t* s_full = v_empty + kTcStages;  // [stream]
+  uint64_t* pv_done = s_full + 2;          // [stream * 2 + P buffer]
+  uint64_t* q_ready = pv_done + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -358,17 +364,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nt = t_end - t_begin;  // >= 1
 
   if (threadIdx.x == 0) {
-    for (int st = 0; st < kTcStages; ++st) {
-      mbar_init(&k_full[st], 1);
-      mbar_init(&k_empty[st], 1);
-      mbar_init(&v_full[st], 1);
-      mbar_init(&v_empty[st], 1);
+    for (int b = 0; b < kTcGo; ++b) mbar_init(&go[b], kTcGoCount);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&k_init[b], 1);
+      mbar_init(&s_full[b], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 4);
-      mbar_init(&p_full[s], 4);
-      mbar_init(&pv_done[s], 1);
+    for (int st = 0; st < kTcStages; ++st) {
+      mbar_init(&k_empty[st], 1);
+      mbar_init(&v_empty[st], 1);
+      mbar_init(&pv_done[st], 1);  // four P buffers, like the four stages
     }
     mbar_init(q_ready, 8);
     fence_mbar_init();
@@ -383,26 +387,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0 || warp == 2) {
-    // ---- TMA producers: warp 0 streams K, warp 2 streams V
+    // ---- TMA producers: warp 0 streams K (tile t feeds group t - 2), warp 2 streams V (tile t feeds group t)
     if (lane == 0) {
       const bool is_k = warp == 0;
       const CUtensorMap* map = is_k ? &tmK : &tmV;
-      uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
       uint8_t* ring = is_k ? kbuf : vbuf;
       tma_prefetch_desc(map);
+      bool ok = true;
       for (int i = 0; i < nt; ++i) {
         const int st = i % kTcStages;
         if (!mbar_wait(&empty[st], ((i / kTcStages) & 1) ^ 1u)) {
           flag_status(status, QCF_DEV_TIMEOUT);
+          ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[st], kTcKVBytes);
+        uint64_t* bar = is_k ? (i < 2 ? &k_init[i] : &go[(i - 2) % kTcGo]) : &go[i % kTcGo];
+        mbar_arrive_expect_tx(bar, kTcKVBytes);
         uint8_t* dst = ring + st * kTcKVBytes;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2)
-          tma_load_2d(dst + h2 * (kTcKeys * 128), map, &full[st], g * D + h2 * 64, (t_begin + i) * kTcKeys);
+          tma_load_2d(dst + h2 * (kTcKeys * 128), map, bar, g * D + h2 * 64, (t_begin + i) * kTcKeys);
       }
+      // the last two groups have no K tile to wait for: their K share of the count arrives now
+      if (is_k && ok)
+        for (int gi = max(nt - 2, 0); gi < nt; ++gi) mbar_arrive(&go[gi % kTcGo]);
     }
   } else if (warp == 1) {
     // ---- MMA issuer
@@ -410,13 +419,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTcKeys, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       const uint32_t q_addr = smem_u32(qbuf);
-      bool ok = mbar_wait(q_ready, 0);
-      tc_fence_after();
-      auto issue_s = [&](int i) -> bool {  // S_s = Q K_i^T
+      auto issue_s = [&](int i) {  // S_{i % 2} = Q K_i^T
         const int st = i % kTcStages, s = i & 1;
-        if (!mbar_wait(&k_full[st], (i / kTcStages) & 1) || !mbar_wait(&s_empty[s], ((i >> 1) & 1) ^ 1u))
-          return false;
-        tc_fence_after();
         const uint32_t k_addr = smem_u32(kbuf + st * kTcKVBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -427,27 +431,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         umma_commit(&s_full[s]);
         umma_commit(&k_empty[st]);
-        return true;
       };
-      auto issue_pv = [&](int i) -> bool {  // O_s += P_i V_i
-        const int st = i % kTcStages, s = i & 1;
-        if (!mbar_wait(&v_full[st], (i / kTcStages) & 1) || !mbar_wait(&p_full[s], (i >> 1) & 1)) return false;
+      bool ok = mbar_wait(q_ready, 0) && mbar_wait(&k_init[0], 0);
+      if (ok) {
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(pbuf + s * kTcPBytes);
+        issue_s(0);
+        if (nt > 1) {
+          ok = mbar_wait(&k_init[1], 0);
+          tc_fence_after();
+          if (ok) issue_s(1);
+        }
+      }
+      for (int gi = 0; gi < nt && ok; ++gi) {
+        if (!mbar_wait(&go[gi % kTcGo], (gi / kTcGo) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (gi + 2 < nt) issue_s(gi + 2);
+        // O_s += P_gi V_gi
+        const int st = gi % kTcStages, s = gi & 1, pb = s * 2 + ((gi >> 1) & 1);
+        const uint32_t p_tm = tmem_base + kTcPCol + pb * 32;
         const uint32_t v_addr = smem_u32(vbuf + st * kTcKVBytes);
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk)
-          umma_f16(tmem_base + 128 + s * 128, sdesc_kmajor_sw128(p_addr + kk * 32),
-                   sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcKeys * 128), idesc_o, (i >= 2 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[s]);
+          umma_f16_ts(tmem_base + 128 + s * 128, p_tm + kk * 8, sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcKeys * 128),
+                      idesc_o, (gi >= 2 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[pb]);
         umma_commit(&v_empty[st]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && nt > 1) ok = issue_s(1);
-      for (int i = 0; i < nt && ok; ++i) {
-        if (i + 2 < nt && !issue_s(i + 2)) ok = false;
-        else if (!issue_pv(i)) ok = false;
       }
       if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
     }
@@ -477,11 +488,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_tm = tmem_base + lane_base + sidx * kTcKeys;
     const uint32_t o_tm = tmem_base + lane_base + 128 + sidx * 128;
-    uint8_t* p_smem = pbuf + sidx * kTcPBytes;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     int k = 0;  // tiles this stream has finished
     for (int i = sidx; i < nt; i += 2, ++k) {
+      uint64_t* gob = &go[i % kTcGo];
       if (!__all_sync(kAll, mbar_wait(&s_full[sidx], k & 1))) {
         ok = false;
         break;
@@ -491,7 +502,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_ld64(s_tm, sv);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[sidx]);
+      if (lane == 0) mbar_arrive(gob);  // S_i read: its buffer may take S_{i+2}
       const int j0 = (t_begin + i) * kTcKeys;
       if (j0 + kTcKeys - 1 > prow) {
 #pragma unroll
@@ -512,7 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (__any_sync(kAll, grow)) {
         const float m_new = grow ? tmax : m;
         if (k > 0) {  // O_s holds this stream's tiles so far: wait for the last P.V, then scale
-          if (!__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) {
+          if (!__all_sync(kAll, mbar_wait(&pv_done[sidx * 2 + ((k - 1) & 1)], ((k - 1) >> 1) & 1))) {
             ok = false;
             break;
           }
@@ -530,36 +541,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         m = m_new;
       }
-      // this stream's P buffer was read by its previous P.V
-      if (k > 0 && !__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) {
+      // P buffer k & 1 was last read by the P.V of this stream's tile k - 2
+      const int pb = sidx * 2 + (k & 1);
+      if (k >= 2 && !__all_sync(kAll, mbar_wait(&pv_done[pb], ((k - 2) >> 1) & 1))) {
         ok = false;
         break;
       }
       const float nm = (m == -INFINITY) ? 0.f : -m;  // m = -inf only when every key so far is masked
       float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float pv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) pv[e] = fast_exp2(fmaf(sv[ch * 8 + e], scale_log2, nm));
-        rs0 += pv[0] + pv[4];
-        rs1 += pv[1] + pv[5];
-        rs2 += pv[2] + pv[6];
-        rs3 += pv[3] + pv[7];
-        uint4 u;
-        u.x = pack_bf16x2(pv[0], pv[1]);
-        u.y = pack_bf16x2(pv[2], pv[3]);
-        u.z = pack_bf16x2(pv[4], pv[5]);
-        u.w = pack_bf16x2(pv[6], pv[7]);
-        *reinterpret_cast<uint4*>(p_smem + sw128_off(rho, ch)) = u;
+      for (int e = 0; e < 32; e += 2) {
+        const float p0 = fast_exp2(fmaf(sv[2 * e], scale_log2, nm));
+        const float p1 = fast_exp2(fmaf(sv[2 * e + 1], scale_log2, nm));
+        const float p2 = fast_exp2(fmaf(sv[2 * e + 2], scale_log2, nm));
+        const float p3 = fast_exp2(fmaf(sv[2 * e + 3], scale_log2, nm));
+        rs0 += p0;
+        rs1 += p1;
+        rs2 += p2;
+        rs3 += p3;
+        pk[e] = pack_bf16x2(p0, p1);  // key 2e in the low half
+        pk[e + 1] = pack_bf16x2(p2, p3);
       }
       l += (rs0 + rs1) + (rs2 + rs3);
-      fence_proxy_async_smem();
+      tmem_st32u(tmem_base + lane_base + kTcPCol + pb * 32, pk);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sidx]);
+      if (lane == 0) mbar_arrive(gob);  // P_i written
     }
-    if (ok && k > 0 && !__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) ok = false;
+    if (ok && k > 0 && !__all_sync(kAll, mbar_wait(&pv_done[sidx * 2 + ((k - 1) & 1)], ((k - 1) >> 1) & 1))) ok = false;
     if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
     // ---- merge the two streams; stream s writes output columns [64 s, 64 s + 64)
     ml_x[sidx * 128 + rho] = ok ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
