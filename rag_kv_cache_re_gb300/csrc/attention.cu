@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
 //   warp 0     TMA producer for K: tiles of 64 keys (two 64-column boxes, 128B swizzle)
 //              into a 4-stage ring; a stage is freed by the Q.K^T that read it
 //   warp 1     TMEM allocation; one thread issues the tensor-core work in groups:
-//              group g = { S_{g+2} = Q K_{g+2}^T (M=128, N=64, K=128),
+//              group g = { S_{g+2} = Q K_{g+2}^T (M=128, N=64, K=128; Q read from TMEM),
 //                          O_s += P_g V_g (M=128, N=128, K=64 keys; P read from TMEM,
 //                          V MN-major from shared memory) },
 //              after S_0 and S_1.  Every dependency of group g lands on one mbarrier,
@@ -300,8 +300,9 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
 //              small MMAs, so fewer reads keep the tensor pipe fed.
 //   warp 2     TMA producer for V: the same tiling, its own 4-stage ring, freed by P.V
 //   warps 3-10 two softmax streams of four warps; stream s owns the key tiles i = s
-//              (mod 2) of the CTA's range with its own S buffer, two P buffers and an
-//              O accumulator.  One score row per thread: causal mask by true position
+//              (mod 2) of the CTA's range with its own S buffer, P buffer and O
+//              accumulator; stream s also stores columns [64 s, 64 s + 64) of the Q
+//              rows into TMEM.  One score row per thread: causal mask by true position
 //              (boundary tiles only), online softmax in the exp2 domain with the scale
 //              folded into one FFMA, P stored to TMEM as packed bf16 pairs, O_s rescaled
 //              in TMEM only when a row max grows by more than 2^8.  The streams are
@@ -309,17 +310,20 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
 //              end (common max, rescale, sum): the algebra of merging split-KV partials.
 // Group g's barrier go[g % 8] completes when: K_{g+2} has landed (or there is none), V_g
 // has landed, and the four warps of stream g % 2 have read S_g and written P_g.
+// Q and P live in TMEM rather than shared memory: every Q.K^T would otherwise re-read
+// the 4 KB Q slice from shared memory, and shared-memory bandwidth (operand reads plus
+// the TMA writes of K and V) is what bounds these small MMAs.
 // TMEM columns: S_s at [64 s, 64 s + 64); O_s at [128 + 128 s, 256 + 128 s);
-// P_{s,b} at [384 + 64 s + 32 b, 416 + 64 s + 32 b) (64 bf16 keys in 32 columns).
+// Q at [384, 448) (128 bf16 per row in 64 columns); P_s at [448 + 32 s, 480 + 32 s).
 constexpr int kTcKeys = 64;
 constexpr int kTcStages = 4;
 constexpr int kTcGo = 8;                       // group barriers in flight
 constexpr int kTcThreads = 352;
-constexpr int kTcQBytes = 128 * 128 * 2;       // Q tile: 2 atoms of 128 rows x 64 columns
 constexpr int kTcKVBytes = kTcKeys * 128 * 2;  // one K or V tile: 2 boxes of 64 keys x 64 columns
 constexpr int kTcMlBytes = 2 * 128 * 8;        // per-stream (m, l) of every row, for the merge
-constexpr int kTcSmem = kTcQBytes + 2 * kTcStages * kTcKVBytes + kTcMlBytes + 256 + 1024;
-constexpr uint32_t kTcPCol = 384;              // first TMEM column of the P buffers
+constexpr int kTcSmem = 2 * kTcStages * kTcKVBytes + kTcMlBytes + 256 + 1024;
+constexpr uint32_t kTcQCol = 384;              // first TMEM column of Q
+constexpr uint32_t kTcPCol = 448;              // first TMEM column of the P buffers
 constexpr uint32_t kTcGoCount = 10;            // K producer + V producer + 4 (S read) + 4 (P written)
 
 // Barrier 1 over the 256 softmax threads (barrier 0 is __syncthreads).
@@ -336,8 +340,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint8_t* qbuf = smem;
-  uint8_t* kbuf = smem + kTcQBytes;  // stage st at st * KV
+  uint8_t* kbuf = smem;  // stage st at st * KV
   uint8_t* vbuf = kbuf + kTcStages * kTcKVBytes;
   float2* ml_x = reinterpret_cast<float2*>(vbuf + kTcStages * kTcKVBytes);  // [stream][row]
   uint64_t* go = reinterpret_cast<uint64_t*>(vbuf + kTcStages * kTcKVBytes + kTcMlBytes);
@@ -345,8 +348,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* k_empty = k_init + 2;
   uint64_t* v_empty = k_empty + kTcStages;
   uint64_t* s_full = v_empty + kTcStages;  // [stream]
-  uint64_t* pv_done = s_full + 2;          // [stream * 2 + P buffer]
-  uint64_t* q_ready = pv_done + 4;
+  uint64_t* pv_done = s_full + 2;          // [stream]
+  uint64_t* q_ready = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -368,11 +371,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&k_init[b], 1);
       mbar_init(&s_full[b], 1);
+      mbar_init(&pv_done[b], 1);
     }
     for (int st = 0; st < kTcStages; ++st) {
       mbar_init(&k_empty[st], 1);
       mbar_init(&v_empty[st], 1);
-      mbar_init(&pv_done[st], 1);  // four P buffers, like the four stages
     }
     mbar_init(q_ready, 8);
     fence_mbar_init();
@@ -418,16 +421,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTcKeys, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
-      const uint32_t q_addr = smem_u32(qbuf);
-      auto issue_s = [&](int i) {  // S_{i % 2} = Q K_i^T
+      auto issue_s = [&](int i) {  // S_{i % 2} = Q K_i^T, Q from TMEM
         const int st = i % kTcStages, s = i & 1;
         const uint32_t k_addr = smem_u32(kbuf + st * kTcKVBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_q = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
           const uint32_t off_k = (kk >> 2) * (kTcKeys * 128) + (kk & 3) * 32;
-          umma_f16(tmem_base + s * kTcKeys, sdesc_kmajor_sw128(q_addr + off_q), sdesc_kmajor_sw128(k_addr + off_k),
-                   idesc_s, kk > 0 ? 1u : 0u);
+          umma_f16_ts(tmem_base + s * kTcKeys, tmem_base + kTcQCol + kk * 8, sdesc_kmajor_sw128(k_addr + off_k), idesc_s,
+                      kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[s]);
         umma_commit(&k_empty[st]);
@@ -450,14 +451,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         if (gi + 2 < nt) issue_s(gi + 2);
         // O_s += P_gi V_gi
-        const int st = gi % kTcStages, s = gi & 1, pb = s * 2 + ((gi >> 1) & 1);
-        const uint32_t p_tm = tmem_base + kTcPCol + pb * 32;
+        const int st = gi % kTcStages, s = gi & 1;
+        const uint32_t p_tm = tmem_base + kTcPCol + s * 32;
         const uint32_t v_addr = smem_u32(vbuf + st * kTcKVBytes);
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk)
           umma_f16_ts(tmem_base + 128 + s * 128, p_tm + kk * 8, sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcKeys * 128),
                       idesc_o, (gi >= 2 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[pb]);
+        umma_commit(&pv_done[s]);
         umma_commit(&v_empty[st]);
       }
       if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
@@ -474,18 +475,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int h = g * G + hh;
     if (check && sidx == 0 && valid && (prow < 0 || prow >= T || (r > 0 && pos[r - 1] >= prow)))
       flag_status(status, QCF_DEV_BAD_INDEX);
-    {  // stream s stores the 64-column atom s of its Q row, 128B-swizzled K-major
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    {  // stream s stores Q columns [64 s, 64 s + 64) of its row into TMEM as 32 packed bf16 pairs
       const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(valid ? r : 0) * Hq + h) * D) + sidx * 8;
+      uint32_t w[32];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(qbuf + sidx * (128 * 128) + sw128_off(rho, ch)) = v;
+        w[4 * ch] = v.x;
+        w[4 * ch + 1] = v.y;
+        w[4 * ch + 2] = v.z;
+        w[4 * ch + 3] = v.w;
       }
-      fence_proxy_async_smem();
+      tmem_st32u(tmem_base + lane_base + kTcQCol + sidx * 32, w);
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_tm = tmem_base + lane_base + sidx * kTcKeys;
     const uint32_t o_tm = tmem_base + lane_base + 128 + sidx * 128;
     float m = -INFINITY, l = 0.f;
@@ -523,7 +529,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (__any_sync(kAll, grow)) {
         const float m_new = grow ? tmax : m;
         if (k > 0) {  // O_s holds this stream's tiles so far: wait for the last P.V, then scale
-          if (!__all_sync(kAll, mbar_wait(&pv_done[sidx * 2 + ((k - 1) & 1)], ((k - 1) >> 1) & 1))) {
+          if (!__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) {
             ok = false;
             break;
           }
@@ -541,9 +547,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         m = m_new;
       }
-      // P buffer k & 1 was last read by the P.V of this stream's tile k - 2
-      const int pb = sidx * 2 + (k & 1);
-      if (k >= 2 && !__all_sync(kAll, mbar_wait(&pv_done[pb], ((k - 2) >> 1) & 1))) {
+      // the P buffer was last read by the P.V of this stream's previous tile
+      if (k >= 1 && !__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) {
         ok = false;
         break;
       }
@@ -564,12 +569,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         pk[e + 1] = pack_bf16x2(p2, p3);
       }
       l += (rs0 + rs1) + (rs2 + rs3);
-      tmem_st32u(tmem_base + lane_base + kTcPCol + pb * 32, pk);
+      tmem_st32u(tmem_base + lane_base + kTcPCol + sidx * 32, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(gob);  // P_i written
     }
-    if (ok && k > 0 && !__all_sync(kAll, mbar_wait(&pv_done[sidx * 2 + ((k - 1) & 1)], ((k - 1) >> 1) & 1))) ok = false;
+    if (ok && k > 0 && !__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) ok = false;
     if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
     // ---- merge the two streams; stream s writes output columns [64 s, 64 s + 64)
     ml_x[sidx * 128 + rho] = ok ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
