@@ -337,6 +337,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           float2* __restrict__ part_ml, unsigned int* status, int check) {
   constexpr int D = 128;
   constexpr unsigned kAll = 0xffffffffu;
+  pdl_wait();  // q, pos and the cache come from the kernels before this one
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -636,6 +638,8 @@ template <int D>
 __global__ void attn_combine_kernel(const int32_t* __restrict__ pos, int n, int Hq, int BR, int split_tiles,
                                     int max_splits, const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= n * Hq) return;
@@ -706,7 +710,7 @@ size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D) {
 template <int D>
 static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,
                                 const __nv_bfloat16* V, int T, int Hq, int Hkv, float scale, __nv_bfloat16* o,
-                                float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc) {
+                                float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc, bool pdl) {
   using Cfg = AttnCfg<D>;
   const AttnPlan plan = plan_attn(n, T, Hq, Hkv, D);
   const int G = plan.G;
@@ -745,9 +749,16 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
     });
     if (attr_tc != cudaSuccess) return cuda_error(attr_tc, "sparse_causal_attn: smem attribute");
     LaunchScope ls(kc, st);
-    sparse_attn_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o, lse,
-                                                              plan.split_tiles, plan.max_splits, part_o, part_ml,
-                                                              device_status_ptr(), check_enabled() ? 1 : 0);
+    if (pdl) {
+      cudaError_t e = launch_pdl(sparse_attn_tc_kernel, grid, dim3(kTcThreads), kTcSmem, st, tk, tv, q, pos, n, T, Hq,
+                                 Hkv, G, BR, scale_log2, o, lse, plan.split_tiles, plan.max_splits, part_o, part_ml,
+                                 device_status_ptr(), check_enabled() ? 1 : 0);
+      if (e != cudaSuccess) return cuda_error(e, "sparse_causal_attn: launch");
+    } else {
+      sparse_attn_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o, lse,
+                                                                plan.split_tiles, plan.max_splits, part_o, part_ml,
+                                                                device_status_ptr(), check_enabled() ? 1 : 0);
+    }
   } else {
     LaunchScope ls(kc, st);
     sparse_attn_kernel<D><<<grid, warps * 32, Cfg::SMEM_BYTES, st>>>(
@@ -757,8 +768,14 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
   if (plan.max_splits > 1) {
     LaunchScope ls(kc == KC_ATTN ? KC_ATTN_COMBINE : kc, st);
     const int warps_total = n * Hq;
-    attn_combine_kernel<D><<<(warps_total + 7) / 8, 256, 0, st>>>(pos, n, Hq, BR, plan.split_tiles, plan.max_splits, part_o,
-                                                                  part_ml, o, lse);
+    if (pdl) {
+      cudaError_t e = launch_pdl(attn_combine_kernel<D>, dim3((warps_total + 7) / 8), dim3(256), 0, st, pos, n, Hq, BR,
+                                 plan.split_tiles, plan.max_splits, part_o, part_ml, o, lse);
+      if (e != cudaSuccess) return cuda_error(e, "sparse_causal_attn: combine launch");
+    } else {
+      attn_combine_kernel<D><<<(warps_total + 7) / 8, 256, 0, st>>>(pos, n, Hq, BR, plan.split_tiles, plan.max_splits,
+                                                                    part_o, part_ml, o, lse);
+    }
   }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "sparse_causal_attn: launch");
@@ -766,12 +783,12 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
 
 qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K, const __nv_bfloat16* V,
                        int T, int Hq, int Hkv, int D, float scale, __nv_bfloat16* o, float* lse, void* ws,
-                       size_t ws_bytes, cudaStream_t st, KernelClass kc) {
+                       size_t ws_bytes, cudaStream_t st, KernelClass kc, bool pdl) {
   if (n <= 0) return QCF_OK;
-  switch (D) {
-    case 16: return attn_launch_d<16>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc);
-    case 64: return attn_launch_d<64>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc);
-    case 128: return attn_launch_d<128>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc);
+  switch (D) {  // the warp-MMA kernel (D = 16, 64) is launched plainly; its combine may still be programmatic
+    case 16: return attn_launch_d<16>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl);
+    case 64: return attn_launch_d<64>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl);
+    case 128: return attn_launch_d<128>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl);
     default: return set_error(QCF_ERR_SHAPE, "sparse_causal_attn: head dim %d unsupported", D);
   }
 }

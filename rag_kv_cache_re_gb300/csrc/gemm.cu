@@ -347,30 +347,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      auto load_w = [&](uint8_t* a_s, int kb, int nt, uint64_t* bar) {
+        if constexpr (BMN) {   // W stored [K][N]: BN/64 boxes of 64 K rows x 64 N columns
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(a_s + Cfg::A_BYTES + j * (kBK * 128), &tmB, bar, nt * BN + j * 64, kb * kBK);
+        } else {
+          tma_load_2d(a_s + Cfg::A_BYTES, &tmB, bar, kb * kBK, nt * BN);
+        }
+      };
+      // The weights are never written by the kernels a programmatic launch overlaps,
+      // so the first unit's weight stages are requested before waiting for them;
+      // the activation half of each of those stages follows the wait.
+      int npre = 0;
+      if (static_cast<int>(blockIdx.x) < units) {
+        int mt, nt, sp;
+        decode(blockIdx.x, mt, nt, sp);
+        const int kb0 = static_cast<int>(static_cast<long long>(kb_total) * sp / splits);
+        const int kb1 = static_cast<int>(static_cast<long long>(kb_total) * (sp + 1) / splits);
+        npre = min(Cfg::STAGES, kb1 - kb0);
+        for (int j = 0; j < npre; ++j) {
+          mbar_arrive_expect_tx(&full[j], Cfg::STAGE_BYTES);
+          load_w(smem + j * Cfg::STAGE_BYTES, kb0 + j, nt, &full[j]);
+        }
+      }
+      pdl_wait();
+      pdl_launch_dependents();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int issued = 0;  // k blocks loaded so far; the first npre had their weights requested above
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         int mt, nt, sp;
         decode(u, mt, nt, sp);
         const int kb0 = static_cast<int>(static_cast<long long>(kb_total) * sp / splits);
         const int kb1 = static_cast<int>(static_cast<long long>(kb_total) * (sp + 1) / splits);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u)) {
-            flag_status(status, QCF_DEV_TIMEOUT);
-            ok = false;
-            break;
-          }
+        for (int kb = kb0; kb < kb1; ++kb, ++issued) {
           uint8_t* a_s = smem + stage * Cfg::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-          tma_load_2d(a_s, &tmA, &full[stage], kb * kBK, mt * kBM);
-          if constexpr (BMN) {   // W stored [K][N]: BN/64 boxes of 64 K rows x 64 N columns
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(a_s + Cfg::A_BYTES + j * (kBK * 128), &tmB, &full[stage], nt * BN + j * 64, kb * kBK);
-          } else {
-            tma_load_2d(a_s + Cfg::A_BYTES, &tmB, &full[stage], kb * kBK, nt * BN);
+          if (issued >= npre) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+              flag_status(status, QCF_DEV_TIMEOUT);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+            load_w(a_s, kb, nt, &full[stage]);
           }
+          tma_load_2d(a_s, &tmA, &full[stage], kb * kBK, mt * kBM);
           if (++stage == Cfg::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -428,6 +451,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
     float* my_tile = epi_tiles + (warp - 2) * (32 * 33);
+    pdl_wait();  // the residual, position tables and output buffers come from earlier kernels
+    pdl_launch_dependents();
     int local = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
       int mt, nt, sp;
@@ -573,7 +598,8 @@ size_t gemm_workspace_size(int M, int N, int K) {
 
 template <int BN, int EPI, int HD, bool BMN = false>
 static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int splits,
-                             const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st, int units) {
+                             const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st, int units,
+                             bool pdl) {
   using Cfg = GemmCfg<BN>;
   auto kern = gemm_tcgen05_kernel<BN, EPI, HD, BMN>;
   static std::once_flag once;
@@ -583,20 +609,26 @@ static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M
   });
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "gemm: shared memory attribute");
   const int grid = units < num_sms() ? units : num_sms();
-  kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, st>>>(ta, tb, M, N, K, splits, ep, part, cnt, device_status_ptr());
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (pdl) {
+    e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg::SMEM_BYTES, st, ta, tb, M, N, K, splits, ep, part, cnt,
+                   device_status_ptr());
+  } else {
+    kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, st>>>(ta, tb, M, N, K, splits, ep, part, cnt, device_status_ptr());
+    e = cudaGetLastError();
+  }
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "gemm: launch");
 }
 
 template <int BN>
 static qcf_status dispatch_kn(EpiKind epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
                               int splits, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
-                              int units) {
+                              int units, bool pdl) {
   if constexpr (BN >= 64) {
     if (epi == EPI_STORE_BF16)
-      return launch_cfg<BN, EPI_STORE_BF16, 0, true>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+      return launch_cfg<BN, EPI_STORE_BF16, 0, true>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
     if (epi == EPI_ADD_F32)
-      return launch_cfg<BN, EPI_ADD_F32, 0, true>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+      return launch_cfg<BN, EPI_ADD_F32, 0, true>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
   }
   return set_error(QCF_ERR_UNSUPPORTED, "gemm: [K][N] weights support the store and add epilogues only");
 }
@@ -604,25 +636,26 @@ static qcf_status dispatch_kn(EpiKind epi, const CUtensorMap& ta, const CUtensor
 template <int BN>
 static qcf_status dispatch_epi(EpiKind epi, int hd, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
                                int splits, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
-                               int units) {
+                               int units, bool pdl) {
   switch (epi) {
-    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0, false>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
-    case EPI_ADD_F32: return launch_cfg<BN, EPI_ADD_F32, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0, false>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
+    case EPI_ADD_F32: return launch_cfg<BN, EPI_ADD_F32, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
     case EPI_SWIGLU:
-      if constexpr (BN >= 128) return launch_cfg<BN, EPI_SWIGLU, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+      if constexpr (BN >= 128) return launch_cfg<BN, EPI_SWIGLU, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
       break;
     case EPI_QKV_ROPE:
-      if (hd == 16) return launch_cfg<BN, EPI_QKV_ROPE, 16>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
-      if (hd == 64) return launch_cfg<BN, EPI_QKV_ROPE, 64>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+      if (hd == 16) return launch_cfg<BN, EPI_QKV_ROPE, 16>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
+      if (hd == 64) return launch_cfg<BN, EPI_QKV_ROPE, 64>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
       if constexpr (BN >= 128)
-        if (hd == 128) return launch_cfg<BN, EPI_QKV_ROPE, 128>(ta, tb, M, N, K, splits, ep, part, cnt, st, units);
+        if (hd == 128) return launch_cfg<BN, EPI_QKV_ROPE, 128>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
       break;
   }
   return set_error(QCF_ERR_UNSUPPORTED, "gemm: no kernel for epilogue %d, BN %d, head dim %d", epi, BN, hd);
 }
 
 qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const __nv_bfloat16* W, int N,
-                       const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc, bool w_kn) {
+                       const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc, bool w_kn,
+                       bool pdl) {
   if (M <= 0) return QCF_OK;
   if (K % kBK || N % 64 || K <= 0 || N <= 0) return set_error(QCF_ERR_SHAPE, "gemm: K=%d N=%d (K%%64, N%%64 required)", K, N);
   const int hd = epi == EPI_QKV_ROPE ? ep.D : 16;
@@ -647,15 +680,15 @@ qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const 
   LaunchScope ls(kc, st);
   if (w_kn) {
     switch (p.BN) {
-      case 256: return dispatch_kn<256>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
-      case 128: return dispatch_kn<128>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
-      default: return dispatch_kn<64>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
+      case 256: return dispatch_kn<256>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
+      case 128: return dispatch_kn<128>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
+      default: return dispatch_kn<64>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
     }
   }
   switch (p.BN) {
-    case 256: return dispatch_epi<256>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
-    case 128: return dispatch_epi<128>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
-    default: return dispatch_epi<64>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units);
+    case 256: return dispatch_epi<256>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
+    case 128: return dispatch_epi<128>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
+    default: return dispatch_epi<64>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
   }
 }
 

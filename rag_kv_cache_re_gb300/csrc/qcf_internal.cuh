@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "../../include/qcf.h"
 
@@ -51,9 +52,30 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Device SM count (cached per device).
 int num_sms();
 
+// Programmatic dependent launch.  A kernel launched this way may start while its
+// predecessor in the stream drains (set-up of barriers, tensor memory and constant
+// operands overlaps the predecessor's tail); it must execute pdl_wait() before it
+// touches anything the predecessor (or earlier work) produced.  Only kernels that do
+// so are launched with it.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Internal launchers (no argument checks; callers validated).
 cudaError_t launch_rmsnorm(const float* x, int n, int d, const __nv_bfloat16* g, float eps,
-                           __nv_bfloat16* h, cudaStream_t st);
+                           __nv_bfloat16* h, cudaStream_t st, bool pdl = false);
 
 // GEMM epilogue parameters (gemm.cu).
 enum EpiKind { EPI_STORE_BF16 = 0, EPI_ADD_F32 = 1, EPI_QKV_ROPE = 2, EPI_SWIGLU = 3 };
@@ -74,7 +96,7 @@ struct EpiParams {
 size_t gemm_workspace_size(int M, int N, int K);
 qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const __nv_bfloat16* W, int N,
                        const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc,
-                       bool w_kn = false);
+                       bool w_kn = false, bool pdl = false);
 
 // Row kernels (rows.cu).
 cudaError_t launch_embed(const __nv_bfloat16* embed, int vocab, int d, const int32_t* ids, const int32_t* rows,
@@ -89,7 +111,8 @@ cudaError_t launch_reposition(const __nv_bfloat16* src, __nv_bfloat16* dst, int6
 size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D);
 qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,
                        const __nv_bfloat16* V, int T, int Hq, int Hkv, int D, float scale, __nv_bfloat16* o,
-                       float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc = KC_ATTN);
+                       float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc = KC_ATTN,
+                       bool pdl = false);
 
 // ------------------------------------------------------------------ device side
 
@@ -100,6 +123,12 @@ __device__ __forceinline__ uint64_t globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Waits until the grids this one depends on have completed and their writes are
+// visible (a no-op for a kernel launched without programmatic serialization).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream, if launched programmatically, start its set-up.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

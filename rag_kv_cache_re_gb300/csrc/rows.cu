@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __re
                                                                const __nv_bfloat16* __restrict__ g, float eps,
                                                                __nv_bfloat16* __restrict__ h) {
   __shared__ float red[kNormThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.x;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(row) * d);
@@ -276,9 +278,10 @@ cudaError_t launch_lm_head(const qcf_model* m, const float* x_last, float* logit
 }
 
 cudaError_t launch_rmsnorm(const float* x, int n, int d, const __nv_bfloat16* g, float eps, __nv_bfloat16* h,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool pdl) {
   if (n <= 0) return cudaSuccess;
   LaunchScope ls(KC_RMSNORM, st);
+  if (pdl) return launch_pdl(rmsnorm_kernel, dim3(n), dim3(kNormThreads), 0, st, x, n, d, g, eps, h);
   rmsnorm_kernel<<<n, kNormThreads, 0, st>>>(x, n, d, g, eps, h);
   return cudaGetLastError();
 }

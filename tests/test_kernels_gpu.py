@@ -201,7 +201,9 @@ def test_sparse_causal_attn(Q, T, n, Hq, Hkv, D, pattern):
 # ----------------------------------------------------------------- dense pieces
 
 @pytest.mark.parametrize("M,N,K", [(23, 192, 64), (1, 64, 64), (300, 384, 192), (832, 6144, 4096), (832, 4096, 4096), (832, 28672, 4096),
-                                   (64, 4096, 14336), (832, 4096, 14336), (200, 28672, 256)])
+                                   (64, 4096, 14336), (832, 4096, 14336), (200, 28672, 256),
+                                   # two 128-row tiles, the second ragged
+                                   (129, 6144, 4096), (144, 28672, 4096), (144, 4096, 4096), (256, 4096, 14336)])
 def test_linear_store_and_add(Q, M, N, K):
     A = qd.normal_bf16((M, K), 1.0, 31, DEV)
     W = qd.normal_bf16((N, K), 0.02, 32, DEV)

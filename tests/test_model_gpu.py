@@ -72,6 +72,12 @@ def test_layer_forward_8b_layer_shape(M, Q):
     _layer_case(M, Q, spec, n_sel=768, T=5184, Cx=5120, seed=42)
 
 
+def test_layer_forward_8b_two_row_tiles(M, Q):
+    # 144 rows: two 128-row GEMM tiles, the second holding 16 rows
+    spec = dataclasses.replace(qd.LLAMA8B, n_layers=1, vocab=512)
+    _layer_case(M, Q, spec, n_sel=80, T=5184, Cx=5120, seed=43)
+
+
 def test_full_prefill_tiny(M, Q):
     weights = qd.ModelWeights(qd.TINY)
     dm = M.DeviceModel(weights, DEV, max_pos=256)
