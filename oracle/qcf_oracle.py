@@ -20,7 +20,11 @@ What it computes, step by step in the pages' order:
 * per-layer selective recompute of the selected rows with location-aware
   causal attention over the fused cache (*QCFuse*, section 2.A "pipelined cache
   reconstruction" and its sparse attention kernel; *KVCache reuse 01*, section
-  1.3.4 "selective recompute flow").
+  1.3.4 "selective recompute flow");
+* the selector variants the pages compare against: QCLast (profiling at the
+  last layer) and QCAll (query-aware profiling at every layer), *QCFuse*,
+  section 4 "Results"; CacheBlend's KV-deviation selection with gradual
+  filtering across layers (*KVCache reuse 01*, sections 1.3.2-1.3.4).
 
 Precision: matmuls in fp32; RoPE angles, softmax normalisers, score sums,
 RMSNorm statistics and the final logits in fp64.  Stored chunk K/V can be
@@ -35,6 +39,15 @@ from basis points; ties go to the lower index; one selection is reused at every
 layer; query rows are always recomputed; RoPE is rotate-half with
 omega_k = theta^(-2k/D); re-rotation applies R(offset) to the stored key;
 fresh K/V of the recomputed rows are written into the cache before attention.
+QCLast is the critical-layer selector with crit = L-1; QCAll keeps the anchors,
+runs the probe through layers 0..L-2 and sums the per-layer profile scores of
+all L layers (each layer's q from the probe against that layer's re-rotated
+keys), then selects once.  HKVD: a token's KV deviation at a layer is the
+squared L2 distance between its fresh and its reused K and V over all KV heads
+(the ranking of the L2 distance); at layer 0 every context token is measured,
+at layer l the tokens kept after layer l-1; the kept set at layer l is the
+top ceil(r_l*C) of those by deviation (ties to the lower position), and only
+the kept rows and the query get fresh K/V, attention and MLP at that layer.
 
 Parity unpinned against the pages for those readings: no printed value decides
 them.  The tests pin the arithmetic to closed forms, library routines and the
@@ -327,14 +340,15 @@ def topn_select(scores: np.ndarray, N: int) -> np.ndarray:
 
 def anchor_probe(model: OracleModel, query_ids: np.ndarray, anchor_K: List[np.ndarray],
                  anchor_V: List[np.ndarray], anchor_delta: np.ndarray, context_len: int,
-                 crit: int) -> np.ndarray:
+                 crit: int, collect_q: Optional[List[np.ndarray]] = None) -> np.ndarray:
     """Context-aware query representation at the critical layer (*QCFuse* 2.A).
 
     The query rows (absolute positions C..C+Q-1) run layers 0..crit-1 with a KV
     prefix made of the anchors' stored K/V (K re-rotated by its chunk offset to
     its absolute position); query row i attends to every anchor and to query
     rows <= i.  At layer `crit` only RMSNorm, W_q and RoPE run: returns q_crit
-    [Q][Hq][D].  anchor_K/V: per layer l < crit, [nA][Hkv][D].
+    [Q][Hq][D].  anchor_K/V: per layer l < crit, [nA][Hkv][D].  `collect_q`,
+    when given, receives the post-RoPE q of every probe layer l < crit.
     """
     s = model.spec
     Q = len(query_ids)
@@ -348,7 +362,10 @@ def anchor_probe(model: OracleModel, query_ids: np.ndarray, anchor_K: List[np.nd
         if nA:
             Kc[:nA] = rope_reposition(anchor_K[l], anchor_delta, s.theta)
             Vc[:nA] = anchor_V[l]
-        x = layer_forward(x, model.layer(l), s, qpos, rows, Kc, Vc)
+        cap: Dict[str, np.ndarray] = {}
+        x = layer_forward(x, model.layer(l), s, qpos, rows, Kc, Vc, capture=cap)
+        if collect_q is not None:
+            collect_q.append(cap["q"])
     W = model.layer(crit)
     h = rmsnorm(x, W["g_attn"], s.eps)
     q = (h @ W["wq"].T).reshape(Q, s.n_heads, s.head_dim)
@@ -358,7 +375,8 @@ def anchor_probe(model: OracleModel, query_ids: np.ndarray, anchor_K: List[np.nd
 def fused_prefill(model: OracleModel, chunk_kv: List[Dict[str, np.ndarray]], context_ids: np.ndarray,
                   chunk_start: np.ndarray, query_ids: np.ndarray, crit: int, ratio_bp: int,
                   n_anchor: int, forced_sel: Optional[np.ndarray] = None,
-                  keep_layers: bool = True, layers: Optional[int] = None) -> Dict[str, object]:
+                  keep_layers: bool = True, layers: Optional[int] = None,
+                  selector: str = "critical") -> Dict[str, object]:
     """The whole fused prefill of one request.
 
     chunk_kv[c] holds the stored K, V [L][L_c][Hkv][D] of the c-th retrieved
@@ -374,6 +392,9 @@ def fused_prefill(model: OracleModel, chunk_kv: List[Dict[str, np.ndarray]], con
        embeddings) with their fresh K/V written into the cache first;
     6. logits of the last query row and the first token.
     `layers` truncates step 5 (for timing samples); then no logits are produced.
+    selector "critical" profiles at `crit` (QCLast: crit = L-1); "all" (QCAll)
+    keeps the anchors chosen at `crit`, runs the probe through layers 0..L-2 and
+    sums the profile scores of every layer before selecting.
     """
     s = model.spec
     C = int(chunk_start[-1])
@@ -387,12 +408,23 @@ def fused_prefill(model: OracleModel, chunk_kv: List[Dict[str, np.ndarray]], con
     anchors = keynorm_anchors(K_crit_stored, chunk_start, n_anchor)
     a_rows = np.concatenate([chunk_start[c] + anchors[c] for c in range(n_chunks)]).astype(np.int64)
     a_delta = row_delta[a_rows]
-    aK = [np.concatenate([chunk_kv[c]["K"][l][anchors[c]] for c in range(n_chunks)]) for l in range(crit)]
-    aV = [np.concatenate([chunk_kv[c]["V"][l][anchors[c]] for c in range(n_chunks)]) for l in range(crit)]
-    q_crit = anchor_probe(model, query_ids, aK, aV, a_delta, C, crit)
+    assert selector in ("critical", "all")
+    depth = crit if selector == "critical" else s.n_layers - 1   # probe layers before the last profiled one
+    aK = [np.concatenate([chunk_kv[c]["K"][l][anchors[c]] for c in range(n_chunks)]) for l in range(depth)]
+    aV = [np.concatenate([chunk_kv[c]["V"][l][anchors[c]] for c in range(n_chunks)]) for l in range(depth)]
+    q_layers: List[np.ndarray] = []
+    q_crit = anchor_probe(model, query_ids, aK, aV, a_delta, C, depth, collect_q=q_layers)
+    scale = 1.0 / np.sqrt(s.head_dim)
 
-    K_hat_crit = rope_reposition(K_crit_stored, row_delta, s.theta)
-    scores = profile_scores(q_crit, K_hat_crit, 1.0 / np.sqrt(s.head_dim))
+    def K_hat(l):
+        return rope_reposition(np.concatenate([ck["K"][l] for ck in chunk_kv], axis=0), row_delta, s.theta)
+
+    if selector == "critical":
+        scores = profile_scores(q_crit, K_hat(crit), scale)
+    else:   # QCAll: every layer's query-to-context profile, summed
+        scores = profile_scores(q_crit, K_hat(depth), scale)
+        for l in range(depth):
+            scores = scores + profile_scores(q_layers[l], K_hat(l), scale)
     N = num_selected(C, ratio_bp)
     sel = topn_select(scores, N) if forced_sel is None else np.sort(np.asarray(forced_sel, dtype=np.int64))
     S = np.concatenate([sel, np.arange(C, T)]).astype(np.int64)
@@ -417,4 +449,78 @@ def fused_prefill(model: OracleModel, chunk_kv: List[Dict[str, np.ndarray]], con
         out.update(lm_head_last(model, x[-1]))
     if keep_layers:
         out.update({"K": np.stack(K_f), "V": np.stack(V_f), "x_layers": xs})
+    return out
+
+
+# --------------------------------------------------------------------------- CacheBlend HKVD selection
+
+def kv_projection(x: np.ndarray, W: Dict[str, np.ndarray], spec, positions: np.ndarray):
+    """Fresh post-RoPE K and V of rows x at `positions` (the K/V part of a layer)."""
+    n = x.shape[0]
+    h = rmsnorm(x, W["g_attn"], spec.eps)
+    k = (h @ W["wk"].T).reshape(n, spec.n_kv_heads, spec.head_dim)
+    v = (h @ W["wv"].T).reshape(n, spec.n_kv_heads, spec.head_dim)
+    return rope_rotate(k, positions, spec.theta), v
+
+
+def kv_deviation(k: np.ndarray, v: np.ndarray, K_reused: np.ndarray, V_reused: np.ndarray) -> np.ndarray:
+    """Per row: squared L2 distance between fresh and reused K and V over all heads
+    (*KVCache reuse 01*, 1.3.2 "KV Deviation"), fp64."""
+    dk = np.asarray(k, dtype=F64) - np.asarray(K_reused, dtype=F64)
+    dv = np.asarray(v, dtype=F64) - np.asarray(V_reused, dtype=F64)
+    return (dk * dk).sum(axis=(1, 2)) + (dv * dv).sum(axis=(1, 2))
+
+
+def hkvd_prefill(model: OracleModel, chunk_kv: List[Dict[str, np.ndarray]], context_ids: np.ndarray,
+                 chunk_start: np.ndarray, query_ids: np.ndarray, layer_ratio_bp: Sequence[int],
+                 forced_layer_sel: Optional[List[np.ndarray]] = None,
+                 keep_layers: bool = True) -> Dict[str, object]:
+    """Fused prefill with CacheBlend's KV-deviation selection and gradual filtering
+    (*KVCache reuse 01*, 1.3.3 "three-level token selection" and 1.3.4).
+
+    Layer l measures the KV deviation of the context rows kept after layer l-1
+    (every context row at layer 0), keeps the top ceil(r_l*C) of them
+    (`layer_ratio_bp[l]`, non-increasing), gives those rows and the query fresh
+    K/V in the fused cache, and runs attention and the MLP for them only.
+    `forced_layer_sel[l]`, when given, replaces layer l's choice (positions,
+    ascending, a subset of the rows kept after layer l-1).
+    """
+    s = model.spec
+    C = int(chunk_start[-1])
+    Q = len(query_ids)
+    T = C + Q
+    row_delta = np.repeat(np.asarray(chunk_start[:-1], dtype=np.int64), np.diff(chunk_start))
+    ids_all = np.concatenate([np.asarray(context_ids), np.asarray(query_ids)]).astype(np.int64)
+    qrows = np.arange(C, T)
+    prev = np.arange(C)
+    x = model.embed_rows(ids_all[np.concatenate([prev, qrows])])
+    devs, sels, K_f, V_f = [], [], [], []
+    for l in range(s.n_layers):
+        W = model.layer(l)
+        Kc = np.zeros((T, s.n_kv_heads, s.head_dim), dtype=F32)
+        Vc = np.zeros_like(Kc)
+        Kc[:C] = rope_reposition(np.concatenate([ck["K"][l] for ck in chunk_kv]), row_delta, s.theta)
+        Vc[:C] = np.concatenate([ck["V"][l] for ck in chunk_kv])
+        pos_prev = np.concatenate([prev, qrows])
+        k, v = kv_projection(x, W, s, pos_prev)
+        dev = kv_deviation(k[:len(prev)], v[:len(prev)], Kc[prev], Vc[prev])
+        N = num_selected(C, int(layer_ratio_bp[l]))
+        assert N <= len(prev), "the ratio schedule must not increase"
+        if forced_layer_sel is None:
+            keep = topn_select(dev, N)
+        else:
+            keep = np.searchsorted(prev, np.asarray(forced_layer_sel[l], dtype=np.int64))
+            assert len(keep) == N and np.array_equal(prev[keep], np.sort(forced_layer_sel[l]))
+        keep_idx = np.concatenate([keep, len(prev) + np.arange(Q)])
+        rows = pos_prev[keep_idx]
+        x = layer_forward(x[keep_idx], W, s, rows, rows, Kc, Vc)
+        prev = prev[keep]
+        devs.append(dev)
+        sels.append(prev.copy())
+        if keep_layers:
+            K_f.append(Kc)
+            V_f.append(Vc)
+    out = {"layer_dev": devs, "layer_sel": sels, "sel": prev, "x": x, **lm_head_last(model, x[-1])}
+    if keep_layers:
+        out.update({"K": np.stack(K_f), "V": np.stack(V_f)})
     return out

@@ -7,6 +7,7 @@ brute-force loop on tiny inputs, or a special case the pages state:
   * full KV reuse only re-rotates stored keys (2.4);
   * ratio 1 recomputes everything, so fusion == full recompute.
 """
+import dataclasses
 import math
 import os
 
@@ -325,3 +326,127 @@ def test_round_bf16_matches_library():
                         np.array([1.00390625, 1.01171875, -2.0078125, 0.0, -0.0], np.float32)])
     want = torch.from_numpy(a).to(torch.bfloat16).float().numpy()
     np.testing.assert_array_equal(O.round_bf16(a), want)
+
+
+# ----------------------------------------------------------------- selector variants (QCLast, QCAll, HKVD)
+
+def _one_chunk_all_anchors(tiny):
+    chunks, start, q = tiny_request(n_chunks=1)
+    kv = [O.chunk_precompute(tiny, chunks[0], store_bf16=False)]
+    return chunks[0], start, q, kv
+
+
+def test_qclast_probe_is_the_real_query_at_the_last_layer(tiny):
+    # crit = L-1 with every token an anchor of the only chunk: q at the last layer is full prefill's q there.
+    ctx, start, q, kv = _one_chunk_all_anchors(tiny)
+    L = qd.TINY.n_layers
+    fused = O.fused_prefill(tiny, kv, ctx, start, q, crit=L - 1, ratio_bp=0, n_anchor=len(ctx))
+    full = O.full_prefill(tiny, np.concatenate([ctx, q]), capture_q_layer=L - 1)
+    np.testing.assert_allclose(fused["q_crit"], full["q"][len(ctx):], atol=5e-5)
+
+
+def test_qcall_scores_bruteforce_from_full_prefill(tiny):
+    # Same exact-probe setting: QCAll's scores are the sum over layers of each
+    # layer's softmax mass on every context key, from full prefill's q and K.
+    ctx, start, q, kv = _one_chunk_all_anchors(tiny)
+    s = qd.TINY
+    C, Qn, G = len(ctx), len(q), s.n_heads // s.n_kv_heads
+    fused = O.fused_prefill(tiny, kv, ctx, start, q, crit=1, ratio_bp=0, n_anchor=C, selector="all")
+    want = np.zeros(C)
+    for l in range(s.n_layers):
+        full = O.full_prefill(tiny, np.concatenate([ctx, q]), capture_q_layer=l)
+        ql, Kl = full["q"][C:].astype(np.float64), full["K"][l][:C].astype(np.float64)
+        for r in range(Qn):
+            for h in range(s.n_heads):
+                logit = [math.fsum(ql[r, h] * Kl[j, h // G]) / math.sqrt(s.head_dim) for j in range(C)]
+                mx = max(logit)
+                e = [math.exp(v - mx) for v in logit]
+                tot = math.fsum(e)
+                for j in range(C):
+                    want[j] += e[j] / tot
+    np.testing.assert_allclose(fused["scores"], want, rtol=2e-4, atol=1e-6)
+
+
+def test_qcall_invariants_and_one_layer_reduction():
+    s1 = dataclasses.replace(qd.TINY, n_layers=1)
+    m1 = O.OracleModel(qd.ModelWeights(s1))
+    chunks = [qd.chunk_tokens(c, 32, s1.vocab) for c in range(3)]
+    start = np.arange(4) * 32
+    q = qd.query_tokens(0, 8, s1.vocab)
+    kv = [O.chunk_precompute(m1, c) for c in chunks]
+    ctx = np.concatenate(chunks)
+    a = O.fused_prefill(m1, kv, ctx, start, q, crit=0, ratio_bp=2000, n_anchor=2, selector="all")
+    b = O.fused_prefill(m1, kv, ctx, start, q, crit=0, ratio_bp=2000, n_anchor=2)
+    np.testing.assert_allclose(a["scores"], b["scores"], atol=1e-12)   # one layer: all layers == the critical one
+    np.testing.assert_array_equal(a["sel"], b["sel"])
+    tiny2 = O.OracleModel(qd.ModelWeights(qd.TINY))
+    kv2 = [O.chunk_precompute(tiny2, c) for c in chunks]
+    c2 = O.fused_prefill(tiny2, kv2, ctx, start, q, crit=1, ratio_bp=2000, n_anchor=2, selector="all")
+    # every layer's softmax puts mass 1 per (query row, head) on the context keys
+    assert abs(c2["scores"].sum() - qd.TINY.n_layers * len(q) * qd.TINY.n_heads) < 1e-9 * c2["scores"].sum()
+
+
+def test_hkvd_full_ratio_is_full_recompute(tiny):
+    chunks, start, q = tiny_request()
+    kv = [O.chunk_precompute(tiny, c, store_bf16=False) for c in chunks]
+    ctx = np.concatenate(chunks)
+    out = O.hkvd_prefill(tiny, kv, ctx, start, q, [10000] * qd.TINY.n_layers)
+    full = O.full_prefill(tiny, np.concatenate([ctx, q]))
+    np.testing.assert_allclose(out["K"], full["K"], atol=5e-5)
+    np.testing.assert_allclose(out["V"], full["V"], atol=5e-5)
+    np.testing.assert_allclose(out["logits"], full["logits"], atol=1e-4)
+
+
+def test_hkvd_zero_ratio_is_full_kv_reuse(tiny):
+    chunks, start, q = tiny_request()
+    kv = [O.chunk_precompute(tiny, c) for c in chunks]
+    ctx = np.concatenate(chunks)
+    out = O.hkvd_prefill(tiny, kv, ctx, start, q, [0] * qd.TINY.n_layers)
+    reuse = O.fused_prefill(tiny, kv, ctx, start, q, crit=1, ratio_bp=0, n_anchor=2)
+    assert all(len(sl) == 0 for sl in out["layer_sel"])
+    np.testing.assert_array_equal(out["K"], reuse["K"])
+    np.testing.assert_allclose(out["logits"], reuse["logits"], atol=1e-9)
+
+
+def _dev_bruteforce(K_fresh, V_fresh, K_reused, V_reused, rows):
+    out = []
+    for j in rows:
+        acc = 0.0
+        for h in range(K_fresh.shape[1]):
+            for e in range(K_fresh.shape[2]):
+                dk = float(K_fresh[j, h, e]) - float(K_reused[j, h, e])
+                dv = float(V_fresh[j, h, e]) - float(V_reused[j, h, e])
+                acc += dk * dk + dv * dv
+        out.append(acc)
+    return np.array(out)
+
+
+def test_hkvd_deviation_bruteforce_from_full_prefill(tiny):
+    # At layer 0 the fresh K/V of every context token is full prefill's layer-0 K/V; with
+    # layer 0 keeping every token, layer 1's fresh K/V is full prefill's layer-1 K/V too.
+    chunks, start, q = tiny_request()
+    kv = [O.chunk_precompute(tiny, c) for c in chunks]
+    ctx = np.concatenate(chunks)
+    C = len(ctx)
+    full = O.full_prefill(tiny, np.concatenate([ctx, q]))
+    out = O.hkvd_prefill(tiny, kv, ctx, start, q, [10000, 3000])
+    row_delta = np.repeat(start[:-1], np.diff(start))
+    for l in (0, 1):
+        Kr = O.rope_reposition(np.concatenate([c["K"][l] for c in kv]), row_delta, qd.TINY.theta)
+        Vr = np.concatenate([c["V"][l] for c in kv])
+        want = _dev_bruteforce(full["K"][l], full["V"][l], Kr, Vr, range(C))
+        np.testing.assert_allclose(out["layer_dev"][l], want, rtol=1e-4, atol=1e-7)
+    order = sorted(range(C), key=lambda j: (-want[j], j))   # layer 1: top 30% by deviation, ties low index
+    assert list(out["layer_sel"][1]) == sorted(order[:O.num_selected(C, 3000)])
+
+
+def test_hkvd_gradual_filtering_nests(tiny):
+    chunks, start, q = tiny_request()
+    kv = [O.chunk_precompute(tiny, c) for c in chunks]
+    ctx = np.concatenate(chunks)
+    C = len(ctx)
+    out = O.hkvd_prefill(tiny, kv, ctx, start, q, [5000, 2000])
+    a, b = out["layer_sel"]
+    assert len(a) == O.num_selected(C, 5000) and len(b) == O.num_selected(C, 2000)
+    assert np.all(np.diff(a) > 0) and np.all(np.diff(b) > 0) and set(b) <= set(a)
+    assert len(out["layer_dev"][1]) == len(a)   # layer 1 measures only the rows kept after layer 0
