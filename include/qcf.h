@@ -175,6 +175,16 @@ qcf_status qcf_profile_scores_noalloc(const qcf_bf16* q, const qcf_bf16* K, int 
  * Exact on the fp32 bit patterns; -0.0 counts as +0.0; scores must not be NaN. */
 qcf_status qcf_topn_select(const float* scores, int C, int N, int32_t* sel, void* stream);
 
+/* KV deviation of recomputed rows ("KVCache reuse 01" 1.3.2, "KV Deviation"): for i < n,
+ * dev[i] = sum over the Hkv*D entries of (k_new[i] - K_cache[pos[i]])^2 + (v_new[i] - V_cache[pos[i]])^2,
+ * fp32 accumulation of bf16 inputs.
+ *   k_new, v_new  device [n][Hkv][D] bf16 (fresh rows); pos device [n] in [0, T)
+ *   K_cache, V_cache device [T][Hkv][D] bf16 (the reused rows); dev device [n] fp32.
+ * A position outside [0, T) gives dev 0 and sets QCF_DEV_BAD_INDEX in the device status word. */
+qcf_status qcf_kv_deviation(const qcf_bf16* k_new, const qcf_bf16* v_new, const int32_t* pos, int n,
+                            const qcf_bf16* K_cache, const qcf_bf16* V_cache, int T, int Hkv, int D, float* dev,
+                            void* stream);
+
 /* dst[i][:] = src[idx[i]][:] for i < n; rows of `width` bf16 (width % 8 == 0).
  * idx device [n], each in [0, src_rows). */
 qcf_status qcf_gather_rows(const qcf_bf16* src, int64_t src_rows, int width, const int32_t* idx, int n,
@@ -303,7 +313,31 @@ typedef struct qcf_request {
   int crit_layer;
   int ratio_bp;
   const int32_t* forced_sel;
+  /* Appended fields: a zero-initialised request keeps the critical-layer selector. */
+  int selector;                  /* QCF_SELECT_*; see below */
+  const int32_t* layer_ratio_bp; /* HOST [L], QCF_SELECT_HKVD only: share of C kept after layer l, basis points,
+                                    non-increasing, layer_ratio_bp[L-1] == ratio_bp */
 } qcf_request;
+
+/* Selectors (qcf_request.selector):
+ *   QCF_SELECT_CRITICAL    QCFuse: probe layers 0..crit-1 with the anchor prefix, profile at crit_layer
+ *                          (QCFuse 2.A); crit_layer = L-1 is the QCLast variant (QCFuse 4, "Results").
+ *   QCF_SELECT_ALL_LAYERS  QCAll (QCFuse 4): the probe runs layers 0..L-2 (anchor stores must hold those
+ *                          layers); the profile scores of every layer's query against that layer's
+ *                          re-rotated keys are summed, then one top-N selection.  Every layer's keys must
+ *                          land before the recompute starts: the cost the pages attribute to all-layer
+ *                          profiling.  crit_layer still names the anchors' layer (chosen offline).
+ *   QCF_SELECT_HKVD        CacheBlend's KV-deviation selection with gradual filtering ("KVCache reuse 01"
+ *                          1.3.2-1.3.4): layer 0 projects K/V for every context token, layer l for the
+ *                          tokens kept after layer l-1; a token's deviation is the squared L2 distance of
+ *                          its fresh K and V to the reused (re-rotated) cache rows; the top
+ *                          ceil(layer_ratio_bp[l] * C / 10000) by deviation (ties to the lower position)
+ *                          are kept and get fresh K/V, attention and MLP at layer l with the query rows.
+ *                          Anchors, crit_layer and forced_sel are ignored; out->scores gets layer 0's
+ *                          deviation of every context token, out->sel the rows kept after the last layer. */
+#define QCF_SELECT_CRITICAL 0
+#define QCF_SELECT_ALL_LAYERS 1
+#define QCF_SELECT_HKVD 2
 
 /* Outputs: the fused cache of every layer (HOST arrays of device pointers
  * [C + Q][Hkv][D]), sel [N], scores [C], q_crit [Q][Hq][D] (nullable), the last
@@ -319,6 +353,9 @@ typedef struct qcf_outputs {
   int32_t* first_token;
   int32_t* first_token_host;
   float* x_rows;  /* device fp32 [N + Q][d] final hidden states of the recomputed rows, or NULL */
+  /* Appended: QCF_SELECT_HKVD only, or NULL.  device [L][N_0]: row l holds the N_l context rows kept
+   * after layer l (ascending), N_l = ceil(layer_ratio_bp[l] * C / 10000). */
+  int32_t* layer_sel;
 } qcf_outputs;
 
 /* The per-request fused prefill with the per-layer pipeline (QCFuse 2.A
@@ -327,6 +364,9 @@ typedef struct qcf_outputs {
  * probe, profiling and top-N run, then layer l is recomputed on compute_stream
  * while later layers' chunk K/V are copied on copy_stream.  Enqueues only. */
 size_t qcf_request_workspace_size(const qcf_dims* dims, int C, int Q, int n_anchor_total, int N);
+/* Workspace for this particular request, any selector (QCF_SELECT_HKVD needs full-row buffers for
+ * layer 0, which the size above does not cover).  0 when the request is malformed. */
+size_t qcf_request_workspace_size_for(const qcf_dims* dims, const qcf_request* r);
 qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, void* ws,
                                size_t ws_bytes, void* compute_stream, void* copy_stream);
 

@@ -53,13 +53,14 @@ class Request(C.Structure):
                 ("n_anchor", C.c_int), ("anchor_idx", C.POINTER(C.c_int32)),
                 ("anchor_K_host", C.POINTER(C.c_void_p)), ("anchor_V_host", C.POINTER(C.c_void_p)),
                 ("ids", C.c_void_p), ("query_len", C.c_int), ("crit_layer", C.c_int), ("ratio_bp", C.c_int),
-                ("forced_sel", C.c_void_p)]
+                ("forced_sel", C.c_void_p), ("selector", C.c_int), ("layer_ratio_bp", C.POINTER(C.c_int32))]
 
 
 class Outputs(C.Structure):
     _fields_ = [("K_layers", C.POINTER(C.c_void_p)), ("V_layers", C.POINTER(C.c_void_p)), ("sel", C.c_void_p),
                 ("scores", C.c_void_p), ("q_crit", C.c_void_p), ("last_logits", C.c_void_p),
-                ("first_token", C.c_void_p), ("first_token_host", C.c_void_p), ("x_rows", C.c_void_p)]
+                ("first_token", C.c_void_p), ("first_token_host", C.c_void_p), ("x_rows", C.c_void_p),
+                ("layer_sel", C.c_void_p)]
 
 
 P, I, I64, F, D64, SZ = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_double, C.c_size_t
@@ -95,6 +96,8 @@ PROTOTYPES = {
     "qcf_full_prefill_workspace_size": (SZ, [C.POINTER(Dims), I]),
     "qcf_full_prefill": (I, [C.POINTER(Model), P, I, C.POINTER(P), C.POINTER(P), P, P, P, SZ, P]),
     "qcf_request_workspace_size": (SZ, [C.POINTER(Dims), I, I, I, I]),
+    "qcf_request_workspace_size_for": (SZ, [C.POINTER(Dims), C.POINTER(Request)]),
+    "qcf_kv_deviation": (I, [P, P, P, I, P, P, I, I, I, P, P]),
     "qcf_request_prefill": (I, [C.POINTER(Model), C.POINTER(Request), C.POINTER(Outputs), P, SZ, P, P]),
     "qcf_embed_rows": (I, [C.POINTER(Model), P, P, I, P, P]),
     "qcf_lm_head_workspace_size": (SZ, [C.POINTER(Dims)]),

@@ -169,6 +169,25 @@ __global__ void make_rows_kernel(const int32_t* __restrict__ sel, int N, int C, 
   if (i < n) rows[i] = i < N ? sel[i] : C + (i - N);
 }
 
+// HKVD compaction: keep_idx[i] = sel_idx[i] for i < N (context rows kept, indices into
+// the previous row list), then the query rows, which follow the n_ctx context rows
+// there; rows_new[i] = rows_prev[keep_idx[i]].
+__global__ void keep_rows_kernel(const int32_t* __restrict__ sel_idx, int N, int n_ctx, int n,
+                                 const int32_t* __restrict__ rows_prev, int32_t* __restrict__ keep_idx,
+                                 int32_t* __restrict__ rows_new) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int k = i < N ? sel_idx[i] : n_ctx + (i - N);
+  keep_idx[i] = k;
+  rows_new[i] = rows_prev[k];
+}
+
+// dst[i] += src[i]
+__global__ void add_f32_kernel(float* __restrict__ dst, const float* __restrict__ src, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] += src[i];
+}
+
 constexpr int kMaxReqChunks = 512;
 struct ChunkOffsets {
   int n_chunks;
@@ -229,6 +248,8 @@ struct RequestLayout {
   __nv_bfloat16* pV;
   __nv_bfloat16* q_crit; // [Q][Hq*D]
   float* scores;         // [C]
+  float* scores_acc;     // [C] QCAll: the probe layers' scores
+  float* scores_tmp;     // [C] QCAll: one layer's scores
   int32_t* sel;          // [N]
   void* prof_ws;
   size_t prof_ws_bytes;
@@ -261,11 +282,169 @@ static bool carve_request(Carve& c, const qcf_dims& d, int C, int Q, int nA, int
   r->pV = c.take<__nv_bfloat16>(static_cast<size_t>(nA + Q) * HD);
   r->q_crit = c.take<__nv_bfloat16>(static_cast<size_t>(Q) * d.n_heads * d.head_dim);
   r->scores = c.take<float>(C);
+  r->scores_acc = c.take<float>(C);
+  r->scores_tmp = c.take<float>(C);
   r->sel = c.take<int32_t>(N > 0 ? N : 1);
   r->prof_ws_bytes = qcf_profile_scores_workspace_size(Q, C, d.n_heads, d.n_kv_heads, d.head_dim);
   r->prof_ws = c.take<uint8_t>(r->prof_ws_bytes);
   r->lm_ws = c.take<uint8_t>(256);
   return c.ok;
+}
+
+// ------------------------------------------------------------------ HKVD (CacheBlend) selection
+
+// Buffers of the KV-deviation path.  Layer 0 projects K/V for all T rows, so the
+// projection buffers hold T rows; the kept rows (at most N_0 + Q) get the rest.
+struct HkvdLayout {
+  int C, Q, T, N0, nk;    // nk = N_0 + Q
+  float* x_a;             // [T][d]   rows of the previous layer / kept rows, alternating
+  float* x_b;             // [T][d]
+  int32_t* rows_a;        // [T] positions
+  int32_t* rows_b;        // [T]
+  int32_t* iota;          // [T] 0..T-1: temporary K/V rows of the projection
+  __nv_bfloat16* h;       // [T][d]
+  __nv_bfloat16* q;       // [T][Hq*D]
+  __nv_bfloat16* k_tmp;   // [T][HD]
+  __nv_bfloat16* v_tmp;   // [T][HD]
+  __nv_bfloat16* q_keep;  // [nk][Hq*D]
+  __nv_bfloat16* k_keep;  // [nk][HD]
+  __nv_bfloat16* v_keep;  // [nk][HD]
+  float* dev;             // [C]
+  int32_t* sel_idx;       // [max(N_0, 1)]
+  int32_t* keep_idx;      // [nk]
+  LayerBufs lb;           // o, act and the GEMM / attention workspaces for nk rows (h, q unused)
+  void* lm_ws;
+};
+
+static bool hkvd_counts(const int32_t* sched, int L, int C, int ratio_bp, std::vector<int>* Nl) {
+  if (!sched) return false;
+  Nl->assign(L, 0);
+  for (int l = 0; l < L; ++l) {
+    if (sched[l] < 0 || sched[l] > 10000 || (l > 0 && sched[l] > sched[l - 1])) return false;
+    qcf_num_selected(C, sched[l], &(*Nl)[l]);
+  }
+  return sched[L - 1] == ratio_bp;
+}
+
+static bool carve_hkvd(Carve& c, const qcf_dims& d, int C, int Q, const std::vector<int>& Nl, HkvdLayout* H) {
+  const int T = C + Q, N0 = Nl.empty() ? 0 : Nl[0], nk = N0 + Q;
+  const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim, QD = static_cast<size_t>(d.n_heads) * d.head_dim;
+  H->C = C; H->Q = Q; H->T = T; H->N0 = N0; H->nk = nk;
+  H->x_a = c.take<float>(static_cast<size_t>(T) * d.d_model);
+  H->x_b = c.take<float>(static_cast<size_t>(T) * d.d_model);
+  H->rows_a = c.take<int32_t>(T);
+  H->rows_b = c.take<int32_t>(T);
+  H->iota = c.take<int32_t>(T);
+  H->h = c.take<__nv_bfloat16>(static_cast<size_t>(T) * d.d_model);
+  H->q = c.take<__nv_bfloat16>(static_cast<size_t>(T) * QD);
+  H->k_tmp = c.take<__nv_bfloat16>(static_cast<size_t>(T) * HD);
+  H->v_tmp = c.take<__nv_bfloat16>(static_cast<size_t>(T) * HD);
+  H->q_keep = c.take<__nv_bfloat16>(static_cast<size_t>(nk) * QD);
+  H->k_keep = c.take<__nv_bfloat16>(static_cast<size_t>(nk) * HD);
+  H->v_keep = c.take<__nv_bfloat16>(static_cast<size_t>(nk) * HD);
+  H->dev = c.take<float>(C > 0 ? C : 1);
+  H->sel_idx = c.take<int32_t>(N0 > 0 ? N0 : 1);
+  H->keep_idx = c.take<int32_t>(nk);
+  H->lb.h = H->h;
+  H->lb.q = H->q_keep;
+  H->lb.o = c.take<__nv_bfloat16>(static_cast<size_t>(nk) * QD);
+  H->lb.act = c.take<__nv_bfloat16>(static_cast<size_t>(nk) * d.ffn_padded);
+  size_t gws = std::max(gemm_ws_layer(d, T), gemm_ws_layer(d, nk));
+  size_t aws = 0;
+  for (int l = 0; l < static_cast<int>(Nl.size()); ++l) {
+    gws = std::max(gws, gemm_ws_layer(d, Nl[l] + Q));
+    aws = std::max(aws, attn_workspace_size(Nl[l] + Q, T, d.n_heads, d.n_kv_heads, d.head_dim));
+  }
+  H->lb.gemm_ws_bytes = gws;
+  H->lb.gemm_ws = c.take<uint8_t>(gws);
+  H->lb.attn_ws_bytes = aws;
+  H->lb.attn_ws = c.take<uint8_t>(aws > 0 ? aws : 1);
+  H->lm_ws = c.take<uint8_t>(256);
+  return c.ok;
+}
+
+// One layer of the KV-deviation path.  In: x_prev [n_prev][d] at positions rows_prev
+// (the n_ctx context rows kept so far, then the Q query rows).  Projects K/V for all
+// of them, measures the context rows' deviation against the layer's reused cache,
+// keeps the top N of those, compacts the kept rows plus the query into x_new /
+// rows_new, writes their fresh K/V into the cache and runs attention, O and the MLP
+// for them.  dev0 (layer 0 only, nullable) receives the deviations.
+static qcf_status hkvd_layer(const qcf_model* m, int l, HkvdLayout& H, const float* x_prev, const int32_t* rows_prev,
+                             int n_ctx, int N, float* x_new, int32_t* rows_new, __nv_bfloat16* Kl, __nv_bfloat16* Vl,
+                             float* dev_out, int32_t* sel_out, cudaStream_t st) {
+  const qcf_dims& d = m->dims;
+  const qcf_layer_weights& w = m->layers[l];
+  const int D = d.head_dim, Hq = d.n_heads, Hkv = d.n_kv_heads, Q = H.Q, T = H.T;
+  const int n_prev = n_ctx + Q, nk = N + Q;
+  const int HD = Hkv * D, QD = Hq * D;
+  cudaError_t e = launch_rmsnorm(x_prev, n_prev, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, H.h, st);
+  if (e != cudaSuccess) return cuda_error(e, "hkvd: rmsnorm");
+  EpiParams ep{};
+  ep.q_out = H.q;
+  ep.k_cache = H.k_tmp;
+  ep.v_cache = H.v_tmp;
+  ep.rope_pos = rows_prev;
+  ep.cache_row = H.iota;
+  ep.cos_t = m->rope.cos;
+  ep.sin_t = m->rope.sin;
+  ep.Hq = Hq;
+  ep.Hkv = Hkv;
+  ep.D = D;
+  ep.T = n_prev;
+  ep.max_pos = m->rope.max_pos;
+  ep.status = device_status_ptr();
+  qcf_status s = gemm_launch(EPI_QKV_ROPE, H.h, n_prev, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
+                             (Hq + 2 * Hkv) * D, ep, H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_QKV);
+  if (s != QCF_OK) return s;
+  float* dev = dev_out ? dev_out : H.dev;
+  if ((e = launch_kv_deviation(H.k_tmp, H.v_tmp, rows_prev, n_ctx, Kl, Vl, T, HD, dev, st)) != cudaSuccess)
+    return cuda_error(e, "hkvd: deviation");
+  if (N > 0 && (s = qcf_topn_select(dev, n_ctx, N, H.sel_idx, st)) != QCF_OK) return s;
+  {
+    LaunchScope ls(KC_MISC, st);
+    keep_rows_kernel<<<(nk + 255) / 256, 256, 0, st>>>(H.sel_idx, N, n_ctx, nk, rows_prev, H.keep_idx, rows_new);
+  }
+  // compact: hidden rows (fp32, moved as 2d bf16-sized words), q and the fresh K/V
+  if ((s = qcf_gather_rows(reinterpret_cast<const qcf_bf16*>(x_prev), n_prev, 2 * d.d_model, H.keep_idx, nk,
+                           reinterpret_cast<qcf_bf16*>(x_new), st)) != QCF_OK ||
+      (s = qcf_gather_rows(reinterpret_cast<const qcf_bf16*>(H.q), n_prev, QD, H.keep_idx, nk,
+                           reinterpret_cast<qcf_bf16*>(H.q_keep), st)) != QCF_OK ||
+      (s = qcf_gather_rows(reinterpret_cast<const qcf_bf16*>(H.k_tmp), n_prev, HD, H.keep_idx, nk,
+                           reinterpret_cast<qcf_bf16*>(H.k_keep), st)) != QCF_OK ||
+      (s = qcf_gather_rows(reinterpret_cast<const qcf_bf16*>(H.v_tmp), n_prev, HD, H.keep_idx, nk,
+                           reinterpret_cast<qcf_bf16*>(H.v_keep), st)) != QCF_OK)
+    return s;
+  if ((s = qcf_scatter_kv(reinterpret_cast<const qcf_bf16*>(H.k_keep), reinterpret_cast<const qcf_bf16*>(H.v_keep),
+                          rows_new, nk, Hkv, D, reinterpret_cast<qcf_bf16*>(Kl), reinterpret_cast<qcf_bf16*>(Vl), T,
+                          st)) != QCF_OK)
+    return s;
+  if (sel_out && N > 0 &&
+      (e = cudaMemcpyAsync(sel_out, rows_new, N * sizeof(int32_t), cudaMemcpyDeviceToDevice, st)) != cudaSuccess)
+    return cuda_error(e, "hkvd: selection copy");
+  // attention, O projection and the MLP for the kept rows
+  s = attn_launch(H.q_keep, rows_new, nk, Kl, Vl, T, Hq, Hkv, D, 1.0f / sqrtf(static_cast<float>(D)), H.lb.o, nullptr,
+                  H.lb.attn_ws, H.lb.attn_ws_bytes, st, KC_ATTN);
+  if (s != QCF_OK) return s;
+  EpiParams eo{};
+  eo.out = x_new;
+  eo.ldo = d.d_model;
+  s = gemm_launch(EPI_ADD_F32, H.lb.o, nk, QD, reinterpret_cast<const __nv_bfloat16*>(w.w_o), d.d_model, eo,
+                  H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_O);
+  if (s != QCF_OK) return s;
+  if ((e = launch_rmsnorm(x_new, nk, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_mlp), d.eps, H.h, st)) !=
+      cudaSuccess)
+    return cuda_error(e, "hkvd: rmsnorm");
+  EpiParams eg{};
+  eg.out = H.lb.act;
+  eg.ldo = d.ffn_padded;
+  s = gemm_launch(EPI_SWIGLU, H.h, nk, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_gu), 2 * d.ffn_padded, eg,
+                  H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_GU);
+  if (s != QCF_OK) return s;
+  EpiParams edn{};
+  edn.out = x_new;
+  edn.ldo = d.d_model;
+  return gemm_launch(EPI_ADD_F32, H.lb.act, nk, d.ffn_padded, reinterpret_cast<const __nv_bfloat16*>(w.w_down),
+                     d.d_model, edn, H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_DOWN);
 }
 
 struct EventPool {
@@ -376,6 +555,35 @@ size_t qcf_request_workspace_size(const qcf_dims* dims, int C, int Q, int n_anch
   return c.used;
 }
 
+size_t qcf_request_workspace_size_for(const qcf_dims* dims, const qcf_request* r) {
+  if (!dims || !r || !r->chunk_len || r->n_chunks <= 0 || r->n_chunks > kMaxReqChunks || r->query_len <= 0 ||
+      r->ratio_bp < 0 || r->ratio_bp > 10000 || r->n_anchor < 0)
+    return 0;
+  long long Cl = 0;
+  for (int c = 0; c < r->n_chunks; ++c) {
+    if (r->chunk_len[c] <= 0) return 0;
+    Cl += r->chunk_len[c];
+  }
+  if (Cl > (1 << 30)) return 0;
+  const int C = static_cast<int>(Cl), Q = r->query_len, L = dims->n_layers;
+  int N = 0;
+  qcf_num_selected(C, r->ratio_bp, &N);
+  Carve c{nullptr, 0};
+  if (r->selector == QCF_SELECT_HKVD) {
+    std::vector<int> Nl;
+    if (!hkvd_counts(r->layer_ratio_bp, L, C, r->ratio_bp, &Nl)) return 0;
+    HkvdLayout H;
+    carve_hkvd(c, *dims, C, Q, Nl, &H);
+    return c.used;
+  }
+  const int crit = r->selector == QCF_SELECT_ALL_LAYERS ? L - 1 : r->crit_layer;
+  if (crit < 0 || crit >= L) return 0;
+  const int nA = crit > 0 ? r->n_anchor * r->n_chunks : 0;
+  RequestLayout rl;
+  carve_request(c, *dims, C, Q, nA, N, r->n_chunks, crit, r->n_anchor, &rl);
+  return c.used;
+}
+
 qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, void* ws,
                                size_t ws_bytes, void* compute_stream, void* copy_stream) {
   qcf_status s = check_model(m, "qcf_request_prefill");
@@ -390,6 +598,10 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
       r->crit_layer >= L || r->ratio_bp < 0 || r->ratio_bp > 10000 || r->n_anchor < 0)
     return set_error(QCF_ERR_SHAPE, "qcf_request_prefill: n_chunks=%d query_len=%d crit=%d ratio_bp=%d n_anchor=%d",
                      r->n_chunks, r->query_len, r->crit_layer, r->ratio_bp, r->n_anchor);
+  if (r->selector < QCF_SELECT_CRITICAL || r->selector > QCF_SELECT_HKVD)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill: unknown selector %d", r->selector);
+  const bool all_layers = r->selector == QCF_SELECT_ALL_LAYERS;
+  const bool hkvd = r->selector == QCF_SELECT_HKVD;
   std::vector<int32_t> seg_start(r->n_chunks + 1, 0), seg_delta(r->n_chunks, 0);
   ChunkOffsets co;
   co.n_chunks = r->n_chunks;
@@ -404,9 +616,15 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
   const int C = seg_start[r->n_chunks], Q = r->query_len, T = C + Q;
   int N = 0;
   qcf_num_selected(C, r->ratio_bp, &N);
-  const int crit = r->crit_layer;
+  // probe depth: the critical layer (QCLast: L-1); QCAll probes L-1 layers and profiles all L;
+  // HKVD has no probe (layer 0's keys are then simply copied first)
+  const int crit = hkvd ? 0 : (all_layers ? L - 1 : r->crit_layer);
   const int A = r->n_anchor;
-  const int nA = (crit > 0) ? A * r->n_chunks : 0;
+  const int nA = (!hkvd && crit > 0) ? A * r->n_chunks : 0;
+  std::vector<int> Nl;
+  if (hkvd && !hkvd_counts(r->layer_ratio_bp, L, C, r->ratio_bp, &Nl))
+    return set_error(QCF_ERR_INVALID_ARG,
+                     "qcf_request_prefill: HKVD needs layer_ratio_bp[L] in [0,10000], non-increasing, last == ratio_bp");
   if (nA > 0 && (!r->anchor_K_host || !r->anchor_V_host))
     return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill: anchor stores are NULL");
   if (m->rope.max_pos < T) return set_error(QCF_ERR_SHAPE, "qcf_request_prefill: RoPE table %d shorter than T=%d", m->rope.max_pos, T);
@@ -416,10 +634,12 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
   if (take_fault(4) || !aligned16(ws)) return set_error(QCF_ERR_ALIGN, "qcf_request_prefill: workspace misaligned");
   if (take_fault(1)) return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill: injected invalid index table");
   Carve cv{static_cast<uint8_t*>(ws), ws_bytes};
-  RequestLayout rl;
-  if (take_fault(2) || !carve_request(cv, d, C, Q, nA, N, r->n_chunks, crit, A, &rl))
+  RequestLayout rl{};
+  HkvdLayout H{};
+  const bool carved = hkvd ? carve_hkvd(cv, d, C, Q, Nl, &H) : carve_request(cv, d, C, Q, nA, N, r->n_chunks, crit, A, &rl);
+  if (take_fault(2) || !carved)
     return set_error(QCF_ERR_WORKSPACE, "qcf_request_prefill: workspace %zu too small (need %zu)", ws_bytes, cv.used);
-  float* scores = out->scores ? out->scores : rl.scores;
+  float* scores = out->scores ? out->scores : (hkvd ? H.dev : rl.scores);
   int32_t* sel = out->sel ? out->sel : rl.sel;
   __nv_bfloat16* q_crit = out->q_crit ? reinterpret_cast<__nv_bfloat16*>(out->q_crit) : rl.q_crit;
 
@@ -482,89 +702,140 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
 
   // ---- compute stream
   const __nv_bfloat16* embed = reinterpret_cast<const __nv_bfloat16*>(m->embed);
-  // probe: query rows at positions C..T-1 with the anchors as KV prefix (probe cache rows 0..nA-1)
-  if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, nullptr, C, Q, rl.x, cs)) != cudaSuccess)
-    return cuda_error(e, "qcf_request_prefill: embed");
-  {
-    LaunchScope ls(KC_MISC, cs);
-    iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_pos, Q, C);
-  }
-  {
-    LaunchScope ls(KC_MISC, cs);
-    iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_row, Q, nA);
-  }
-  if (crit > 0) {
-    if ((e = cudaStreamWaitEvent(cs, ev_anchor, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
-    for (int l = 0; l < crit; ++l) {
-      if (nA > 0) {
-        const int threads = nA * d.n_kv_heads * (d.head_dim / 16);
-        LaunchScope ls(KC_ROPE, cs);
-        anchor_assemble_kernel<<<(threads + 255) / 256, 256, 0, cs>>>(rl.stK, rl.stV, l, crit, A, d.n_kv_heads,
-                                                                      d.head_dim, m->rope.cos, m->rope.sin, co, rl.pK,
-                                                                      rl.pV);
+  const float* x_final = nullptr;  // final hidden states of the recomputed rows [ns][d]
+  int ns = 0;
+  if (hkvd) {
+    // every context row and the query enter layer 0; the kept set shrinks layer by layer
+    {
+      LaunchScope ls(KC_MISC, cs);
+      iota_kernel<<<(T + 255) / 256, 256, 0, cs>>>(H.rows_a, T, 0);
+      iota_kernel<<<(T + 255) / 256, 256, 0, cs>>>(H.iota, T, 0);
+    }
+    if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, nullptr, 0, T, H.x_a, cs)) != cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: embed");
+    float* xp = H.x_a;
+    float* xn = H.x_b;
+    int32_t* rp = H.rows_a;
+    int32_t* rn = H.rows_b;
+    int n_ctx = C;
+    for (int l = 0; l < L; ++l) {
+      if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+      s = hkvd_layer(m, l, H, xp, rp, n_ctx, Nl[l], xn, rn, reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]),
+                     reinterpret_cast<__nv_bfloat16*>(out->V_layers[l]), l == 0 ? scores : nullptr,
+                     out->layer_sel ? out->layer_sel + static_cast<size_t>(l) * (H.N0 > 0 ? H.N0 : 1) : nullptr, cs);
+      if (s != QCF_OK) return s;
+      std::swap(xp, xn);
+      std::swap(rp, rn);
+      n_ctx = Nl[l];
+    }
+    if (N > 0 && out->sel &&
+        (e = cudaMemcpyAsync(out->sel, rp, N * sizeof(int32_t), cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: selection copy");
+    ns = N + Q;
+    x_final = xp;
+    if ((e = launch_lm_head(m, xp + static_cast<size_t>(ns - 1) * d.d_model, out->last_logits, out->first_token,
+                            H.lm_ws, cs)) != cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: lm head");
+  } else {
+    // probe: query rows at positions C..T-1 with the anchors as KV prefix (probe cache rows 0..nA-1)
+    if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, nullptr, C, Q, rl.x, cs)) != cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: embed");
+    {
+      LaunchScope ls(KC_MISC, cs);
+      iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_pos, Q, C);
+    }
+    {
+      LaunchScope ls(KC_MISC, cs);
+      iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_row, Q, nA);
+    }
+    const float scale = 1.0f / sqrtf(static_cast<float>(d.head_dim));
+    if (all_layers && (e = cudaMemsetAsync(rl.scores_acc, 0, static_cast<size_t>(C) * sizeof(float), cs)) != cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: clear scores");
+    if (crit > 0) {
+      if ((e = cudaStreamWaitEvent(cs, ev_anchor, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+      for (int l = 0; l < crit; ++l) {
+        if (nA > 0) {
+          const int threads = nA * d.n_kv_heads * (d.head_dim / 16);
+          LaunchScope ls(KC_ROPE, cs);
+          anchor_assemble_kernel<<<(threads + 255) / 256, 256, 0, cs>>>(rl.stK, rl.stV, l, crit, A, d.n_kv_heads,
+                                                                        d.head_dim, m->rope.cos, m->rope.sin, co, rl.pK,
+                                                                        rl.pV);
+        }
+        s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK, rl.pV, nA + Q, rl.lb, cs, true);
+        if (s != QCF_OK) return s;
+        if (all_layers) {   // QCAll: this probe layer's q against this layer's re-rotated keys
+          if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+          s = qcf_profile_scores(reinterpret_cast<const qcf_bf16*>(rl.lb.q), out->K_layers[l], Q, C, d.n_heads,
+                                 d.n_kv_heads, d.head_dim, scale, rl.scores_tmp, rl.prof_ws, rl.prof_ws_bytes, cs);
+          if (s != QCF_OK) return s;
+          LaunchScope ls(KC_MISC, cs);
+          add_f32_kernel<<<(C + 255) / 256, 256, 0, cs>>>(rl.scores_acc, rl.scores_tmp, C);
+        }
       }
-      s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK, rl.pV, nA + Q, rl.lb, cs, true);
+    }
+    // critical layer: q = RoPE(RMSNorm(x) W_q) only
+    {
+      const qcf_layer_weights& w = m->layers[crit];
+      if ((e = launch_rmsnorm(rl.x, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, rl.lb.h, cs)) !=
+          cudaSuccess)
+        return cuda_error(e, "qcf_request_prefill: rmsnorm");
+      EpiParams ep{};
+      ep.q_out = q_crit;
+      ep.rope_pos = rl.probe_pos;
+      ep.cache_row = nullptr;
+      ep.cos_t = m->rope.cos;
+      ep.sin_t = m->rope.sin;
+      ep.Hq = d.n_heads;
+      ep.Hkv = d.n_kv_heads;
+      ep.D = d.head_dim;
+      ep.T = 1;
+      ep.max_pos = m->rope.max_pos;
+      ep.status = device_status_ptr();
+      s = gemm_launch(EPI_QKV_ROPE, rl.lb.h, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
+                      d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_PROBE, false, Q <= kPdlMaxRows);
       if (s != QCF_OK) return s;
     }
-  }
-  // critical layer: q = RoPE(RMSNorm(x) W_q) only
-  {
-    const qcf_layer_weights& w = m->layers[crit];
-    if ((e = launch_rmsnorm(rl.x, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, rl.lb.h, cs)) !=
-        cudaSuccess)
-      return cuda_error(e, "qcf_request_prefill: rmsnorm");
-    EpiParams ep{};
-    ep.q_out = q_crit;
-    ep.rope_pos = rl.probe_pos;
-    ep.cache_row = nullptr;
-    ep.cos_t = m->rope.cos;
-    ep.sin_t = m->rope.sin;
-    ep.Hq = d.n_heads;
-    ep.Hkv = d.n_kv_heads;
-    ep.D = d.head_dim;
-    ep.T = 1;
-    ep.max_pos = m->rope.max_pos;
-    ep.status = device_status_ptr();
-    s = gemm_launch(EPI_QKV_ROPE, rl.lb.h, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
-                    d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_PROBE, false, Q <= kPdlMaxRows);
+    // profile the re-rotated critical-layer keys and select
+    if ((e = cudaStreamWaitEvent(cs, ev_crit, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+    __nv_bfloat16* Kcrit = reinterpret_cast<__nv_bfloat16*>(out->K_layers[crit]);
+    s = qcf_profile_scores(reinterpret_cast<const qcf_bf16*>(q_crit), reinterpret_cast<const qcf_bf16*>(Kcrit), Q, C,
+                           d.n_heads, d.n_kv_heads, d.head_dim, scale, scores, rl.prof_ws, rl.prof_ws_bytes, cs);
     if (s != QCF_OK) return s;
-  }
-  // profile the re-rotated critical-layer keys and select
-  if ((e = cudaStreamWaitEvent(cs, ev_crit, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
-  __nv_bfloat16* Kcrit = reinterpret_cast<__nv_bfloat16*>(out->K_layers[crit]);
-  s = qcf_profile_scores(reinterpret_cast<const qcf_bf16*>(q_crit), reinterpret_cast<const qcf_bf16*>(Kcrit), Q, C,
-                         d.n_heads, d.n_kv_heads, d.head_dim, 1.0f / sqrtf(static_cast<float>(d.head_dim)), scores,
-                         rl.prof_ws, rl.prof_ws_bytes, cs);
-  if (s != QCF_OK) return s;
-  if (N > 0) {
-    if (r->forced_sel) {
-      if ((e = cudaMemcpyAsync(sel, r->forced_sel, N * sizeof(int32_t), cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
-        return cuda_error(e, "qcf_request_prefill: forced selection");
-    } else {
-      s = qcf_topn_select(scores, C, N, sel, cs);
+    if (all_layers) {
+      LaunchScope ls(KC_MISC, cs);
+      add_f32_kernel<<<(C + 255) / 256, 256, 0, cs>>>(scores, rl.scores_acc, C);
+    }
+    if (N > 0) {
+      if (r->forced_sel) {
+        if ((e = cudaMemcpyAsync(sel, r->forced_sel, N * sizeof(int32_t), cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
+          return cuda_error(e, "qcf_request_prefill: forced selection");
+      } else {
+        s = qcf_topn_select(scores, C, N, sel, cs);
+        if (s != QCF_OK) return s;
+      }
+    }
+    ns = N + Q;
+    {
+      LaunchScope ls(KC_MISC, cs);
+      make_rows_kernel<<<(ns + 255) / 256, 256, 0, cs>>>(sel, N, C, ns, rl.rows);
+    }
+    // pipelined per-layer recompute of the selected rows and the query
+    if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, rl.rows, 0, ns, rl.x, cs)) != cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: embed");
+    for (int l = 0; l < L; ++l) {
+      if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+      __nv_bfloat16* Kl = reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]);
+      __nv_bfloat16* Vl = reinterpret_cast<__nv_bfloat16*>(out->V_layers[l]);
+      s = layer_forward_impl(m, l, rl.x, rl.rows, rl.rows, ns, Kl, Vl, T, rl.lb, cs);
       if (s != QCF_OK) return s;
     }
+    if ((e = launch_lm_head(m, rl.x + static_cast<size_t>(ns - 1) * d.d_model, out->last_logits, out->first_token,
+                            rl.lm_ws, cs)) != cudaSuccess)
+      return cuda_error(e, "qcf_request_prefill: lm head");
+    x_final = rl.x;
   }
-  const int ns = N + Q;
-  {
-    LaunchScope ls(KC_MISC, cs);
-    make_rows_kernel<<<(ns + 255) / 256, 256, 0, cs>>>(sel, N, C, ns, rl.rows);
-  }
-  // pipelined per-layer recompute of the selected rows and the query
-  if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, rl.rows, 0, ns, rl.x, cs)) != cudaSuccess)
-    return cuda_error(e, "qcf_request_prefill: embed");
-  for (int l = 0; l < L; ++l) {
-    if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
-    __nv_bfloat16* Kl = reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]);
-    __nv_bfloat16* Vl = reinterpret_cast<__nv_bfloat16*>(out->V_layers[l]);
-    s = layer_forward_impl(m, l, rl.x, rl.rows, rl.rows, ns, Kl, Vl, T, rl.lb, cs);
-    if (s != QCF_OK) return s;
-  }
-  if ((e = launch_lm_head(m, rl.x + static_cast<size_t>(ns - 1) * d.d_model, out->last_logits, out->first_token,
-                          rl.lm_ws, cs)) != cudaSuccess)
-    return cuda_error(e, "qcf_request_prefill: lm head");
   if (out->x_rows &&
-      (e = cudaMemcpyAsync(out->x_rows, rl.x, static_cast<size_t>(ns) * d.d_model * sizeof(float),
+      (e = cudaMemcpyAsync(out->x_rows, x_final, static_cast<size_t>(ns) * d.d_model * sizeof(float),
                            cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
     return cuda_error(e, "qcf_request_prefill: copy rows");
   if (out->first_token_host &&

@@ -107,6 +107,11 @@ cudaError_t launch_reposition(const __nv_bfloat16* src, __nv_bfloat16* dst, int6
                               const int32_t* seg_start, const int32_t* seg_delta, int n_seg, const qcf_rope_table* t,
                               cudaStream_t st);
 
+// KV deviation of fresh rows against the cache (select.cu).
+cudaError_t launch_kv_deviation(const __nv_bfloat16* k_new, const __nv_bfloat16* v_new, const int32_t* pos, int n,
+                                const __nv_bfloat16* K, const __nv_bfloat16* V, int T, int width, float* dev,
+                                cudaStream_t st);
+
 // Attention internals (attention.cu).
 size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D);
 qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,

@@ -204,6 +204,58 @@ __global__ void __launch_bounds__(kTopnThreads) topn_kernel(const float* __restr
   }
 }
 
+// ------------------------------------------------------------------ KV deviation (CacheBlend HKVD)
+
+__device__ __forceinline__ float sqdiff8(const uint4 a, const uint4 b) {
+  const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 u = __bfloat1622float2(x[i]), v = __bfloat1622float2(y[i]);
+    const float d0 = u.x - v.x, d1 = u.y - v.y;
+    acc = fmaf(d0, d0, fmaf(d1, d1, acc));
+  }
+  return acc;
+}
+
+// dev[i] = |k_new[i] - K[pos[i]]|^2 + |v_new[i] - V[pos[i]]|^2 over the row's width
+// entries; one warp per row, 16-byte loads.
+__global__ void kv_deviation_kernel(const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
+                                    const int32_t* __restrict__ pos, int n, const __nv_bfloat16* __restrict__ K,
+                                    const __nv_bfloat16* __restrict__ V, int T, int width, float* __restrict__ dev,
+                                    unsigned int* status) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= n) return;
+  const int p = pos[warp];
+  if (p < 0 || p >= T) {
+    if (lane == 0) {
+      flag_status(status, QCF_DEV_BAD_INDEX);
+      dev[warp] = 0.f;
+    }
+    return;
+  }
+  const uint4* a = reinterpret_cast<const uint4*>(k_new + static_cast<int64_t>(warp) * width);
+  const uint4* b = reinterpret_cast<const uint4*>(K + static_cast<int64_t>(p) * width);
+  const uint4* c = reinterpret_cast<const uint4*>(v_new + static_cast<int64_t>(warp) * width);
+  const uint4* d = reinterpret_cast<const uint4*>(V + static_cast<int64_t>(p) * width);
+  float acc = 0.f;
+  for (int i = lane; i < width / 8; i += 32) acc += sqdiff8(a[i], b[i]) + sqdiff8(c[i], d[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) dev[warp] = acc;
+}
+
+cudaError_t launch_kv_deviation(const __nv_bfloat16* k_new, const __nv_bfloat16* v_new, const int32_t* pos, int n,
+                                const __nv_bfloat16* K, const __nv_bfloat16* V, int T, int width, float* dev,
+                                cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  LaunchScope ls(KC_MISC, st);
+  kv_deviation_kernel<<<(n + 7) / 8, 256, 0, st>>>(k_new, v_new, pos, n, K, V, T, width, dev, device_status_ptr());
+  return cudaGetLastError();
+}
+
 }  // namespace qcf
 
 using namespace qcf;
@@ -245,6 +297,23 @@ qcf_status qcf_anchor_keynorm_topk(const qcf_bf16* K, const int32_t* chunk_start
                                                      anchor_idx, norms);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_anchor_keynorm_topk: launch");
+}
+
+qcf_status qcf_kv_deviation(const qcf_bf16* k_new, const qcf_bf16* v_new, const int32_t* pos, int n,
+                            const qcf_bf16* K_cache, const qcf_bf16* V_cache, int T, int Hkv, int D, float* dev,
+                            void* stream) {
+  if (!k_new || !v_new || !pos || !K_cache || !V_cache || !dev)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_kv_deviation: NULL pointer");
+  if (n < 0 || T < 0 || Hkv <= 0 || D <= 0 || (Hkv * D) % 8)
+    return set_error(QCF_ERR_SHAPE, "qcf_kv_deviation: n=%d T=%d Hkv=%d D=%d", n, T, Hkv, D);
+  if (take_fault(4) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(K_cache) || !aligned16(V_cache))
+    return set_error(QCF_ERR_ALIGN, "qcf_kv_deviation: alignment");
+  cudaError_t e = launch_kv_deviation(reinterpret_cast<const __nv_bfloat16*>(k_new),
+                                      reinterpret_cast<const __nv_bfloat16*>(v_new), pos, n,
+                                      reinterpret_cast<const __nv_bfloat16*>(K_cache),
+                                      reinterpret_cast<const __nv_bfloat16*>(V_cache), T, Hkv * D, dev,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_kv_deviation: launch");
 }
 
 qcf_status qcf_topn_select(const float* scores, int C, int N, int32_t* sel, void* stream) {

@@ -119,11 +119,20 @@ class ChunkStore:
         return c
 
 
+SELECT_CRITICAL, SELECT_ALL_LAYERS, SELECT_HKVD = 0, 1, 2
+
+
 class FusedRequest:
-    """Inputs, outputs and workspace of one fused prefill (structs for qcf_request_prefill)."""
+    """Inputs, outputs and workspace of one fused prefill (structs for qcf_request_prefill).
+
+    selector: SELECT_CRITICAL (QCFuse; the store's critical layer, L-1 for QCLast),
+    SELECT_ALL_LAYERS (QCAll) or SELECT_HKVD (CacheBlend's KV-deviation selection with
+    gradual filtering, kept shares `layer_ratio_bp` [L], non-increasing, ending at ratio_bp).
+    """
 
     def __init__(self, model: DeviceModel, store: ChunkStore, chunk_ids: Sequence[int], query_ids: np.ndarray,
-                 ratio_bp: int, forced_sel: Optional[np.ndarray] = None):
+                 ratio_bp: int, forced_sel: Optional[np.ndarray] = None, selector: int = SELECT_CRITICAL,
+                 layer_ratio_bp: Optional[Sequence[int]] = None):
         s = model.spec
         dev = model.device
         self.model, self.store = model, store
@@ -150,9 +159,18 @@ class FusedRequest:
         self.forced = None
         if forced_sel is not None:
             self.forced = torch.as_tensor(np.sort(np.asarray(forced_sel, np.int32)), device=dev)
+        self.selector = int(selector)
+        self._sched = None
+        self.layer_N = None
+        if self.selector == SELECT_HKVD:
+            if layer_ratio_bp is None or len(layer_ratio_bp) != s.n_layers:
+                raise ValueError("HKVD needs one kept share per layer")
+            self._sched = (C.c_int32 * s.n_layers)(*[int(v) for v in layer_ratio_bp])
+            self.layer_N = [Q.qcf_num_selected(self.C, int(v)) for v in layer_ratio_bp]
         self.req = _lib.Request(len(chunks), self._lens, self._kh, self._vh, A, self._aidx, self._akh, self._avh,
                                 self.ids.data_ptr(), self.Q, store.crit, int(ratio_bp),
-                                self.forced.data_ptr() if self.forced is not None else None)
+                                self.forced.data_ptr() if self.forced is not None else None, self.selector,
+                                self._sched)
         kv = (self.T, s.n_kv_heads, s.head_dim)
         self.K = [torch.empty(kv, dtype=torch.bfloat16, device=dev) for _ in range(s.n_layers)]
         self.V = [torch.empty(kv, dtype=torch.bfloat16, device=dev) for _ in range(s.n_layers)]
@@ -165,12 +183,16 @@ class FusedRequest:
         self.x_rows = torch.empty((self.ns, s.d_model), dtype=torch.float32, device=dev)
         self._kp = (C.c_void_p * s.n_layers)(*[k.data_ptr() for k in self.K])
         self._vp = (C.c_void_p * s.n_layers)(*[v.data_ptr() for v in self.V])
+        self.layer_sel = None
+        if self.selector == SELECT_HKVD:
+            self.layer_sel = torch.zeros((s.n_layers, max(1, self.layer_N[0])), dtype=torch.int32, device=dev)
         self.outs = _lib.Outputs(self._kp, self._vp, self.sel.data_ptr(), self.scores.data_ptr(),
                                  self.q_crit.data_ptr(), self.logits.data_ptr(), self.token.data_ptr(),
-                                 self.token_host.data_ptr(), self.x_rows.data_ptr())
-        nA = len(chunks) * A if store.crit > 0 else 0
-        nb = _lib.lib().qcf_request_workspace_size(C.byref(model.struct.dims), self.C, self.Q, max(nA, len(chunks) * A),
-                                                   self.N)
+                                 self.token_host.data_ptr(), self.x_rows.data_ptr(),
+                                 self.layer_sel.data_ptr() if self.layer_sel is not None else None)
+        nb = _lib.lib().qcf_request_workspace_size_for(C.byref(model.struct.dims), C.byref(self.req))
+        if nb == 0:
+            raise ValueError("malformed request (workspace size 0)")
         self.ws = torch.empty(max(256, nb), dtype=torch.uint8, device=dev)
 
     def run(self, compute_stream=None, copy_stream=None, ids_from_host: bool = False) -> None:

@@ -175,6 +175,16 @@ def qcf_scatter_kv(k_new, v_new, pos, K_cache, V_cache, stream=None) -> None:
          K_cache.shape[0], _stream(stream))
 
 
+def qcf_kv_deviation(k_new, v_new, pos, K_cache, V_cache, stream=None):
+    """dev[i] = |k_new[i] - K_cache[pos[i]]|^2 + |v_new[i] - V_cache[pos[i]]|^2 (fp32)."""
+    _need_cuda(k_new, v_new, pos, K_cache, V_cache)
+    n, Hkv, D = k_new.shape
+    dev = torch.empty(n, dtype=torch.float32, device=k_new.device)
+    call("qcf_kv_deviation", _ptr(k_new), _ptr(v_new), _ptr(pos), n, _ptr(K_cache), _ptr(V_cache), K_cache.shape[0],
+         Hkv, D, _ptr(dev), _stream(stream))
+    return dev
+
+
 def qcf_sparse_causal_attn(q, pos, K, V, scale: float, want_lse: bool = False, stream=None):
     _need_cuda(q, pos, K, V)
     n, Hq, D = q.shape
