@@ -172,6 +172,46 @@ def gemm_flops(spec, n_rows, ffn_padded):
             "gemm_down_resid": 2.0 * n_rows * ffn_padded * d}
 
 
+def hkvd_schedule(L, ratio_bp):
+    """Kept share per layer for the KV-deviation selector: 2r at layer 0 falling linearly to r."""
+    sched = [int(round(2 * ratio_bp - ratio_bp * l / (L - 1))) for l in range(L)]
+    sched[-1] = ratio_bp
+    return sched
+
+
+def time_selectors(dm, store, fr, spec, req, cs, xs, reps):
+    """TTFT (CUDA events on the compute stream) of the selector variants on the same chunks and query."""
+    from rag_kv_cache_re_gb300 import model as M
+    store_last = M.ChunkStore(dm, spec.n_layers - 1, req.n_anchor)   # QCLast: anchors and profile at the last layer
+    for c in fr.chunk_ids:
+        store_last.ingest(c, store.chunks[c].tokens)
+    query = fr.ids_host[fr.C:].numpy()
+    sched = hkvd_schedule(spec.n_layers, req.ratio_bp)
+    variants = {
+        "qclast": M.FusedRequest(dm, store_last, fr.chunk_ids, query, req.ratio_bp),
+        "qcall": M.FusedRequest(dm, store, fr.chunk_ids, query, req.ratio_bp, selector=M.SELECT_ALL_LAYERS),
+        "hkvd": M.FusedRequest(dm, store, fr.chunk_ids, query, req.ratio_bp, selector=M.SELECT_HKVD,
+                               layer_ratio_bp=sched),
+    }
+    out = {}
+    for name, v in variants.items():
+        for _ in range(2):
+            v.run(cs, xs)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        for _ in range(reps):
+            v.run(cs, xs)
+        e1.record(cs)
+        torch.cuda.synchronize()
+        out[f"{name}_ttft_ms"] = round(e0.elapsed_time(e1) / reps, 3)
+    out["hkvd_schedule_bp"] = f"{sched[0]} at layer 0 falling linearly to {sched[-1]} at layer {spec.n_layers - 1}"
+    out["hkvd_rows_per_layer"] = [n + fr.Q for n in variants["hkvd"].layer_N]
+    del variants, store_last
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     from rag_kv_cache_re_gb300 import qcf as Q
     world, rank, local = _dist_env()
@@ -265,6 +305,9 @@ def run_gpu(args):
     torch.cuda.synchronize()
     full_ms = reduce_max_over_ranks(f0.elapsed_time(f1) / n_full, world, device)
 
+    # ---- the selector variants on the same request: QCLast, QCAll, CacheBlend HKVD
+    selectors = None if args.no_selectors else time_selectors(dm, store, fr, spec, req, cs, xs, max(2, min(5, args.steps)))
+
     # ---- roofline of the dominant kernel (gate/up GEMM with SwiGLU epilogue)
     peaks = load_peaks()
     flops = gemm_flops(spec, fr.ns, dm.ffn_padded)
@@ -311,6 +354,8 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h, "ttft_ms": round(e_ms / args.steps, 3)},
         "gpu_launches": int(launches), "clocks": clk, "roofline": roofline, "kernels": kernels,
     }
+    if selectors:
+        out["selectors"] = selectors
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(dm, fr, budget_s=args.cpu_budget)
     if rank == 0:
@@ -500,6 +545,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["qcf", "reference"], default="qcf")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-selectors", action="store_true", help="skip timing the QCLast, QCAll and HKVD variants")
     ap.add_argument("--sweep", action="store_true", help="time the kernel-sweep shapes instead of the request")
     args = ap.parse_args(argv)
     if args.warmup < 3:
