@@ -212,6 +212,51 @@ def time_selectors(dm, store, fr, spec, req, cs, xs, reps):
     return out
 
 
+def time_dedupe(dm, store, fr, spec, req, cs, xs, reps):
+    """Two 8B requests sharing 70 % of their chunks: one after the other vs one batch
+    whose shared chunks cross the host link once per layer (TTFT of both, bytes sent)."""
+    from rag_kv_cache_re_gb300 import model as M
+    sets = qd.shared_chunk_requests(req.n_chunks, 0.70)
+    for c in sorted(set(np.concatenate(sets).tolist())):
+        if int(c) not in store.chunks:
+            store.ingest(int(c), qd.chunk_tokens(int(c), req.chunk_len, spec.vocab))
+    make = lambda: [M.FusedRequest(dm, store, list(map(int, ids)), qd.query_tokens(i, req.query_len, spec.vocab),
+                                   req.ratio_bp) for i, ids in enumerate(sets)]
+    seq, bat = make(), make()
+
+    def run_seq():
+        for r in seq:
+            r.run(cs, xs)
+
+    h2d = {}
+
+    def run_bat():
+        h2d["batch"] = M.run_batch(bat, cs, xs)
+
+    out = {}
+    for name, fn in (("sequential", run_seq), ("batched", run_bat)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        for _ in range(reps):
+            fn()
+        e1.record(cs)
+        torch.cuda.synchronize()
+        out[f"{name}_ms"] = round(e0.elapsed_time(e1) / reps, 3)
+    same = all(torch.equal(a.logits, b.logits) and torch.equal(a.selected, b.selected) for a, b in zip(seq, bat))
+    per_req = sum(store.chunks[int(c)].K.numel() * 2 + store.chunks[int(c)].V.numel() * 2 for c in sets[0])
+    anchors = sum(store.chunks[int(c)].aK[: req.crit_layer].numel() * 4 for ids in sets for c in ids)
+    out.update({"requests": len(sets), "chunks_per_request": req.n_chunks,
+                "distinct_chunks": len(set(np.concatenate(sets).tolist())),
+                "h2d_bytes_sequential": int(2 * per_req + anchors), "h2d_bytes_batched": int(h2d["batch"]),
+                "results_equal": bool(same)})
+    del seq, bat
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     from rag_kv_cache_re_gb300 import qcf as Q
     world, rank, local = _dist_env()
@@ -307,6 +352,7 @@ def run_gpu(args):
 
     # ---- the selector variants on the same request: QCLast, QCAll, CacheBlend HKVD
     selectors = None if args.no_selectors else time_selectors(dm, store, fr, spec, req, cs, xs, max(2, min(5, args.steps)))
+    dedupe = None if args.no_selectors else time_dedupe(dm, store, fr, spec, req, cs, xs, max(2, min(5, args.steps)))
 
     # ---- roofline of the dominant kernel (gate/up GEMM with SwiGLU epilogue)
     peaks = load_peaks()
@@ -356,6 +402,8 @@ def run_gpu(args):
     }
     if selectors:
         out["selectors"] = selectors
+    if dedupe:
+        out["shared_chunks"] = dedupe
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(dm, fr, budget_s=args.cpu_budget)
     if rank == 0:

@@ -370,6 +370,24 @@ size_t qcf_request_workspace_size_for(const qcf_dims* dims, const qcf_request* r
 qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, void* ws,
                                size_t ws_bytes, void* compute_stream, void* copy_stream);
 
+/* Several requests whose retrieved chunks overlap (QCFuse 1: retrieved context chunks of
+ * different queries overlap by more than 70 %; 2.B: a position-independent cache index
+ * with content-based hash search).  A chunk is the same chunk when two requests pass the
+ * same host K and V arrays with the same length (a content-keyed chunk store gives equal
+ * chunks the same arrays).  On copy_stream every distinct chunk's K and V of a layer
+ * cross the host link once, into a shared staging area, and are written from there into
+ * each request's fused cache with that request's own offset (keys re-rotated, values
+ * copied); on compute_stream the requests then run one after another exactly as
+ * qcf_request_prefill would, each waiting only for the layers it reaches.  Results equal
+ * those of qcf_request_prefill per request.
+ *   reqs, outs   host arrays [n_req], 1 <= n_req <= 64, any selectors
+ *   ws           device, qcf_batch_workspace_size(dims, reqs, n_req) bytes, caller-owned
+ *   h2d_bytes    host, nullable: bytes this call sends host -> device
+ * Enqueues only; argument errors are returned before any launch. */
+size_t qcf_batch_workspace_size(const qcf_dims* dims, const qcf_request* reqs, int n_req);
+qcf_status qcf_batch_prefill(const qcf_model* m, const qcf_request* reqs, const qcf_outputs* outs, int n_req,
+                             void* ws, size_t ws_bytes, void* compute_stream, void* copy_stream, int64_t* h2d_bytes);
+
 /* Embedding rows as fp32 residual: x[i] = embed[ids[rows[i]]] (device). */
 qcf_status qcf_embed_rows(const qcf_model* m, const int32_t* ids, const int32_t* rows, int n, float* x,
                           void* stream);

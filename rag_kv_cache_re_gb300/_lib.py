@@ -98,6 +98,9 @@ PROTOTYPES = {
     "qcf_request_workspace_size": (SZ, [C.POINTER(Dims), I, I, I, I]),
     "qcf_request_workspace_size_for": (SZ, [C.POINTER(Dims), C.POINTER(Request)]),
     "qcf_kv_deviation": (I, [P, P, P, I, P, P, I, I, I, P, P]),
+    "qcf_batch_workspace_size": (SZ, [C.POINTER(Dims), C.POINTER(Request), I]),
+    "qcf_batch_prefill": (I, [C.POINTER(Model), C.POINTER(Request), C.POINTER(Outputs), I, P, SZ, P, P,
+                              C.POINTER(C.c_int64)]),
     "qcf_request_prefill": (I, [C.POINTER(Model), C.POINTER(Request), C.POINTER(Outputs), P, SZ, P, P]),
     "qcf_embed_rows": (I, [C.POINTER(Model), P, P, I, P, P]),
     "qcf_lm_head_workspace_size": (SZ, [C.POINTER(Dims)]),

@@ -2,7 +2,9 @@
 // fused-prefill driver (probe -> profile -> top-N -> pipelined per-layer recompute).
 #include <algorithm>
 #include <cmath>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "qcf_internal.cuh"
@@ -465,127 +467,24 @@ static EventPool& event_pool() {
   return p;
 }
 
-}  // namespace qcf
+// Everything a request needs between validation and its launches.
+struct ReqPlan {
+  bool all_layers = false, hkvd = false;
+  int C = 0, Q = 0, T = 0, N = 0, crit = 0, A = 0, nA = 0;
+  std::vector<int32_t> seg_start, seg_delta;
+  ChunkOffsets co;
+  std::vector<int> Nl;
+  RequestLayout rl{};
+  HkvdLayout H{};
+  float* scores = nullptr;
+  int32_t* sel = nullptr;
+  __nv_bfloat16* q_crit = nullptr;
+  size_t ws_used = 0;
+};
 
-using namespace qcf;
-
-extern "C" {
-
-size_t qcf_layer_workspace_size(const qcf_dims* dims, int n, int T) {
-  if (!dims || n <= 0 || T <= 0) return 0;
-  return layer_ws_bytes(*dims, n, T);
-}
-
-qcf_status qcf_fused_layer_forward(const qcf_model* m, int layer, float* x, const int32_t* rope_pos,
-                                   const int32_t* cache_row, int n, qcf_bf16* K_cache, qcf_bf16* V_cache, int T,
-                                   void* ws, size_t ws_bytes, void* stream) {
-  qcf_status s = check_model(m, "qcf_fused_layer_forward");
-  if (s != QCF_OK) return s;
-  if (!x || !rope_pos || !cache_row || !K_cache || !V_cache || !ws)
-    return set_error(QCF_ERR_INVALID_ARG, "qcf_fused_layer_forward: NULL pointer");
-  if (layer < 0 || layer >= m->dims.n_layers || n < 0 || T <= 0 || n > T)
-    return set_error(QCF_ERR_SHAPE, "qcf_fused_layer_forward: layer=%d n=%d T=%d", layer, n, T);
-  if (m->rope.max_pos < T) return set_error(QCF_ERR_SHAPE, "qcf_fused_layer_forward: RoPE table shorter than T");
-  if (take_fault(4) || !aligned16(x) || !aligned16(K_cache) || !aligned16(V_cache) || !aligned16(ws))
-    return set_error(QCF_ERR_ALIGN, "qcf_fused_layer_forward: alignment");
-  if (take_fault(2) || ws_bytes < layer_ws_bytes(m->dims, n, T))
-    return set_error(QCF_ERR_WORKSPACE, "qcf_fused_layer_forward: workspace %zu < %zu", ws_bytes,
-                     layer_ws_bytes(m->dims, n, T));
-  if (n == 0) return QCF_OK;
-  Carve c{static_cast<uint8_t*>(ws), ws_bytes};
-  LayerBufs b;
-  if (!carve_layer(c, m->dims, n, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_fused_layer_forward: workspace");
-  return layer_forward_impl(m, layer, x, rope_pos, cache_row, n, reinterpret_cast<__nv_bfloat16*>(K_cache),
-                            reinterpret_cast<__nv_bfloat16*>(V_cache), T, b, static_cast<cudaStream_t>(stream));
-}
-
-size_t qcf_full_prefill_workspace_size(const qcf_dims* dims, int T) {
-  if (!dims || T <= 0) return 0;
-  Carve c{nullptr, 0};
-  c.take<float>(static_cast<size_t>(T) * dims->d_model);
-  c.take<int32_t>(T);
-  c.take<uint8_t>(256);
-  c.take<uint8_t>(layer_ws_bytes(*dims, T, T));
-  return c.used;
-}
-
-qcf_status qcf_full_prefill(const qcf_model* m, const int32_t* ids, int T, qcf_bf16* const* K_layers,
-                            qcf_bf16* const* V_layers, float* last_logits, int32_t* first_token, void* ws,
-                            size_t ws_bytes, void* stream) {
-  qcf_status s = check_model(m, "qcf_full_prefill");
-  if (s != QCF_OK) return s;
-  if (!ids || !K_layers || !V_layers || !last_logits || !first_token || !ws)
-    return set_error(QCF_ERR_INVALID_ARG, "qcf_full_prefill: NULL pointer");
-  if (T <= 0 || m->rope.max_pos < T) return set_error(QCF_ERR_SHAPE, "qcf_full_prefill: T=%d (RoPE table %d)", T, m->rope.max_pos);
-  for (int l = 0; l < m->dims.n_layers; ++l)
-    if (!K_layers[l] || !V_layers[l] || !aligned16(K_layers[l]) || !aligned16(V_layers[l]))
-      return set_error(QCF_ERR_ALIGN, "qcf_full_prefill: layer %d cache pointer NULL or misaligned", l);
-  if (take_fault(2) || ws_bytes < qcf_full_prefill_workspace_size(&m->dims, T))
-    return set_error(QCF_ERR_WORKSPACE, "qcf_full_prefill: workspace too small");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  Carve c{static_cast<uint8_t*>(ws), ws_bytes};
-  float* x = c.take<float>(static_cast<size_t>(T) * m->dims.d_model);
-  int32_t* pos = c.take<int32_t>(T);
-  void* lm_ws = c.take<uint8_t>(256);
-  LayerBufs b;
-  if (!carve_layer(c, m->dims, T, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_full_prefill: workspace");
-  cudaError_t e = launch_embed(reinterpret_cast<const __nv_bfloat16*>(m->embed), m->dims.vocab, m->dims.d_model, ids,
-                               nullptr, 0, T, x, st);
-  if (e != cudaSuccess) return cuda_error(e, "qcf_full_prefill: embed");
-  {
-    LaunchScope ls(KC_MISC, st);
-    iota_kernel<<<(T + 255) / 256, 256, 0, st>>>(pos, T, 0);
-  }
-  for (int l = 0; l < m->dims.n_layers; ++l) {
-    s = layer_forward_impl(m, l, x, pos, pos, T, reinterpret_cast<__nv_bfloat16*>(K_layers[l]),
-                           reinterpret_cast<__nv_bfloat16*>(V_layers[l]), T, b, st);
-    if (s != QCF_OK) return s;
-  }
-  e = launch_lm_head(m, x + static_cast<size_t>(T - 1) * m->dims.d_model, last_logits, first_token, lm_ws, st);
-  return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_full_prefill: lm head");
-}
-
-size_t qcf_request_workspace_size(const qcf_dims* dims, int C, int Q, int n_anchor_total, int N) {
-  if (!dims || C <= 0 || Q <= 0 || N < 0 || N > C || n_anchor_total < 0) return 0;
-  // staging holds every chunk's anchors for the probe layers; bound it by the total anchor count
-  Carve c{nullptr, 0};
-  RequestLayout r;
-  const int crit = dims->n_layers;  // upper bound on probe layers
-  carve_request(c, *dims, C, Q, n_anchor_total, N, 1, crit, n_anchor_total > 0 ? n_anchor_total : 1, &r);
-  return c.used;
-}
-
-size_t qcf_request_workspace_size_for(const qcf_dims* dims, const qcf_request* r) {
-  if (!dims || !r || !r->chunk_len || r->n_chunks <= 0 || r->n_chunks > kMaxReqChunks || r->query_len <= 0 ||
-      r->ratio_bp < 0 || r->ratio_bp > 10000 || r->n_anchor < 0)
-    return 0;
-  long long Cl = 0;
-  for (int c = 0; c < r->n_chunks; ++c) {
-    if (r->chunk_len[c] <= 0) return 0;
-    Cl += r->chunk_len[c];
-  }
-  if (Cl > (1 << 30)) return 0;
-  const int C = static_cast<int>(Cl), Q = r->query_len, L = dims->n_layers;
-  int N = 0;
-  qcf_num_selected(C, r->ratio_bp, &N);
-  Carve c{nullptr, 0};
-  if (r->selector == QCF_SELECT_HKVD) {
-    std::vector<int> Nl;
-    if (!hkvd_counts(r->layer_ratio_bp, L, C, r->ratio_bp, &Nl)) return 0;
-    HkvdLayout H;
-    carve_hkvd(c, *dims, C, Q, Nl, &H);
-    return c.used;
-  }
-  const int crit = r->selector == QCF_SELECT_ALL_LAYERS ? L - 1 : r->crit_layer;
-  if (crit < 0 || crit >= L) return 0;
-  const int nA = crit > 0 ? r->n_anchor * r->n_chunks : 0;
-  RequestLayout rl;
-  carve_request(c, *dims, C, Q, nA, N, r->n_chunks, crit, r->n_anchor, &rl);
-  return c.used;
-}
-
-qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, void* ws,
-                               size_t ws_bytes, void* compute_stream, void* copy_stream) {
+// Validates a request and carves its buffers from ws.
+static qcf_status request_plan(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, void* ws,
+                               size_t ws_bytes, ReqPlan* P) {
   qcf_status s = check_model(m, "qcf_request_prefill");
   if (s != QCF_OK) return s;
   if (!r || !out || !ws || !r->chunk_len || !r->chunk_K_host || !r->chunk_V_host || !r->ids)
@@ -639,35 +538,53 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
   const bool carved = hkvd ? carve_hkvd(cv, d, C, Q, Nl, &H) : carve_request(cv, d, C, Q, nA, N, r->n_chunks, crit, A, &rl);
   if (take_fault(2) || !carved)
     return set_error(QCF_ERR_WORKSPACE, "qcf_request_prefill: workspace %zu too small (need %zu)", ws_bytes, cv.used);
-  float* scores = out->scores ? out->scores : (hkvd ? H.dev : rl.scores);
-  int32_t* sel = out->sel ? out->sel : rl.sel;
-  __nv_bfloat16* q_crit = out->q_crit ? reinterpret_cast<__nv_bfloat16*>(out->q_crit) : rl.q_crit;
+  P->all_layers = all_layers;
+  P->hkvd = hkvd;
+  P->C = C; P->Q = Q; P->T = T; P->N = N; P->crit = crit; P->A = A; P->nA = nA;
+  P->seg_start = std::move(seg_start);
+  P->seg_delta = std::move(seg_delta);
+  P->co = co;
+  P->Nl = std::move(Nl);
+  P->rl = rl;
+  P->H = H;
+  P->scores = out->scores ? out->scores : (hkvd ? H.dev : rl.scores);
+  P->sel = out->sel ? out->sel : rl.sel;
+  P->q_crit = out->q_crit ? reinterpret_cast<__nv_bfloat16*>(out->q_crit) : rl.q_crit;
+  P->ws_used = cv.used;
+  return QCF_OK;
 
-  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
-  cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+}
+
+// Host-to-device copies of the request's anchor stores for the probe layers.
+static qcf_status request_copy_anchors(const qcf_model* m, const qcf_request* r, const ReqPlan& P, cudaStream_t xs) {
+  const qcf_dims& d = m->dims;
+  const int nA = P.nA, crit = P.crit, A = P.A;
+  const RequestLayout& rl = P.rl;
   const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim;
   const size_t eb = sizeof(qcf_bf16);
-
-  EventPool& pool = event_pool();
-  std::lock_guard<std::mutex> lk(pool.mu);
-  cudaEvent_t* ev = nullptr;
-  if (!pool.get(static_cast<size_t>(L) + 3, &ev)) return set_error(QCF_ERR_CUDA, "qcf_request_prefill: event create");
-  cudaEvent_t ev_start = ev[0], ev_anchor = ev[1], ev_crit = ev[2];
-  cudaEvent_t* ev_layer = ev + 3;
-
-  cudaError_t e = cudaEventRecord(ev_start, cs);
-  if (e != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record start");
-  if ((e = cudaStreamWaitEvent(xs, ev_start, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: copy wait");
-
-  // ---- copy stream: anchors of the probe layers, the critical layer's keys, then every layer in order
-  if (take_fault(3)) return set_error(QCF_ERR_CUDA, "qcf_request_prefill: injected host-to-device copy failure");
+  cudaError_t e = cudaSuccess;
   for (int c = 0; c < r->n_chunks && nA > 0; ++c) {
     const size_t n_el = static_cast<size_t>(crit) * A * HD;
     if ((e = cudaMemcpyAsync(rl.stK + c * n_el, r->anchor_K_host[c], n_el * eb, cudaMemcpyHostToDevice, xs)) != cudaSuccess ||
         (e = cudaMemcpyAsync(rl.stV + c * n_el, r->anchor_V_host[c], n_el * eb, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
       return cuda_error(e, "qcf_request_prefill: anchor copy");
   }
-  if ((e = cudaEventRecord(ev_anchor, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
+  return QCF_OK;
+}
+
+// The request's chunk K/V of every layer straight into its fused cache: the critical
+// layer's keys first (ev_crit), then layer by layer (ev_layer[l]), each layer's keys
+// re-rotated to their offsets on the copy stream right after they land.
+static qcf_status request_copy_layers(const qcf_model* m, const qcf_request* r, const qcf_outputs* out,
+                                      const ReqPlan& P, cudaStream_t xs, cudaEvent_t ev_crit,
+                                      const cudaEvent_t* ev_layer) {
+  const qcf_dims& d = m->dims;
+  const int L = d.n_layers, C = P.C, crit = P.crit;
+  const std::vector<int32_t>& seg_start = P.seg_start;
+  const std::vector<int32_t>& seg_delta = P.seg_delta;
+  const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim;
+  const size_t eb = sizeof(qcf_bf16);
+  cudaError_t e = cudaSuccess;
   auto copy_layer = [&](int l, bool keys, bool values) -> cudaError_t {
     for (int c = 0; c < r->n_chunks; ++c) {
       const int len = r->chunk_len[c];
@@ -684,8 +601,6 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
     }
     return cudaSuccess;
   };
-  // Each layer's chunk keys are re-rotated to their offsets on the copy stream right
-  // after they land, so the rotation overlaps the recompute of earlier layers.
   auto rotate_layer = [&](int l) -> cudaError_t {
     __nv_bfloat16* Kl = reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]);
     return launch_reposition(Kl, Kl, C, d.n_kv_heads, d.head_dim, seg_start.data(), seg_delta.data(), r->n_chunks,
@@ -700,6 +615,27 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
     if ((e = cudaEventRecord(ev_layer[l], xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
   }
 
+  return QCF_OK;
+}
+
+// The compute stream of one request: probe, profile and selection (or the
+// KV-deviation filter), the per-layer recompute waiting on ev_layer[l], LM head.
+static qcf_status request_compute(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, ReqPlan& P,
+                                  cudaStream_t cs, cudaEvent_t ev_anchor, cudaEvent_t ev_crit,
+                                  const cudaEvent_t* ev_layer) {
+  const qcf_dims& d = m->dims;
+  const int L = d.n_layers;
+  const bool all_layers = P.all_layers, hkvd = P.hkvd;
+  const int C = P.C, Q = P.Q, T = P.T, N = P.N, crit = P.crit, A = P.A, nA = P.nA;
+  const std::vector<int>& Nl = P.Nl;
+  const ChunkOffsets& co = P.co;
+  RequestLayout& rl = P.rl;
+  HkvdLayout& H = P.H;
+  float* scores = P.scores;
+  int32_t* sel = P.sel;
+  __nv_bfloat16* q_crit = P.q_crit;
+  qcf_status s = QCF_OK;
+  cudaError_t e = cudaSuccess;
   // ---- compute stream
   const __nv_bfloat16* embed = reinterpret_cast<const __nv_bfloat16*>(m->embed);
   const float* x_final = nullptr;  // final hidden states of the recomputed rows [ns][d]
@@ -842,6 +778,357 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
       (e = cudaMemcpyAsync(out->first_token_host, out->first_token, sizeof(int32_t), cudaMemcpyDeviceToHost, cs)) !=
           cudaSuccess)
     return cuda_error(e, "qcf_request_prefill: first token copy");
+  return QCF_OK;
+}
+
+// ------------------------------------------------------------------ batches with shared chunks
+
+constexpr int kMaxBatch = 64;
+
+// The distinct chunks of a batch (the same host K and V arrays and length; a content-keyed
+// chunk store hands equal chunks the same arrays) and where each request's chunk slots
+// point in the shared staging rows.
+struct UniqueChunks {
+  std::vector<const qcf_bf16*> K, V;
+  std::vector<int> len, start;            // staging rows [start, start + len)
+  int rows = 0;
+  std::vector<std::vector<int>> of_req;   // [request][chunk slot] -> distinct chunk
+};
+
+static bool unique_chunks(const qcf_request* reqs, int n_req, UniqueChunks* U) {
+  std::map<std::tuple<const void*, const void*, int>, int> idx;
+  U->of_req.assign(n_req, {});
+  for (int i = 0; i < n_req; ++i) {
+    const qcf_request& r = reqs[i];
+    if (r.n_chunks <= 0 || !r.chunk_len || !r.chunk_K_host || !r.chunk_V_host) return false;
+    for (int c = 0; c < r.n_chunks; ++c) {
+      const auto key = std::make_tuple(static_cast<const void*>(r.chunk_K_host[c]),
+                                       static_cast<const void*>(r.chunk_V_host[c]), r.chunk_len[c]);
+      auto it = idx.find(key);
+      int u;
+      if (it == idx.end()) {
+        u = static_cast<int>(U->K.size());
+        idx.emplace(key, u);
+        U->K.push_back(r.chunk_K_host[c]);
+        U->V.push_back(r.chunk_V_host[c]);
+        U->len.push_back(r.chunk_len[c]);
+        U->start.push_back(U->rows);
+        U->rows += r.chunk_len[c];
+      } else {
+        u = it->second;
+      }
+      U->of_req[i].push_back(u);
+    }
+  }
+  return true;
+}
+
+struct BatchStaging {
+  __nv_bfloat16* K[2];   // [rows][HD] per layer parity
+  __nv_bfloat16* V[2];
+  __nv_bfloat16* Kc;     // critical-layer keys
+  std::vector<int32_t*> src_row, delta;   // per request [C]
+};
+
+static bool carve_staging(Carve& c, const qcf_dims& d, const UniqueChunks& U, const std::vector<int>& Cs,
+                          BatchStaging* B) {
+  const size_t n = static_cast<size_t>(U.rows) * d.n_kv_heads * d.head_dim;
+  for (int b = 0; b < 2; ++b) {
+    B->K[b] = c.take<__nv_bfloat16>(n);
+    B->V[b] = c.take<__nv_bfloat16>(n);
+  }
+  B->Kc = c.take<__nv_bfloat16>(n);
+  B->src_row.clear();
+  B->delta.clear();
+  for (int C : Cs) {
+    B->src_row.push_back(c.take<int32_t>(C));
+    B->delta.push_back(c.take<int32_t>(C));
+  }
+  return c.ok;
+}
+
+}  // namespace qcf
+
+using namespace qcf;
+
+extern "C" {
+
+size_t qcf_layer_workspace_size(const qcf_dims* dims, int n, int T) {
+  if (!dims || n <= 0 || T <= 0) return 0;
+  return layer_ws_bytes(*dims, n, T);
+}
+
+qcf_status qcf_fused_layer_forward(const qcf_model* m, int layer, float* x, const int32_t* rope_pos,
+                                   const int32_t* cache_row, int n, qcf_bf16* K_cache, qcf_bf16* V_cache, int T,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  qcf_status s = check_model(m, "qcf_fused_layer_forward");
+  if (s != QCF_OK) return s;
+  if (!x || !rope_pos || !cache_row || !K_cache || !V_cache || !ws)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_fused_layer_forward: NULL pointer");
+  if (layer < 0 || layer >= m->dims.n_layers || n < 0 || T <= 0 || n > T)
+    return set_error(QCF_ERR_SHAPE, "qcf_fused_layer_forward: layer=%d n=%d T=%d", layer, n, T);
+  if (m->rope.max_pos < T) return set_error(QCF_ERR_SHAPE, "qcf_fused_layer_forward: RoPE table shorter than T");
+  if (take_fault(4) || !aligned16(x) || !aligned16(K_cache) || !aligned16(V_cache) || !aligned16(ws))
+    return set_error(QCF_ERR_ALIGN, "qcf_fused_layer_forward: alignment");
+  if (take_fault(2) || ws_bytes < layer_ws_bytes(m->dims, n, T))
+    return set_error(QCF_ERR_WORKSPACE, "qcf_fused_layer_forward: workspace %zu < %zu", ws_bytes,
+                     layer_ws_bytes(m->dims, n, T));
+  if (n == 0) return QCF_OK;
+  Carve c{static_cast<uint8_t*>(ws), ws_bytes};
+  LayerBufs b;
+  if (!carve_layer(c, m->dims, n, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_fused_layer_forward: workspace");
+  return layer_forward_impl(m, layer, x, rope_pos, cache_row, n, reinterpret_cast<__nv_bfloat16*>(K_cache),
+                            reinterpret_cast<__nv_bfloat16*>(V_cache), T, b, static_cast<cudaStream_t>(stream));
+}
+
+size_t qcf_full_prefill_workspace_size(const qcf_dims* dims, int T) {
+  if (!dims || T <= 0) return 0;
+  Carve c{nullptr, 0};
+  c.take<float>(static_cast<size_t>(T) * dims->d_model);
+  c.take<int32_t>(T);
+  c.take<uint8_t>(256);
+  c.take<uint8_t>(layer_ws_bytes(*dims, T, T));
+  return c.used;
+}
+
+qcf_status qcf_full_prefill(const qcf_model* m, const int32_t* ids, int T, qcf_bf16* const* K_layers,
+                            qcf_bf16* const* V_layers, float* last_logits, int32_t* first_token, void* ws,
+                            size_t ws_bytes, void* stream) {
+  qcf_status s = check_model(m, "qcf_full_prefill");
+  if (s != QCF_OK) return s;
+  if (!ids || !K_layers || !V_layers || !last_logits || !first_token || !ws)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_full_prefill: NULL pointer");
+  if (T <= 0 || m->rope.max_pos < T) return set_error(QCF_ERR_SHAPE, "qcf_full_prefill: T=%d (RoPE table %d)", T, m->rope.max_pos);
+  for (int l = 0; l < m->dims.n_layers; ++l)
+    if (!K_layers[l] || !V_layers[l] || !aligned16(K_layers[l]) || !aligned16(V_layers[l]))
+      return set_error(QCF_ERR_ALIGN, "qcf_full_prefill: layer %d cache pointer NULL or misaligned", l);
+  if (take_fault(2) || ws_bytes < qcf_full_prefill_workspace_size(&m->dims, T))
+    return set_error(QCF_ERR_WORKSPACE, "qcf_full_prefill: workspace too small");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c{static_cast<uint8_t*>(ws), ws_bytes};
+  float* x = c.take<float>(static_cast<size_t>(T) * m->dims.d_model);
+  int32_t* pos = c.take<int32_t>(T);
+  void* lm_ws = c.take<uint8_t>(256);
+  LayerBufs b;
+  if (!carve_layer(c, m->dims, T, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_full_prefill: workspace");
+  cudaError_t e = launch_embed(reinterpret_cast<const __nv_bfloat16*>(m->embed), m->dims.vocab, m->dims.d_model, ids,
+                               nullptr, 0, T, x, st);
+  if (e != cudaSuccess) return cuda_error(e, "qcf_full_prefill: embed");
+  {
+    LaunchScope ls(KC_MISC, st);
+    iota_kernel<<<(T + 255) / 256, 256, 0, st>>>(pos, T, 0);
+  }
+  for (int l = 0; l < m->dims.n_layers; ++l) {
+    s = layer_forward_impl(m, l, x, pos, pos, T, reinterpret_cast<__nv_bfloat16*>(K_layers[l]),
+                           reinterpret_cast<__nv_bfloat16*>(V_layers[l]), T, b, st);
+    if (s != QCF_OK) return s;
+  }
+  e = launch_lm_head(m, x + static_cast<size_t>(T - 1) * m->dims.d_model, last_logits, first_token, lm_ws, st);
+  return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_full_prefill: lm head");
+}
+
+size_t qcf_request_workspace_size(const qcf_dims* dims, int C, int Q, int n_anchor_total, int N) {
+  if (!dims || C <= 0 || Q <= 0 || N < 0 || N > C || n_anchor_total < 0) return 0;
+  // staging holds every chunk's anchors for the probe layers; bound it by the total anchor count
+  Carve c{nullptr, 0};
+  RequestLayout r;
+  const int crit = dims->n_layers;  // upper bound on probe layers
+  carve_request(c, *dims, C, Q, n_anchor_total, N, 1, crit, n_anchor_total > 0 ? n_anchor_total : 1, &r);
+  return c.used;
+}
+
+size_t qcf_request_workspace_size_for(const qcf_dims* dims, const qcf_request* r) {
+  if (!dims || !r || !r->chunk_len || r->n_chunks <= 0 || r->n_chunks > kMaxReqChunks || r->query_len <= 0 ||
+      r->ratio_bp < 0 || r->ratio_bp > 10000 || r->n_anchor < 0)
+    return 0;
+  long long Cl = 0;
+  for (int c = 0; c < r->n_chunks; ++c) {
+    if (r->chunk_len[c] <= 0) return 0;
+    Cl += r->chunk_len[c];
+  }
+  if (Cl > (1 << 30)) return 0;
+  const int C = static_cast<int>(Cl), Q = r->query_len, L = dims->n_layers;
+  int N = 0;
+  qcf_num_selected(C, r->ratio_bp, &N);
+  Carve c{nullptr, 0};
+  if (r->selector == QCF_SELECT_HKVD) {
+    std::vector<int> Nl;
+    if (!hkvd_counts(r->layer_ratio_bp, L, C, r->ratio_bp, &Nl)) return 0;
+    HkvdLayout H;
+    carve_hkvd(c, *dims, C, Q, Nl, &H);
+    return c.used;
+  }
+  const int crit = r->selector == QCF_SELECT_ALL_LAYERS ? L - 1 : r->crit_layer;
+  if (crit < 0 || crit >= L) return 0;
+  const int nA = crit > 0 ? r->n_anchor * r->n_chunks : 0;
+  RequestLayout rl;
+  carve_request(c, *dims, C, Q, nA, N, r->n_chunks, crit, r->n_anchor, &rl);
+  return c.used;
+}
+
+qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, void* ws,
+                               size_t ws_bytes, void* compute_stream, void* copy_stream) {
+  ReqPlan P;
+  qcf_status s = request_plan(m, r, out, ws, ws_bytes, &P);
+  if (s != QCF_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+  cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+  const int L = m->dims.n_layers;
+  EventPool& pool = event_pool();
+  std::lock_guard<std::mutex> lk(pool.mu);
+  cudaEvent_t* ev = nullptr;
+  if (!pool.get(static_cast<size_t>(L) + 3, &ev)) return set_error(QCF_ERR_CUDA, "qcf_request_prefill: event create");
+  cudaEvent_t ev_start = ev[0], ev_anchor = ev[1], ev_crit = ev[2];
+  cudaEvent_t* ev_layer = ev + 3;
+  cudaError_t e = cudaEventRecord(ev_start, cs);
+  if (e != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record start");
+  if ((e = cudaStreamWaitEvent(xs, ev_start, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: copy wait");
+  // ---- copy stream: anchors of the probe layers, the critical layer's keys, then every layer in order
+  if (take_fault(3)) return set_error(QCF_ERR_CUDA, "qcf_request_prefill: injected host-to-device copy failure");
+  if ((s = request_copy_anchors(m, r, P, xs)) != QCF_OK) return s;
+  if ((e = cudaEventRecord(ev_anchor, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
+  if ((s = request_copy_layers(m, r, out, P, xs, ev_crit, ev_layer)) != QCF_OK) return s;
+  return request_compute(m, r, out, P, cs, ev_anchor, ev_crit, ev_layer);
+}
+
+size_t qcf_batch_workspace_size(const qcf_dims* dims, const qcf_request* reqs, int n_req) {
+  if (!dims || !reqs || n_req <= 0 || n_req > kMaxBatch) return 0;
+  size_t total = 0;
+  std::vector<int> Cs;
+  for (int i = 0; i < n_req; ++i) {
+    const size_t sz = qcf_request_workspace_size_for(dims, &reqs[i]);
+    if (!sz) return 0;
+    total = align_up(total + sz, 256);
+    int C = 0;
+    for (int c = 0; c < reqs[i].n_chunks; ++c) C += reqs[i].chunk_len[c];
+    Cs.push_back(C);
+  }
+  UniqueChunks U;
+  if (!unique_chunks(reqs, n_req, &U)) return 0;
+  Carve c{nullptr, 0};
+  BatchStaging B;
+  carve_staging(c, *dims, U, Cs, &B);
+  return total + c.used + 256;
+}
+
+qcf_status qcf_batch_prefill(const qcf_model* m, const qcf_request* reqs, const qcf_outputs* outs, int n_req,
+                             void* ws, size_t ws_bytes, void* compute_stream, void* copy_stream, int64_t* h2d_bytes) {
+  if (!m || !reqs || !outs || !ws) return set_error(QCF_ERR_INVALID_ARG, "qcf_batch_prefill: NULL pointer");
+  if (n_req <= 0 || n_req > kMaxBatch) return set_error(QCF_ERR_SHAPE, "qcf_batch_prefill: n_req=%d not in [1,%d]", n_req, kMaxBatch);
+  if (!aligned16(ws)) return set_error(QCF_ERR_ALIGN, "qcf_batch_prefill: workspace misaligned");
+  const qcf_dims& d = m->dims;
+  const int L = d.n_layers;
+  std::vector<ReqPlan> P(n_req);
+  std::vector<int> Cs;
+  size_t off = 0;
+  for (int i = 0; i < n_req; ++i) {
+    if (off > ws_bytes) return set_error(QCF_ERR_WORKSPACE, "qcf_batch_prefill: workspace too small");
+    qcf_status s = request_plan(m, &reqs[i], &outs[i], static_cast<uint8_t*>(ws) + off, ws_bytes - off, &P[i]);
+    if (s != QCF_OK) return s;
+    off = align_up(off + P[i].ws_used, 256);
+    Cs.push_back(P[i].C);
+  }
+  UniqueChunks U;
+  if (!unique_chunks(reqs, n_req, &U)) return set_error(QCF_ERR_INVALID_ARG, "qcf_batch_prefill: chunk tables");
+  if (off > ws_bytes) return set_error(QCF_ERR_WORKSPACE, "qcf_batch_prefill: workspace too small");
+  Carve cv{static_cast<uint8_t*>(ws) + off, ws_bytes - off};
+  BatchStaging B;
+  if (!carve_staging(cv, d, U, Cs, &B)) return set_error(QCF_ERR_WORKSPACE, "qcf_batch_prefill: workspace too small");
+  // row maps: request row -> staging row, and the rotation offset of its chunk in this request
+  std::vector<std::vector<int32_t>> src_row(n_req), delta(n_req);
+  for (int i = 0; i < n_req; ++i) {
+    src_row[i].resize(P[i].C);
+    delta[i].resize(P[i].C);
+    for (int c = 0; c < reqs[i].n_chunks; ++c) {
+      const int u = U.of_req[i][c], o = P[i].seg_start[c];
+      for (int j = 0; j < reqs[i].chunk_len[c]; ++j) {
+        src_row[i][o + j] = U.start[u] + j;
+        delta[i][o + j] = o;
+      }
+    }
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+  cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+  const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim;
+  const size_t eb = sizeof(qcf_bf16);
+  // events: start and anchors shared; each request has its own critical-layer and per-layer
+  // events, recorded right after its own cache rows are written, so a request never waits
+  // for another request's copies
+  EventPool& pool = event_pool();
+  std::lock_guard<std::mutex> lk(pool.mu);
+  cudaEvent_t* ev = nullptr;
+  const size_t per_req_ev = static_cast<size_t>(L) + 1;
+  if (!pool.get(2 + n_req * per_req_ev, &ev)) return set_error(QCF_ERR_CUDA, "qcf_batch_prefill: event create");
+  cudaEvent_t ev_start = ev[0], ev_anchor = ev[1];
+  auto ev_crit_of = [&](int i) { return ev[2 + i * per_req_ev]; };
+  auto ev_layer_of = [&](int i) { return ev + 2 + i * per_req_ev + 1; };
+  cudaError_t e = cudaEventRecord(ev_start, cs);
+  if (e != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: record start");
+  if ((e = cudaStreamWaitEvent(xs, ev_start, 0)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: copy wait");
+  int64_t h2d = 0;
+  for (int i = 0; i < n_req; ++i) {
+    if ((e = cudaMemcpyAsync(B.src_row[i], src_row[i].data(), P[i].C * sizeof(int32_t), cudaMemcpyHostToDevice, xs)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(B.delta[i], delta[i].data(), P[i].C * sizeof(int32_t), cudaMemcpyHostToDevice, xs)) !=
+            cudaSuccess)
+      return cuda_error(e, "qcf_batch_prefill: row maps");
+    h2d += 2 * static_cast<int64_t>(P[i].C) * sizeof(int32_t);
+  }
+  // anchors: per request (each request's probe reads its own staging)
+  for (int i = 0; i < n_req; ++i) {
+    qcf_status s = request_copy_anchors(m, &reqs[i], P[i], xs);
+    if (s != QCF_OK) return s;
+    h2d += static_cast<int64_t>(P[i].nA > 0 ? reqs[i].n_chunks : 0) * P[i].crit * P[i].A * HD * eb * 2;
+  }
+  if ((e = cudaEventRecord(ev_anchor, xs)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: record");
+  // every distinct chunk crosses the host link once per layer (and once more for a critical layer)
+  auto stage = [&](int l, __nv_bfloat16* dK, __nv_bfloat16* dV) -> cudaError_t {
+    for (size_t u = 0; u < U.K.size(); ++u) {
+      const size_t n_el = static_cast<size_t>(U.len[u]) * HD;
+      const size_t src = static_cast<size_t>(l) * n_el, dst = static_cast<size_t>(U.start[u]) * HD;
+      cudaError_t ce;
+      if (dK && (ce = cudaMemcpyAsync(dK + dst, U.K[u] + src, n_el * eb, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+        return ce;
+      if (dV && (ce = cudaMemcpyAsync(dV + dst, U.V[u] + src, n_el * eb, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+        return ce;
+      h2d += static_cast<int64_t>(n_el * eb) * ((dK ? 1 : 0) + (dV ? 1 : 0));
+    }
+    return cudaSuccess;
+  };
+  std::vector<int> crits;
+  for (int i = 0; i < n_req; ++i)
+    if (std::find(crits.begin(), crits.end(), P[i].crit) == crits.end()) crits.push_back(P[i].crit);
+  for (int c : crits) {
+    if ((e = stage(c, B.Kc, nullptr)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: critical-layer copy");
+    for (int i = 0; i < n_req; ++i) {
+      if (P[i].crit != c) continue;
+      if ((e = launch_stage_scatter(B.Kc, nullptr, B.src_row[i], B.delta[i], P[i].C, U.rows, d.n_kv_heads, d.head_dim,
+                                    &m->rope, reinterpret_cast<__nv_bfloat16*>(outs[i].K_layers[c]), nullptr, true,
+                                    false, xs)) != cudaSuccess)
+        return cuda_error(e, "qcf_batch_prefill: scatter");
+      if ((e = cudaEventRecord(ev_crit_of(i), xs)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: record");
+    }
+  }
+  for (int l = 0; l < L; ++l) {
+    bool need_k = false;
+    for (int i = 0; i < n_req; ++i) need_k |= P[i].crit != l;
+    const int b = l & 1;
+    if ((e = stage(l, need_k ? B.K[b] : nullptr, B.V[b])) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: layer copy");
+    for (int i = 0; i < n_req; ++i) {
+      if ((e = launch_stage_scatter(B.K[b], B.V[b], B.src_row[i], B.delta[i], P[i].C, U.rows, d.n_kv_heads, d.head_dim,
+                                    &m->rope, reinterpret_cast<__nv_bfloat16*>(outs[i].K_layers[l]),
+                                    reinterpret_cast<__nv_bfloat16*>(outs[i].V_layers[l]), P[i].crit != l, true, xs)) !=
+          cudaSuccess)
+        return cuda_error(e, "qcf_batch_prefill: scatter");
+      if ((e = cudaEventRecord(ev_layer_of(i)[l], xs)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: record");
+    }
+  }
+  if (h2d_bytes) *h2d_bytes = h2d;
+  // compute: the requests one after another, each waiting only for the layers it reaches
+  for (int i = 0; i < n_req; ++i) {
+    qcf_status s = request_compute(m, &reqs[i], &outs[i], P[i], cs, ev_anchor, ev_crit_of(i), ev_layer_of(i));
+    if (s != QCF_OK) return s;
+  }
   return QCF_OK;
 }
 

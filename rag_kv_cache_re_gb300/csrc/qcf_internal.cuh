@@ -107,6 +107,11 @@ cudaError_t launch_reposition(const __nv_bfloat16* src, __nv_bfloat16* dst, int6
                               const int32_t* seg_start, const int32_t* seg_delta, int n_seg, const qcf_rope_table* t,
                               cudaStream_t st);
 
+cudaError_t launch_stage_scatter(const __nv_bfloat16* stK, const __nv_bfloat16* stV, const int32_t* src_row,
+                                 const int32_t* delta, int64_t n_rows, int64_t staged_rows, int Hkv, int D,
+                                 const qcf_rope_table* t, __nv_bfloat16* K, __nv_bfloat16* V, bool do_k, bool do_v,
+                                 cudaStream_t st);
+
 // KV deviation of fresh rows against the cache (select.cu).
 cudaError_t launch_kv_deviation(const __nv_bfloat16* k_new, const __nv_bfloat16* v_new, const int32_t* pos, int n,
                                 const __nv_bfloat16* K, const __nv_bfloat16* V, int T, int width, float* dev,

@@ -31,6 +31,28 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
   return u;
 }
 
+// Pairs (a_i, b_i) = (x_k, x_{k+D/2}) turned by angles with cosines c and sines s.
+// Every product and sum is rounded on its own (no contraction into FMAs), so all
+// kernels that re-rotate keys give the same bits for the same inputs.
+__device__ __forceinline__ void rotate8(const float* a, const float* b, const float* c, const float* s, float* o1,
+                                        float* o2) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    o1[i] = __fsub_rn(__fmul_rn(a[i], c[i]), __fmul_rn(b[i], s[i]));
+    o2[i] = __fadd_rn(__fmul_rn(b[i], c[i]), __fmul_rn(a[i], s[i]));
+  }
+}
+
+__device__ __forceinline__ void load_angles8(const float* cos_t, const float* sin_t, int delta, int half, int k0,
+                                             float* c, float* s) {
+  const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(delta) * half + k0);
+  const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(delta) * half + k0);
+  *reinterpret_cast<float4*>(c) = cp[0];
+  *reinterpret_cast<float4*>(c + 4) = cp[1];
+  *reinterpret_cast<float4*>(s) = sp[0];
+  *reinterpret_cast<float4*>(s + 4) = sp[1];
+}
+
 // One thread per (row, kv head, group of 8 pair indices k..k+7): the pairs
 // (k, k + D/2) of the row's segment turn by delta * omega_k from the fp32 table.
 __global__ void __launch_bounds__(256) rope_reposition_kernel(const __nv_bfloat16* __restrict__ src,
@@ -58,20 +80,56 @@ __global__ void __launch_bounds__(256) rope_reposition_kernel(const __nv_bfloat1
   float a[8], b[8], c[8], s[8];
   bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + base + k0), a);
   bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + base + half + k0), b);
-  const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(delta) * half + k0);
-  const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(delta) * half + k0);
-  *reinterpret_cast<float4*>(c) = cp[0];
-  *reinterpret_cast<float4*>(c + 4) = cp[1];
-  *reinterpret_cast<float4*>(s) = sp[0];
-  *reinterpret_cast<float4*>(s + 4) = sp[1];
+  load_angles8(cos_t, sin_t, delta, half, k0, c, s);
   float o1[8], o2[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    o1[i] = a[i] * c[i] - b[i] * s[i];
-    o2[i] = b[i] * c[i] + a[i] * s[i];
-  }
+  rotate8(a, b, c, s, o1, o2);
   *reinterpret_cast<uint4*>(dst + base + k0) = f32_to_bf16x8(o1);
   *reinterpret_cast<uint4*>(dst + base + half + k0) = f32_to_bf16x8(o2);
+}
+
+// Batched requests share a staging copy of each distinct chunk's layer K/V; this
+// writes one request's cache rows from it: row i takes staging row src_row[i], its K
+// turned by R(delta[i]) (the request's offset of that chunk) when do_k, its V copied
+// when do_v.  One thread per (row, kv head, group of 8 pair indices).
+__global__ void __launch_bounds__(256) stage_scatter_kernel(const __nv_bfloat16* __restrict__ stK,
+                                                            const __nv_bfloat16* __restrict__ stV,
+                                                            const int32_t* __restrict__ src_row,
+                                                            const int32_t* __restrict__ delta, int64_t n_rows,
+                                                            int64_t staged_rows, int Hkv, int D,
+                                                            const float* __restrict__ cos_t,
+                                                            const float* __restrict__ sin_t, int max_pos,
+                                                            __nv_bfloat16* __restrict__ K, __nv_bfloat16* __restrict__ V,
+                                                            int do_k, int do_v, unsigned int* status) {
+  const int half = D / 2;
+  const int groups = half / 8;
+  const int64_t per_row = static_cast<int64_t>(Hkv) * groups;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (tid >= n_rows * per_row) return;
+  const int64_t row = tid / per_row;
+  const int rem = static_cast<int>(tid - row * per_row);
+  const int h = rem / groups;
+  const int k0 = (rem - h * groups) * 8;
+  const int64_t sr = src_row[row];
+  const int dl = delta[row];
+  if (sr < 0 || sr >= staged_rows || dl < 0 || dl >= max_pos) {
+    if (k0 == 0 && h == 0) flag_status(status, QCF_DEV_BAD_INDEX);
+    return;
+  }
+  const size_t sb = static_cast<size_t>(sr) * Hkv * D + static_cast<size_t>(h) * D;
+  const size_t db = static_cast<size_t>(row) * Hkv * D + static_cast<size_t>(h) * D;
+  if (do_k) {
+    float a[8], b[8], c[8], s[8], o1[8], o2[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(stK + sb + k0), a);
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(stK + sb + half + k0), b);
+    load_angles8(cos_t, sin_t, dl, half, k0, c, s);
+    rotate8(a, b, c, s, o1, o2);
+    *reinterpret_cast<uint4*>(K + db + k0) = f32_to_bf16x8(o1);
+    *reinterpret_cast<uint4*>(K + db + half + k0) = f32_to_bf16x8(o2);
+  }
+  if (do_v) {
+    *reinterpret_cast<uint4*>(V + db + k0) = *reinterpret_cast<const uint4*>(stV + sb + k0);
+    *reinterpret_cast<uint4*>(V + db + half + k0) = *reinterpret_cast<const uint4*>(stV + sb + half + k0);
+  }
 }
 
 // dst[i] = src[idx[i]] (rows of `width` bf16, width % 8 == 0); one warp per row.
@@ -306,6 +364,19 @@ static qcf_status check_seg(const int32_t* seg_start, const int32_t* seg_delta, 
 }
 
 static bool head_dim_ok(int D) { return D == 16 || D == 64 || D == 128; }
+
+cudaError_t launch_stage_scatter(const __nv_bfloat16* stK, const __nv_bfloat16* stV, const int32_t* src_row,
+                                 const int32_t* delta, int64_t n_rows, int64_t staged_rows, int Hkv, int D,
+                                 const qcf_rope_table* t, __nv_bfloat16* K, __nv_bfloat16* V, bool do_k, bool do_v,
+                                 cudaStream_t st) {
+  if (n_rows <= 0 || (!do_k && !do_v)) return cudaSuccess;
+  const int64_t threads = n_rows * Hkv * (D / 16);
+  LaunchScope ls(KC_ROPE, st);
+  stage_scatter_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(
+      stK, stV, src_row, delta, n_rows, staged_rows, Hkv, D, t->cos, t->sin, t->max_pos, K, V, do_k ? 1 : 0,
+      do_v ? 1 : 0, device_status_ptr());
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reposition(const __nv_bfloat16* src, __nv_bfloat16* dst, int64_t n_rows, int Hkv, int D,
                               const int32_t* seg_start, const int32_t* seg_delta, int n_seg, const qcf_rope_table* t,

@@ -8,6 +8,7 @@ own full prefill, anchor and gather kernels.
 from __future__ import annotations
 
 import ctypes as C
+import hashlib
 from typing import Dict, List, Optional, Sequence
 
 import numpy as np
@@ -79,11 +80,32 @@ class StoredChunk:
 
 
 class ChunkStore:
-    """Offline chunk KV (computed alone at positions 0..len-1) and key-norm anchors."""
+    """Offline chunk KV (computed alone at positions 0..len-1) and key-norm anchors.
+
+    Chunks are keyed by content: a chunk's stored K/V depends only on its tokens, so a
+    chunk id whose tokens were seen before maps to the stored chunk with those tokens
+    (the same host arrays, which the batched prefill then copies once per layer).
+    """
 
     def __init__(self, model: DeviceModel, crit_layer: int, n_anchor: int):
         self.model, self.crit, self.n_anchor = model, int(crit_layer), int(n_anchor)
         self.chunks: Dict[int, StoredChunk] = {}
+        self.by_content: Dict[bytes, StoredChunk] = {}
+
+    @staticmethod
+    def content_key(tokens) -> bytes:
+        return hashlib.sha256(np.ascontiguousarray(np.asarray(tokens, dtype=np.int32)).tobytes()).digest()
+
+    def _known(self, chunk_id: int, tokens) -> Optional[StoredChunk]:
+        c = self.by_content.get(self.content_key(tokens))
+        if c is not None:
+            self.chunks[int(chunk_id)] = c
+        return c
+
+    def _keep(self, chunk_id: int, c: StoredChunk) -> StoredChunk:
+        self.chunks[int(chunk_id)] = c
+        self.by_content[self.content_key(c.tokens)] = c
+        return c
 
     def _anchors(self, K_dev: List[torch.Tensor], V_dev: List[torch.Tensor]):
         L = len(K_dev)
@@ -99,24 +121,27 @@ class ChunkStore:
 
     def ingest(self, chunk_id: int, tokens: np.ndarray) -> StoredChunk:
         """Prefill the chunk alone on the GPU, keep its K/V and anchors in pinned host memory."""
+        known = self._known(chunk_id, tokens)
+        if known is not None:
+            return known
         ids = torch.as_tensor(np.asarray(tokens, dtype=np.int32), device=self.model.device)
         K, V, _, _ = Q.qcf_full_prefill(self.model, ids)
         idx, aK, aV = self._anchors(K, V)
         Kh = torch.stack(K).cpu().pin_memory()
         Vh = torch.stack(V).cpu().pin_memory()
-        c = StoredChunk(np.asarray(tokens, np.int32), Kh, Vh, idx, aK, aV)
-        self.chunks[int(chunk_id)] = c
-        return c
+        return self._keep(chunk_id, StoredChunk(np.asarray(tokens, np.int32), Kh, Vh, idx, aK, aV))
 
     def add_precomputed(self, chunk_id: int, tokens: np.ndarray, K: torch.Tensor, V: torch.Tensor) -> StoredChunk:
         """Store given K/V [L][len][Hkv][D] (bf16, any device) and compute its anchors on the GPU."""
+        known = self._known(chunk_id, tokens)
+        if known is not None:
+            return known
         Kd = [k.to(self.model.device).contiguous() for k in K]
         Vd = [v.to(self.model.device).contiguous() for v in V]
         idx, aK, aV = self._anchors(Kd, Vd)
-        c = StoredChunk(np.asarray(tokens, np.int32), K.to(torch.bfloat16).cpu().contiguous().pin_memory(),
-                        V.to(torch.bfloat16).cpu().contiguous().pin_memory(), idx, aK, aV)
-        self.chunks[int(chunk_id)] = c
-        return c
+        return self._keep(chunk_id, StoredChunk(np.asarray(tokens, np.int32),
+                                                K.to(torch.bfloat16).cpu().contiguous().pin_memory(),
+                                                V.to(torch.bfloat16).cpu().contiguous().pin_memory(), idx, aK, aV))
 
 
 SELECT_CRITICAL, SELECT_ALL_LAYERS, SELECT_HKVD = 0, 1, 2
@@ -207,3 +232,18 @@ class FusedRequest:
     @property
     def selected(self) -> torch.Tensor:
         return self.sel[: self.N]
+
+
+def run_batch(requests: Sequence["FusedRequest"], compute_stream=None, copy_stream=None) -> int:
+    """Enqueue several fused prefills whose shared chunks cross the host link once per
+    layer; every request's outputs land in its own FusedRequest.  Returns the bytes sent."""
+    reqs = list(requests)
+    model = reqs[0].model
+    cs = compute_stream or torch.cuda.current_stream()
+    xs = copy_stream or cs
+    structs = [r.req for r in reqs]
+    nb = Q.qcf_batch_workspace_size(model, structs)
+    if nb == 0:
+        raise ValueError("malformed batch (workspace size 0)")
+    ws = Q.workspace(nb, model.device, tag="batch")
+    return Q.qcf_batch_prefill(model, structs, [r.outs for r in reqs], ws, cs, xs)

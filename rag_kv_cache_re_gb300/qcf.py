@@ -278,3 +278,21 @@ def qcf_request_prefill(model, req: "_lib.Request", outs: "_lib.Outputs", ws: to
     """Enqueues the fused prefill of one request (structs built by model.FusedRequest)."""
     call("qcf_request_prefill", C.byref(model.struct), C.byref(req), C.byref(outs), _ptr(ws), ws.numel(),
          C.c_void_p(compute_stream.cuda_stream), C.c_void_p(copy_stream.cuda_stream))
+
+
+def qcf_batch_prefill(model, reqs, outs, ws: torch.Tensor, compute_stream, copy_stream) -> int:
+    """Enqueues several fused prefills sharing their common chunks' host-to-device copies
+    (structs built by model.FusedRequest); returns the bytes the call sends to the device."""
+    n = len(reqs)
+    ra = (_lib.Request * n)(*reqs)
+    oa = (_lib.Outputs * n)(*outs)
+    h2d = C.c_int64(0)
+    call("qcf_batch_prefill", C.byref(model.struct), ra, oa, n, _ptr(ws), ws.numel(),
+         C.c_void_p(compute_stream.cuda_stream), C.c_void_p(copy_stream.cuda_stream), C.byref(h2d))
+    return int(h2d.value)
+
+
+def qcf_batch_workspace_size(model, reqs) -> int:
+    n = len(reqs)
+    ra = (_lib.Request * n)(*reqs)
+    return int(_lib.lib().qcf_batch_workspace_size(C.byref(model.struct.dims), ra, n))

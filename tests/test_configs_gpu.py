@@ -136,6 +136,26 @@ def test_llama70b_two_requests_sharing_chunks():
     # a chunk shared by both requests sits at different offsets: where neither request
     # recomputed a token, its value rows are equal and each key is the stored key
     # rotated to that request's offset
+    # the same two requests as one batch: shared chunks cross the host link once per layer,
+    # and every result is bitwise what the request gave alone
+    batch = [M.FusedRequest(dm, store, ids, qd.query_tokens(i, req.query_len, spec.vocab), req.ratio_bp)
+             for i, ids in enumerate(reqs)]
+    h2d = M.run_batch(batch, cs, xs)
+    torch.cuda.synchronize()
+    for fr, bt in zip(frs, batch):
+        assert torch.equal(fr.selected, bt.selected) and torch.equal(fr.logits, bt.logits)
+        for l in (0, req.crit_layer, spec.n_layers - 1):
+            assert torch.equal(fr.K[l], bt.K[l]) and torch.equal(fr.V[l], bt.V[l])
+    row_bytes = spec.n_kv_heads * spec.head_dim * 2
+    layer_bytes = req.chunk_len * row_bytes
+    n_distinct = len(set(np.concatenate(reqs).tolist()))
+    assert n_distinct == 45
+    # distinct chunks: V of every layer, K of every other layer, the critical layer's K once;
+    # per request: the anchors of the probe layers and two int32 row maps
+    per_req = 2 * req.n_chunks * req.crit_layer * req.n_anchor * row_bytes + 2 * req.n_chunks * req.chunk_len * 4
+    assert h2d == n_distinct * layer_bytes * 2 * spec.n_layers + 2 * per_req
+    assert h2d < 0.7 * 2 * req.n_chunks * layer_bytes * 2 * spec.n_layers   # the two requests alone: 70 chunks
+    del batch
     a, b = frs
     shared = sorted(set(a.chunk_ids) & set(b.chunk_ids))[:3]
     sa, sb = set(a.selected.cpu().numpy().tolist()), set(b.selected.cpu().numpy().tolist())
