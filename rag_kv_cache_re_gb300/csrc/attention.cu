@@ -10,6 +10,7 @@
 // in, fp32 accumulate); the softmax is online in fp32 registers with quad
 // shuffles for the row max.  Blocks are scheduled longest (highest position)
 // first.
+#include <algorithm>
 #include <mutex>
 
 #include "qcf_internal.cuh"
@@ -690,7 +691,18 @@ static AttnPlan plan_attn(int n, int T, int Hq, int Hkv, int D) {
   const int max_tiles = (T + kKeyTile - 1) / kKeyTile;
   p.split_tiles = max_tiles;
   p.max_splits = 1;
-  if (p.n_blocks * Hkv < 4 * num_sms() && max_tiles > 16) {
+  const int ctas = p.n_blocks * Hkv, sms = num_sms();
+  if (D == 128) {
+    // tensor-core kernel, one CTA per SM: a CTA's set-up and drain cost more than the
+    // imbalance of unsplit rows once every SM has a CTA (8B recompute shape: 81 us
+    // unsplit vs 99 us with 4 splits plus the combine), so split only a grid smaller
+    // than the SM count, into at most 4 ranges of at least 16 tiles
+    if (ctas < sms && max_tiles > 16) {
+      p.max_splits = std::min(4, (sms + ctas - 1) / ctas);
+      p.split_tiles = std::max(16, (max_tiles + p.max_splits - 1) / p.max_splits);
+      p.max_splits = (max_tiles + p.split_tiles - 1) / p.split_tiles;
+    }
+  } else if (ctas < 4 * sms && max_tiles > 16) {
     p.max_splits = 4;
     p.split_tiles = (max_tiles + p.max_splits - 1) / p.max_splits;
     if (p.split_tiles < 8) p.split_tiles = 8;
