@@ -288,47 +288,40 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
 // ------------------------------------------------------------------ tensor-core (tcgen05) variant, D = 128
 //
 // One CTA = 128 score rows: BRp = floor(128 / G) consecutive recomputed rows x the
-// G query heads of one KV head (row rho = p * G + hh).  Eleven warps:
-//   warp 0     TMA producer for K: tiles of 64 keys (two 64-column boxes, 128B swizzle)
-//              into a 4-stage ring; a stage is freed by the Q.K^T that read it
+// G query heads of one KV head (row rho = p * G + hh), over key tiles of 128.  Seven warps:
+//   warp 0     TMA producer for K: tiles of 128 keys (two 64-column boxes, 128B swizzle)
+//              into a 3-stage ring; a stage is freed by the Q.K^T that read it
 //   warp 1     TMEM allocation; one thread issues the tensor-core work in groups:
-//              group g = { S_{g+2} = Q K_{g+2}^T (M=128, N=64, K=128; Q read from TMEM),
-//                          O_s += P_g V_g (M=128, N=128, K=64 keys; P read from TMEM,
-//                          V MN-major from shared memory) },
-//              after S_0 and S_1.  Every dependency of group g lands on one mbarrier,
-//              so the issuing thread waits once per tile: a barrier read stalls the
-//              issuing thread for longer than the tensor core needs for one of these
-//              small MMAs, so fewer reads keep the tensor pipe fed.
-//   warp 2     TMA producer for V: the same tiling, its own 4-stage ring, freed by P.V
-//   warps 3-10 two softmax streams of four warps; stream s owns the key tiles i = s
-//              (mod 2) of the CTA's range with its own S buffer, P buffer and O
-//              accumulator; stream s also stores columns [64 s, 64 s + 64) of the Q
-//              rows into TMEM.  One score row per thread: causal mask by true position
-//              (boundary tiles only), online softmax in the exp2 domain with the scale
-//              folded into one FFMA, P stored to TMEM as packed bf16 pairs, O_s rescaled
-//              in TMEM only when a row max grows by more than 2^8.  The streams are
-//              independent online softmaxes over disjoint key sets, merged once at the
-//              end (common max, rescale, sum): the algebra of merging split-KV partials.
+//              group g = { S_{g+2} = Q K_{g+2}^T  (M=128, N=128, K=128; Q read from TMEM),
+//                          O += P_g V_g          (M=128, N=128, K=128 keys; P read from TMEM,
+//                                                 V MN-major from shared memory) },
+//              after S_0 and S_1.  Every dependency of group g lands on one mbarrier, so
+//              the issuing thread reads one barrier per 16 MMAs of N=128: a barrier read
+//              stalls the issuing thread longer than a small MMA takes, so long groups of
+//              wide MMAs keep the tensor pipe fed.
+//   warp 2     TMA producer for V: the same tiling, its own 3-stage ring, freed by P.V
+//   warps 3-6  softmax, one score row per thread, 128 scores per tile: causal mask by
+//              true position (boundary tiles only), online softmax in the exp2 domain with
+//              the scale folded into one FFMA, P stored to TMEM as packed bf16 pairs, O
+//              rescaled in TMEM only when a row max grows by more than 2^8.  S is double
+//              buffered, so the scores of tile i+1 are ready while P.V of tile i runs.
 // Group g's barrier go[g % 8] completes when: K_{g+2} has landed (or there is none), V_g
-// has landed, and the four warps of stream g % 2 have read S_g and written P_g.
-// Q and P live in TMEM rather than shared memory: every Q.K^T would otherwise re-read
-// the 4 KB Q slice from shared memory, and shared-memory bandwidth (operand reads plus
-// the TMA writes of K and V) is what bounds these small MMAs.
-// TMEM columns: S_s at [64 s, 64 s + 64); O_s at [128 + 128 s, 256 + 128 s);
-// Q at [384, 448) (128 bf16 per row in 64 columns); P_s at [448 + 32 s, 480 + 32 s).
-constexpr int kTcKeys = 64;
-constexpr int kTcStages = 4;
+// has landed, and the four softmax warps have read S_g and written P_g.
+// Q and P live in TMEM: each Q.K^T would otherwise re-read the Q slice from shared
+// memory, whose bandwidth the operand reads and the TMA writes of K and V already share.
+// TMEM columns: S_b at [128 b, 128 b + 128); O at [256, 384); Q at [384, 448) (128 bf16
+// per row in 64 columns); P at [448, 512) (128 bf16 keys in 64 columns).
+constexpr int kTcKeys = 128;
+constexpr int kTcStages = 3;
 constexpr int kTcGo = 8;                       // group barriers in flight
-constexpr int kTcThreads = 352;
-constexpr int kTcKVBytes = kTcKeys * 128 * 2;  // one K or V tile: 2 boxes of 64 keys x 64 columns
-constexpr int kTcMlBytes = 2 * 128 * 8;        // per-stream (m, l) of every row, for the merge
-constexpr int kTcSmem = 2 * kTcStages * kTcKVBytes + kTcMlBytes + 256 + 1024;
+constexpr int kTcThreads = 224;
+constexpr int kTcKVBytes = kTcKeys * 128 * 2;  // one K or V tile: 2 boxes of 128 keys x 64 columns
+constexpr int kTcBoxBytes = kTcKeys * 128;     // one 64-column box
+constexpr int kTcSmem = 2 * kTcStages * kTcKVBytes + 256 + 1024;
+constexpr uint32_t kTcOCol = 256;              // first TMEM column of O
 constexpr uint32_t kTcQCol = 384;              // first TMEM column of Q
-constexpr uint32_t kTcPCol = 448;              // first TMEM column of the P buffers
+constexpr uint32_t kTcPCol = 448;              // first TMEM column of P
 constexpr uint32_t kTcGoCount = 10;            // K producer + V producer + 4 (S read) + 4 (P written)
-
-// Barrier 1 over the 256 softmax threads (barrier 0 is __syncthreads).
-__device__ __forceinline__ void softmax_threads_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -337,7 +330,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           float* __restrict__ lse, int split_tiles, int max_splits, float* __restrict__ part_o,
                           float2* __restrict__ part_ml, unsigned int* status, int check) {
   constexpr int D = 128;
-  constexpr unsigned kAll = 0xffffffffu;
   pdl_wait();  // q, pos and the cache come from the kernels before this one
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -345,14 +337,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* kbuf = smem;  // stage st at st * KV
   uint8_t* vbuf = kbuf + kTcStages * kTcKVBytes;
-  float2* ml_x = reinterpret_cast<float2*>(vbuf + kTcStages * kTcKVBytes);  // [stream][row]
-  uint64_t* go = reinterpret_cast<uint64_t*>(vbuf + kTcStages * kTcKVBytes + kTcMlBytes);
-  uint64_t* k_init = go + kTcGo;          // K_0 and K_1, read by S_0 and S_1
+  uint64_t* go = reinterpret_cast<uint64_t*>(vbuf + kTcStages * kTcKVBytes);
+  uint64_t* k_init = go + kTcGo;  // K_0 and K_1, read by S_0 and S_1
   uint64_t* k_empty = k_init + 2;
   uint64_t* v_empty = k_empty + kTcStages;
-  uint64_t* s_full = v_empty + kTcStages;  // [stream]
-  uint64_t* pv_done = s_full + 2;          // [stream]
-  uint64_t* q_ready = pv_done + 2;
+  uint64_t* s_full = v_empty + kTcStages;  // [S buffer]
+  uint64_t* pv_done = s_full + 2;
+  uint64_t* q_ready = pv_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -374,13 +365,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&k_init[b], 1);
       mbar_init(&s_full[b], 1);
-      mbar_init(&pv_done[b], 1);
     }
     for (int st = 0; st < kTcStages; ++st) {
       mbar_init(&k_empty[st], 1);
       mbar_init(&v_empty[st], 1);
     }
-    mbar_init(q_ready, 8);
+    mbar_init(pv_done, 1);
+    mbar_init(q_ready, 4);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -413,7 +404,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t* dst = ring + st * kTcKVBytes;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2)
-          tma_load_2d(dst + h2 * (kTcKeys * 128), map, bar, g * D + h2 * 64, (t_begin + i) * kTcKeys);
+          tma_load_2d(dst + h2 * kTcBoxBytes, map, bar, g * D + h2 * 64, (t_begin + i) * kTcKeys);
       }
       // the last two groups have no K tile to wait for: their K share of the count arrives now
       if (is_k && ok)
@@ -425,15 +416,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTcKeys, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       auto issue_s = [&](int i) {  // S_{i % 2} = Q K_i^T, Q from TMEM
-        const int st = i % kTcStages, s = i & 1;
+        const int st = i % kTcStages, b = i & 1;
         const uint32_t k_addr = smem_u32(kbuf + st * kTcKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_k = (kk >> 2) * (kTcKeys * 128) + (kk & 3) * 32;
-          umma_f16_ts(tmem_base + s * kTcKeys, tmem_base + kTcQCol + kk * 8, sdesc_kmajor_sw128(k_addr + off_k), idesc_s,
-                      kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[s]);
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_f16_ts(tmem_base + b * kTcKeys, tmem_base + kTcQCol + kk * 8,
+                      sdesc_kmajor_sw128(k_addr + (kk >> 2) * kTcBoxBytes + (kk & 3) * 32), idesc_s, kk > 0 ? 1u : 0u);
+        umma_commit(&s_full[b]);
         umma_commit(&k_empty[st]);
       };
       bool ok = mbar_wait(q_ready, 0) && mbar_wait(&k_init[0], 0);
@@ -453,22 +442,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         if (gi + 2 < nt) issue_s(gi + 2);
-        // O_s += P_gi V_gi
-        const int st = gi % kTcStages, s = gi & 1;
-        const uint32_t p_tm = tmem_base + kTcPCol + s * 32;
+        // O += P_gi V_gi
+        const int st = gi % kTcStages;
         const uint32_t v_addr = smem_u32(vbuf + st * kTcKVBytes);
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk)
-          umma_f16_ts(tmem_base + 128 + s * 128, p_tm + kk * 8, sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcKeys * 128),
-                      idesc_o, (gi >= 2 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[s]);
+          umma_f16_ts(tmem_base + kTcOCol, tmem_base + kTcPCol + kk * 8,
+                      sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcBoxBytes), idesc_o, (gi > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(pv_done);
         umma_commit(&v_empty[st]);
       }
       if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
     }
   } else {
-    // ---- softmax streams: thread = score row
-    const int sidx = (warp - 3) >> 2;
+    // ---- softmax: thread = score row
+    constexpr unsigned kAll = 0xffffffffu;
     const int quarter = warp & 3;
     const int rho = quarter * 32 + lane;
     const int p_local = rho / G, hh = rho - p_local * G;
@@ -476,51 +464,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool valid = p_local < BRp && r < row_end;
     const int prow = valid ? pos[r] : -1;
     const int h = g * G + hh;
-    if (check && sidx == 0 && valid && (prow < 0 || prow >= T || (r > 0 && pos[r - 1] >= prow)))
-      flag_status(status, QCF_DEV_BAD_INDEX);
+    if (check && valid && (prow < 0 || prow >= T || (r > 0 && pos[r - 1] >= prow))) flag_status(status, QCF_DEV_BAD_INDEX);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    {  // stream s stores Q columns [64 s, 64 s + 64) of its row into TMEM as 32 packed bf16 pairs
-      const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(valid ? r : 0) * Hq + h) * D) + sidx * 8;
-      uint32_t w[32];
+    {  // the Q row into TMEM as 64 packed bf16 pairs
+      const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(valid ? r : 0) * Hq + h) * D);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-        w[4 * ch] = v.x;
-        w[4 * ch + 1] = v.y;
-        w[4 * ch + 2] = v.z;
-        w[4 * ch + 3] = v.w;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = valid ? src[half * 8 + ch] : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * ch] = v.x;
+          w[4 * ch + 1] = v.y;
+          w[4 * ch + 2] = v.z;
+          w[4 * ch + 3] = v.w;
+        }
+        tmem_st32u(tmem_base + lane_base + kTcQCol + half * 32, w);
       }
-      tmem_st32u(tmem_base + lane_base + kTcQCol + sidx * 32, w);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
-    const uint32_t s_tm = tmem_base + lane_base + sidx * kTcKeys;
-    const uint32_t o_tm = tmem_base + lane_base + 128 + sidx * 128;
+    const uint32_t o_tm = tmem_base + lane_base + kTcOCol;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    int k = 0;  // tiles this stream has finished
-    for (int i = sidx; i < nt; i += 2, ++k) {
+    for (int i = 0; i < nt; ++i) {
       uint64_t* gob = &go[i % kTcGo];
-      if (!__all_sync(kAll, mbar_wait(&s_full[sidx], k & 1))) {
+      const int b = i & 1;
+      if (!__all_sync(kAll, mbar_wait(&s_full[b], (i >> 1) & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float sv[64];
-      tmem_ld64(s_tm, sv);
+      float sv[kTcKeys];
+      tmem_ld64(tmem_base + lane_base + b * kTcKeys, sv);
+      tmem_ld64(tmem_base + lane_base + b * kTcKeys + 64, sv + 64);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(gob);  // S_i read: its buffer may take S_{i+2}
       const int j0 = (t_begin + i) * kTcKeys;
       if (j0 + kTcKeys - 1 > prow) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
+        for (int j = 0; j < kTcKeys; ++j)
           if (j0 + j > prow) sv[j] = -INFINITY;
       }
       float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-      for (int j = 4; j < 64; j += 4) {
+      for (int j = 4; j < kTcKeys; j += 4) {
         mx0 = fmaxf(mx0, sv[j]);
         mx1 = fmaxf(mx1, sv[j + 1]);
         mx2 = fmaxf(mx2, sv[j + 2]);
@@ -531,8 +521,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool grow = tmax > m + 8.0f;
       if (__any_sync(kAll, grow)) {
         const float m_new = grow ? tmax : m;
-        if (k > 0) {  // O_s holds this stream's tiles so far: wait for the last P.V, then scale
-          if (!__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) {
+        if (i > 0) {  // O holds the tiles so far: wait for the last P.V, then scale
+          if (!__all_sync(kAll, mbar_wait(pv_done, (i - 1) & 1))) {
             ok = false;
             break;
           }
@@ -550,16 +540,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         m = m_new;
       }
-      // the P buffer was last read by the P.V of this stream's previous tile
-      if (k >= 1 && !__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) {
-        ok = false;
-        break;
-      }
       const float nm = (m == -INFINITY) ? 0.f : -m;  // m = -inf only when every key so far is masked
       float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
-      uint32_t pk[32];
+      uint32_t pk[64];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
+      for (int e = 0; e < 64; e += 2) {
         const float p0 = fast_exp2(fmaf(sv[2 * e], scale_log2, nm));
         const float p1 = fast_exp2(fmaf(sv[2 * e + 1], scale_log2, nm));
         const float p2 = fast_exp2(fmaf(sv[2 * e + 2], scale_log2, nm));
@@ -572,56 +557,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         pk[e + 1] = pack_bf16x2(p2, p3);
       }
       l += (rs0 + rs1) + (rs2 + rs3);
-      tmem_st32u(tmem_base + lane_base + kTcPCol + sidx * 32, pk);
+      // the P buffer was last read by the previous tile's P.V
+      if (i > 0 && !__all_sync(kAll, mbar_wait(pv_done, (i - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32u(tmem_base + lane_base + kTcPCol, pk);
+      tmem_st32u(tmem_base + lane_base + kTcPCol + 32, pk + 32);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(gob);  // P_i written
     }
-    if (ok && k > 0 && !__all_sync(kAll, mbar_wait(&pv_done[sidx], (k - 1) & 1))) ok = false;
-    if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
-    // ---- merge the two streams; stream s writes output columns [64 s, 64 s + 64)
-    ml_x[sidx * 128 + rho] = ok ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
-    softmax_threads_sync();
-    tc_fence_after();
-    const float2 a0 = ml_x[rho], a1 = ml_x[128 + rho];
-    const float M = fmaxf(a0.x, a1.x);
-    const float f0 = a0.x == -INFINITY ? 0.f : fast_exp2(a0.x - M);
-    const float f1 = a1.x == -INFINITY ? 0.f : fast_exp2(a1.x - M);
-    const float L = a0.y * f0 + a1.y * f1;
-    if (ok) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
+    if (ok && !__all_sync(kAll, mbar_wait(pv_done, (nt - 1) & 1))) ok = false;
+    if (!ok) {
+      flag_status(status, QCF_DEV_TIMEOUT);
+    } else {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
       const size_t pstride = static_cast<size_t>(n) * Hq;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c0 = sidx * 64 + cc * 32;
-        float o0[32], o1[32];
-        tmem_ld32(tmem_base + lane_base + 128 + c0, o0);
-        tmem_ld32(tmem_base + lane_base + 256 + c0, o1);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o0[e] = (f0 != 0.f ? o0[e] * f0 : 0.f) + (f1 != 0.f ? o1[e] * f1 : 0.f);
+      for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tmem_ld32(o_tm + c * 32, ov);
         if (!valid) continue;
         if (n_split > 1) {
-          float* po = part_o + (static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h) * D + c0;
+          float* po = part_o + (static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h) * D + c * 32;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(po + e) = make_float4(o0[e], o0[e + 1], o0[e + 2], o0[e + 3]);
+          for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(po + e) = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
         } else {
-          __nv_bfloat16* op = o + (static_cast<size_t>(r) * Hq + h) * D + c0;
+          __nv_bfloat16* op = o + (static_cast<size_t>(r) * Hq + h) * D + c * 32;
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 u;
-            u.x = pack_bf16x2(o0[e] * inv, o0[e + 1] * inv);
-            u.y = pack_bf16x2(o0[e + 2] * inv, o0[e + 3] * inv);
-            u.z = pack_bf16x2(o0[e + 4] * inv, o0[e + 5] * inv);
-            u.w = pack_bf16x2(o0[e + 6] * inv, o0[e + 7] * inv);
+            u.x = pack_bf16x2(ov[e] * inv, ov[e + 1] * inv);
+            u.y = pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv);
+            u.z = pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv);
+            u.w = pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv);
             *reinterpret_cast<uint4*>(op + e) = u;
           }
         }
       }
-      if (valid && sidx == 0) {
+      if (valid) {
         if (n_split > 1)
-          part_ml[static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h] = make_float2(M, L);
+          part_ml[static_cast<size_t>(sp) * pstride + static_cast<size_t>(r) * Hq + h] = make_float2(m, l);
         else if (lse)
-          lse[static_cast<size_t>(r) * Hq + h] = (M + log2f(L)) * 0.69314718055994531f;
+          lse[static_cast<size_t>(r) * Hq + h] = (m + log2f(l)) * 0.69314718055994531f;
       }
     }
   }
@@ -636,7 +617,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Merges the key-range partials of rows whose block was split: one warp per
 // (row, head), splits summed in order (deterministic).
 template <int D>
-__global__ void attn_combine_kernel(const int32_t* __restrict__ pos, int n, int Hq, int BR, int split_tiles,
+__global__ void attn_combine_kernel(const int32_t* __restrict__ pos, int n, int Hq, int BR, int tile, int split_tiles,
                                     int max_splits, const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
   pdl_wait();
@@ -647,7 +628,7 @@ __global__ void attn_combine_kernel(const int32_t* __restrict__ pos, int n, int 
   const int row = w / Hq, h = w - row * Hq;
   const int rb = row / BR;
   const int row_end = min(n, rb * BR + BR);
-  const int n_tiles_all = pos[row_end - 1] / kKeyTile + 1;
+  const int n_tiles_all = pos[row_end - 1] / tile + 1;
   const int n_split = min(max_splits, (n_tiles_all + split_tiles - 1) / split_tiles);
   if (n_split <= 1) return;
   const size_t pstride = static_cast<size_t>(n) * Hq;
@@ -677,7 +658,7 @@ __global__ void attn_combine_kernel(const int32_t* __restrict__ pos, int n, int 
 }
 
 struct AttnPlan {
-  int G, BR, n_blocks, split_tiles, max_splits;
+  int G, BR, tile, n_blocks, split_tiles, max_splits;   // tile: keys per pipeline step
 };
 
 // Long row blocks are split over key ranges only when the grid is too small to
@@ -688,7 +669,8 @@ static AttnPlan plan_attn(int n, int T, int Hq, int Hkv, int D) {
   // rows per CTA: the tensor-core kernel (D = 128) fills 128 score rows, the warp-MMA kernel 16 per warp
   p.BR = D == 128 ? 128 / p.G : 16 * (p.G >= 8 ? 1 : 8 / p.G);
   p.n_blocks = (n + p.BR - 1) / p.BR;
-  const int max_tiles = (T + kKeyTile - 1) / kKeyTile;
+  p.tile = D == 128 ? kTcKeys : kKeyTile;
+  const int max_tiles = (T + p.tile - 1) / p.tile;
   p.split_tiles = max_tiles;
   p.max_splits = 1;
   const int ctas = p.n_blocks * Hkv, sms = num_sms();
@@ -696,10 +678,10 @@ static AttnPlan plan_attn(int n, int T, int Hq, int Hkv, int D) {
     // tensor-core kernel, one CTA per SM: a CTA's set-up and drain cost more than the
     // imbalance of unsplit rows once every SM has a CTA (8B recompute shape: 81 us
     // unsplit vs 99 us with 4 splits plus the combine), so split only a grid smaller
-    // than the SM count, into at most 4 ranges of at least 16 tiles
-    if (ctas < sms && max_tiles > 16) {
+    // than the SM count, into at most 4 ranges of at least 8 tiles of 128 keys
+    if (ctas < sms && max_tiles > 8) {
       p.max_splits = std::min(4, (sms + ctas - 1) / ctas);
-      p.split_tiles = std::max(16, (max_tiles + p.max_splits - 1) / p.max_splits);
+      p.split_tiles = std::max(8, (max_tiles + p.max_splits - 1) / p.max_splits);
       p.max_splits = (max_tiles + p.split_tiles - 1) / p.split_tiles;
     }
   } else if (ctas < 4 * sms && max_tiles > 16) {
@@ -742,8 +724,8 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
   const uint64_t width = static_cast<uint64_t>(Hkv) * D;
   const uint32_t box_cols = D >= 64 ? 64 : D;
   const CUtensorMapSwizzle sw = Cfg::SW128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  if (!encode_tmap_2d(&tk, K, width, T, width * 2, box_cols, kKeyTile, sw) ||
-      !encode_tmap_2d(&tv, V, width, T, width * 2, box_cols, kKeyTile, sw))
+  if (!encode_tmap_2d(&tk, K, width, T, width * 2, box_cols, plan.tile, sw) ||
+      !encode_tmap_2d(&tv, V, width, T, width * 2, box_cols, plan.tile, sw))
     return set_error(QCF_ERR_CUDA, "sparse_causal_attn: tensor map encoding failed");
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
@@ -782,11 +764,11 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
     const int warps_total = n * Hq;
     if (pdl) {
       cudaError_t e = launch_pdl(attn_combine_kernel<D>, dim3((warps_total + 7) / 8), dim3(256), 0, st, pos, n, Hq, BR,
-                                 plan.split_tiles, plan.max_splits, part_o, part_ml, o, lse);
+                                 plan.tile, plan.split_tiles, plan.max_splits, part_o, part_ml, o, lse);
       if (e != cudaSuccess) return cuda_error(e, "sparse_causal_attn: combine launch");
     } else {
-      attn_combine_kernel<D><<<(warps_total + 7) / 8, 256, 0, st>>>(pos, n, Hq, BR, plan.split_tiles, plan.max_splits,
-                                                                    part_o, part_ml, o, lse);
+      attn_combine_kernel<D><<<(warps_total + 7) / 8, 256, 0, st>>>(pos, n, Hq, BR, plan.tile, plan.split_tiles,
+                                                                    plan.max_splits, part_o, part_ml, o, lse);
     }
   }
   cudaError_t e = cudaGetLastError();
