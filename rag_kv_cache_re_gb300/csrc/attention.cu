@@ -292,9 +292,9 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
 //   warp 0     TMA producer for K: tiles of 128 keys (two 64-column boxes, 128B swizzle)
 //              into a 3-stage ring; a stage is freed by the Q.K^T that read it
 //   warp 1     TMEM allocation; one thread issues the tensor-core work in groups:
-//              group g = { S_{g+2} = Q K_{g+2}^T  (M=128, N=128, K=128; Q read from TMEM),
-//                          O += P_g V_g          (M=128, N=128, K=128 keys; P read from TMEM,
-//                                                 V MN-major from shared memory) },
+//              group g = { O += P_g V_g          (M=128, N=128, K=128 keys; P read from TMEM,
+//                                                 V MN-major from shared memory),
+//                          S_{g+2} = Q K_{g+2}^T  (M=128, N=128, K=128; Q read from TMEM) },
 //              after S_0 and S_1.  Every dependency of group g lands on one mbarrier, so
 //              the issuing thread reads one barrier per 16 MMAs of N=128: a barrier read
 //              stalls the issuing thread longer than a small MMA takes, so long groups of
@@ -441,8 +441,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        if (gi + 2 < nt) issue_s(gi + 2);
-        // O += P_gi V_gi
+        // O += P_gi V_gi first: the single P buffer is free again as soon as it completes,
+        // while S_{gi+2} is needed only after the softmax of tile gi+1
         const int st = gi % kTcStages;
         const uint32_t v_addr = smem_u32(vbuf + st * kTcKVBytes);
 #pragma unroll
@@ -451,6 +451,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       sdesc_mnmajor_sw128(v_addr + kk * 2048, kTcBoxBytes), idesc_o, (gi > 0 || kk > 0) ? 1u : 0u);
         umma_commit(pv_done);
         umma_commit(&v_empty[st]);
+        if (gi + 2 < nt) issue_s(gi + 2);
       }
       if (!ok) flag_status(status, QCF_DEV_TIMEOUT);
     }
