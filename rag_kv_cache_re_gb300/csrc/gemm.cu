@@ -37,6 +37,11 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = 2 * BN;
+  // the last unit's residual tile, staged in the (then idle) pipeline stages: 128 rows
+  // of BN floats, each row padded by 16 bytes so row-per-thread float4 reads spread
+  // over all banks
+  static constexpr int X_STRIDE = BN + 4;
+  static_assert(kBM * X_STRIDE * 4 <= STAGES * STAGE_BYTES, "residual tile must fit the stages");
   static constexpr int EPI_BYTES = 4 * 32 * 33 * 4;   // one 32x32 fp32 transpose tile per epilogue warp
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
 };
@@ -78,8 +83,9 @@ __device__ __forceinline__ size_t part_idx(int row, int quad) {
 struct ChunkLoader {
   uint32_t taddr;       // TMEM address of (row quarter, column 0) of the accumulator
   const float* part;    // the tile's first partial slot, or nullptr for TMEM
-  int splits;
-  int part_stride;      // floats between consecutive splits' slots
+  const float* rest;    // its second partial slot; the later ones follow at part_stride
+  int splits;           // partial slots to sum
+  size_t part_stride;   // floats between consecutive slots after the first
   int row;              // row within the tile
   __device__ __forceinline__ void operator()(int c, float* v) const {
     if (part == nullptr) {
@@ -91,7 +97,7 @@ struct ChunkLoader {
         v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
       }
       for (int s = 1; s < splits; ++s) {
-        const float* p = part + static_cast<size_t>(s) * part_stride;
+        const float* p = rest + static_cast<size_t>(s - 1) * part_stride;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float4 t = __ldcg(reinterpret_cast<const float4*>(p + part_idx(row, c * 8 + q)));
@@ -293,10 +299,136 @@ __device__ __forceinline__ void tile_epilogue(const ChunkLoader& ld, const EpiPa
   }
 }
 
+// Residual add of one warp's 32 rows from a tile staged in shared memory: each lane
+// bulk-copies its row's BN floats of x into its padded smem row, adds its TMEM
+// accumulator row in place, and bulk-stores the row back.  All copies of the warp
+// complete on bar (one use per launch).  Rows >= M are skipped.
+template <int BN>
+__device__ __forceinline__ void add_epilogue_staged(uint32_t taddr, float* xs_warp, uint64_t* bar, float* x,
+                                                    int ldo, int row, int M, int n0, unsigned int* status) {
+  constexpr int kStride = BN + 4;
+  constexpr uint32_t kRowBytes = BN * 4;
+  const int lane = threadIdx.x & 31;
+  const bool live = row < M;
+  const unsigned nlive = __popc(__ballot_sync(0xffffffffu, live));
+  float* xs = xs_warp + lane * kStride;
+  float* xg = x + static_cast<size_t>(live ? row : 0) * ldo + n0;
+  if (lane == 0) mbar_arrive_expect_tx(bar, nlive * kRowBytes);
+  __syncwarp();
+  if (live) bulk_load_g2s(xs, xg, kRowBytes, bar);
+  if (!mbar_wait(bar, 0)) {
+    flag_status(status, QCF_DEV_TIMEOUT);
+    mbar_wait(bar, 0);  // once more, bounded, so no copy is left landing in smem
+    return;
+  }
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
+    float4* p = reinterpret_cast<float4*>(xs + c * 32);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4 t = p[q];
+      t.x += v[4 * q]; t.y += v[4 * q + 1]; t.z += v[4 * q + 2]; t.w += v[4 * q + 3];
+      p[q] = t;
+    }
+  }
+  fence_proxy_async_smem();  // the generic-proxy writes above, before the bulk store reads them
+  if (live) {
+    bulk_store_s2g(xg, xs, kRowBytes);
+    bulk_commit_group();
+    bulk_wait_group0();
+  }
+  __syncwarp();
+}
+
+// One work unit: k blocks [kb0, kb1) of output tile (mt, nt).  A tile whose k range
+// is shared by several units (parts > 1) is finished by whichever arrives last: each
+// writes its fp32 partial and bumps the tile's counter, and the last one sums the
+// partials in order and runs the epilogue (no unit ever waits for another).  Partial
+// slots are numbered in units of one slot (128 or 256 rows x BN floats).
+struct Unit {
+  int mt, nt, kb0, kb1;
+  int parts;   // units sharing the tile (1: this unit has the whole k range)
+  int cnt;     // arrival counter of the tile
+  int mine;    // this unit's partial slot
+  int first;   // the tile's first partial slot ...
+  int rest;    // ... its second; later ones follow every `step` slots
+  int step;
+};
+
+// The units one CTA works through, in order.  Two schedules:
+//  * lockstep (groups == 0): unit u = blockIdx.x + i * gridDim.x over tiles x splits,
+//    m tile fastest, so the CTAs running together share each weight tile's k walk;
+//  * grouped stream-K (groups > 0): CTA b computes m tile b % tiles_m for group
+//    b / tiles_m, and group g owns iterations [g I / G, (g + 1) I / G) of the
+//    (n tile, k block) space (I = tiles_n x kb_total, G groups).  The tiles_m CTAs of
+//    a group walk the same weight blocks side by side (one HBM read of each serves
+//    all m tiles), and every CTA gets the same number of k blocks whatever the tile
+//    count, so no last round runs part-empty.  A column cut by a group boundary is
+//    shared: a group's piece of it is its first (slot 0) or last (slot 1) piece.
+// The host keeps I x G below 2^31.
+struct UnitWalk {
+  int tiles_m, kb_total, splits, units, groups;
+  int u, mt, g, total, x, xend;
+
+  __device__ void init(int tm, int tn, int kbt, int sp, int gr) {
+    tiles_m = tm; kb_total = kbt; splits = sp; groups = gr;
+    units = tm * tn * sp;
+    u = blockIdx.x;
+    mt = static_cast<int>(blockIdx.x) % tm;
+    g = static_cast<int>(blockIdx.x) / tm;
+    total = tn * kbt;
+    x = gr > 0 ? start_of(g) : 0;
+    xend = gr > 0 ? start_of(g + 1) : 0;
+  }
+  __device__ int start_of(int grp) const { return grp * total / groups; }
+  // the group whose range holds iteration it: the largest grp with start_of(grp) <= it
+  __device__ int owner(int it) const { return ((it + 1) * groups + total - 1) / total - 1; }
+  __device__ int slot(int grp, int which) const { return (grp * tiles_m + mt) * 2 + which; }
+
+  __device__ bool next(Unit& w) {
+    if (groups == 0) {
+      if (u >= units) return false;
+      w.mt = u % tiles_m;
+      const int r = u / tiles_m;
+      const int sp = r % splits;
+      w.nt = r / splits;
+      w.kb0 = static_cast<int>(static_cast<long long>(kb_total) * sp / splits);
+      w.kb1 = static_cast<int>(static_cast<long long>(kb_total) * (sp + 1) / splits);
+      w.parts = splits;
+      w.cnt = w.nt * tiles_m + w.mt;
+      w.first = w.cnt * splits;
+      w.mine = w.first + sp;
+      w.rest = w.first + 1;
+      w.step = 1;
+      u += gridDim.x;
+      return true;
+    }
+    if (x >= xend) return false;
+    const int nt = x / kb_total;
+    const int c0 = nt * kb_total;
+    const int lim = xend < c0 + kb_total ? xend : c0 + kb_total;
+    w.mt = mt;
+    w.nt = nt;
+    w.kb0 = x - c0;
+    w.kb1 = lim - c0;
+    const int fg = owner(c0), lg = owner(c0 + kb_total - 1);
+    w.parts = lg - fg + 1;
+    w.cnt = nt * tiles_m + mt;
+    w.mine = slot(g, start_of(g) >= c0 ? 0 : 1);
+    w.first = slot(fg, start_of(fg) >= c0 ? 0 : 1);
+    w.rest = slot(fg + 1, 0);  // later contributors start inside the column: their slot 0
+    w.step = 2 * tiles_m;
+    x = lim;
+    return true;
+  }
+};
+
 template <int BN, int EPI, int HD, bool BMN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
-                        int N, int K, int splits, const EpiParams ep, float* __restrict__ ws_part,
+                        int N, int K, int splits, int groups, const EpiParams ep, float* __restrict__ ws_part,
                         unsigned int* __restrict__ ws_cnt, unsigned int* status) {
   using Cfg = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -306,7 +438,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* empty = full + Cfg::STAGES;
   uint64_t* tfull = empty + Cfg::STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* xbar = tempty + 2;  // one per epilogue warp: its staged residual rows landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* epi_tiles = reinterpret_cast<float*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES + 1024);
 
@@ -314,7 +447,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tiles_m = (M + kBM - 1) / kBM;
   const int tiles_n = N / BN;
   const int kb_total = K / kBK;
-  const int units = tiles_m * tiles_n * splits;
+  UnitWalk walk;
+  walk.init(tiles_m, tiles_n, kb_total, splits, groups);
+  constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;  // floats of one partial slot
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -325,6 +460,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 4);
     }
+    for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -335,13 +471,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-
-  auto decode = [&](int u, int& mt, int& nt, int& sp) {
-    mt = u % tiles_m;
-    const int r = u / tiles_m;
-    sp = r % splits;
-    nt = r / splits;
-  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -360,15 +489,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // so the first unit's weight stages are requested before waiting for them;
       // the activation half of each of those stages follows the wait.
       int npre = 0;
-      if (static_cast<int>(blockIdx.x) < units) {
-        int mt, nt, sp;
-        decode(blockIdx.x, mt, nt, sp);
-        const int kb0 = static_cast<int>(static_cast<long long>(kb_total) * sp / splits);
-        const int kb1 = static_cast<int>(static_cast<long long>(kb_total) * (sp + 1) / splits);
-        npre = min(Cfg::STAGES, kb1 - kb0);
-        for (int j = 0; j < npre; ++j) {
-          mbar_arrive_expect_tx(&full[j], Cfg::STAGE_BYTES);
-          load_w(smem + j * Cfg::STAGE_BYTES, kb0 + j, nt, &full[j]);
+      {
+        UnitWalk peek = walk;
+        Unit w0;
+        if (peek.next(w0)) {
+          npre = min(Cfg::STAGES, w0.kb1 - w0.kb0);
+          for (int j = 0; j < npre; ++j) {
+            mbar_arrive_expect_tx(&full[j], Cfg::STAGE_BYTES);
+            load_w(smem + j * Cfg::STAGE_BYTES, w0.kb0 + j, w0.nt, &full[j]);
+          }
         }
       }
       pdl_wait();
@@ -377,12 +506,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int issued = 0;  // k blocks loaded so far; the first npre had their weights requested above
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        int mt, nt, sp;
-        decode(u, mt, nt, sp);
-        const int kb0 = static_cast<int>(static_cast<long long>(kb_total) * sp / splits);
-        const int kb1 = static_cast<int>(static_cast<long long>(kb_total) * (sp + 1) / splits);
-        for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+      Unit w;
+      while (ok && walk.next(w)) {
+        const int mt = w.mt, nt = w.nt;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++issued) {
           uint8_t* a_s = smem + stage * Cfg::STAGE_BYTES;
           if (issued >= npre) {
             if (!mbar_wait(&empty[stage], phase ^ 1u)) {
@@ -406,13 +533,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, BMN);
       int stage = 0;
       uint32_t phase = 0;
-      int local = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
-        int mt, nt, sp;
-        decode(u, mt, nt, sp);
-        const int kb0 = static_cast<int>(static_cast<long long>(kb_total) * sp / splits);
-        const int kb1 = static_cast<int>(static_cast<long long>(kb_total) * (sp + 1) / splits);
+      Unit w;
+      for (int local = 0; ok && walk.next(w); ++local) {
+        const int kb0 = w.kb0, kb1 = w.kb1;
         const int acc = local & 1;
         if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1u)) {
           flag_status(status, QCF_DEV_TIMEOUT);
@@ -453,15 +577,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     float* my_tile = epi_tiles + (warp - 2) * (32 * 33);
     pdl_wait();  // the residual, position tables and output buffers come from earlier kernels
     pdl_launch_dependents();
-    int local = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
-      int mt, nt, sp;
-      decode(u, mt, nt, sp);
+    // shared tiles go through epilogue-wide barriers: with any, abort only together
+    const bool shared_tiles = splits > 1 || groups > 0;
+    Unit w;
+    for (int local = 0; walk.next(w); ++local) {
+      const int mt = w.mt, nt = w.nt;
       const int acc = local & 1;
       const bool got = mbar_wait(&tfull[acc], (local >> 1) & 1);
       if (!got) flag_status(status, QCF_DEV_TIMEOUT);
-      if (splits > 1) {
-        // the split-K path has epilogue-wide barriers: abort only together
+      if (shared_tiles) {
         if (epi_bar_or(!got)) break;
       } else if (!got) {
         break;
@@ -470,16 +594,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
       const int row = mt * kBM + row_in_tile;
       const int n0 = nt * BN;
-      if (splits == 1) {
-        ChunkLoader ld{taddr, nullptr, 1, 0, row_in_tile};
+      bool staged = false;
+      if constexpr (EPI == EPI_ADD_F32) {
+        // On the CTA's last unit no stage will be loaded again and the MMAs that read
+        // them have completed (tfull), so the residual tile is staged there with one
+        // bulk copy per row: one load latency instead of one per 32-column chunk.
+        UnitWalk peek = walk;
+        Unit nx;
+        staged = w.parts == 1 && !peek.next(nx);
+      }
+      if (staged) {
+        add_epilogue_staged<BN>(taddr, reinterpret_cast<float*>(smem) + static_cast<size_t>(quarter) * 32 * Cfg::X_STRIDE,
+                                &xbar[quarter], static_cast<float*>(ep.out), ep.ldo, row, M, n0, status);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else if (w.parts == 1) {
+        ChunkLoader ld{taddr, nullptr, nullptr, 1, 0, row_in_tile};
         tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
       } else {
-        const int tile = nt * tiles_m + mt;
-        const int stride = kBM * BN;
-        float* mine = ws_part + (static_cast<size_t>(tile) * splits + sp) * stride;
+        float* mine = ws_part + static_cast<size_t>(w.mine) * kSlot;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
@@ -495,9 +632,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __threadfence();
         epi_bar();
         if (threadIdx.x == 64) {
-          const unsigned int prev = atomicAdd(&ws_cnt[tile], 1u);
-          const int last = prev == static_cast<unsigned int>(splits - 1);
-          if (last) ws_cnt[tile] = 0u;
+          const unsigned int prev = atomicAdd(&ws_cnt[w.cnt], 1u);
+          const int last = prev == static_cast<unsigned int>(w.parts - 1);
+          if (last) ws_cnt[w.cnt] = 0u;  // back to zero for the next launch on this workspace
           *s_last = last;
         }
         epi_bar();
@@ -505,7 +642,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         epi_bar();
         if (last) {
           __threadfence();
-          ChunkLoader ld{0u, ws_part + static_cast<size_t>(tile) * splits * stride, splits, stride, row_in_tile};
+          ChunkLoader ld{0u, ws_part + static_cast<size_t>(w.first) * kSlot, ws_part + static_cast<size_t>(w.rest) * kSlot,
+                         w.parts, w.step * kSlot, row_in_tile};
           tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
         }
       }
@@ -525,12 +663,29 @@ struct GemmPlan {
   int BN;
   int splits;
   int tiles;
+  int groups;  // > 0: grouped stream-K with this many groups of tiles_m CTAs
 };
 
-// Chooses the tile width BN and the number of k splits from measurements on GB300:
-//  * M > 128 (the recompute GEMMs): tensor-bound; the widest tile (BN = 256) and
-//    no k split were fastest on every 8B layer shape (splits write fp32 partials
-//    whose traffic and fixup cost more than the waves they fill).
+// Arrival counters sit at the front of the workspace, one per output tile, and every
+// launch leaves them zero; a plan that shares tiles needs tiles <= kCntCells.
+constexpr int kCntCells = 4096;
+constexpr size_t kCntBytes = kCntCells * sizeof(unsigned int);
+
+// Main-loop k blocks that a grouped stream-K CTA's shared-tile epilogues cost,
+// measured on GB300: about 10 for the partial write plus 8 per partial the last
+// arriver reads back (its fixup loads are latency-bound).
+constexpr int kSkFixupBase = 10;
+constexpr int kSkFixupPerPart = 8;
+
+// Chooses the tile width BN, the k split and the schedule from measurements on GB300:
+//  * M > 128 (the recompute GEMMs): the widest tile (BN = 256).  The lockstep grid
+//    runs ceil(tiles / SMs) rounds of a whole k range each; grouped stream-K gives
+//    every CTA (SMs / tiles_m groups of tiles_m CTAs) an equal share of the
+//    (n tile, k block) space instead.  Costs are counted in k blocks per CTA plus the
+//    fixup, and stream-K must win by 10 %: a last lockstep round that runs part-empty
+//    is cheaper than its share suggests, because the full rounds are slowed by the
+//    L2 bandwidth all SMs draw together (measured: 0.30 us per k block for a lone CTA,
+//    0.40 us with all 152 busy).
 //  * M <= 128 (the probe's query rows): weight-bound; one busy SM streams about
 //    45 GB/s of weights through the TMA ring, so time ~ rounds x bytes per unit /
 //    45 GB/s, plus ~10 us and the partial traffic when K is split.
@@ -546,20 +701,31 @@ static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
   };
   const int cands[3] = {256, 128, 64};
   if (tiles_m >= 2) {
-    // Widest tile, whole k range.  Measured on the 8B recompute shapes: uniform
-    // k splits (lockstep or stream-K) lost to the plain persistent grid because the
-    // split epilogue (fenced partial write, last-CTA fixup) outlasts a short k
-    // slice's main loop, and stream-K ranges break the m tiles' shared walk over
-    // a weight tile (L2 reuse).
-    for (int bn : cands)
-      if (valid(bn)) return GemmPlan{bn, 1, tiles_m * (N / bn)};
+    int bn = 64;
+    for (int c : cands)
+      if (valid(c)) {
+        bn = c;
+        break;
+      }
+    const int tiles = tiles_m * (N / bn);
+    const long long lockstep = static_cast<long long>((tiles + sms - 1) / sms) * kb;
+    const int groups = sms / tiles_m;
+    const long long iters = static_cast<long long>(N / bn) * kb;
+    if (groups >= 1 && tiles <= kCntCells && iters >= 4LL * groups && (iters + 1) * groups < (1LL << 31)) {
+      const long long per = iters / groups;                                   // k blocks per CTA
+      const long long parts = std::min<long long>(groups, (kb + per - 1) / per + 1);  // per shared tile, at most
+      const long long sk = per + 1 + kSkFixupBase + kSkFixupPerPart * parts;
+      if (sk * 10 < lockstep * 9) return GemmPlan{bn, 1, tiles, groups};
+    }
+    return GemmPlan{bn, 1, tiles, 0};
   }
-  GemmPlan best{64, 1, tiles_m * (N / 64)};
+  GemmPlan best{64, 1, tiles_m * (N / 64), 0};
   double best_t = 1e30;
   for (int bn : cands) {
     if (!valid(bn)) continue;
     const double stream = bn == 64 ? 28.0e9 : 45.0e9;   // bytes/s one SM pulls with this tile's ring
     const int tiles = tiles_m * (N / bn);
+    if (tiles > kCntCells) continue;
     for (int s = 1; s <= 8; ++s) {
       if (s > 1 && kb / s < 4) break;
       const int units = tiles * s;
@@ -570,11 +736,22 @@ static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
       if (s > 1) t += 10.0e-6 + units * (kBM * bn * 4.0 * 2.0) / 1.5e12;
       if (t < best_t * 0.98) {
         best_t = t;
-        best = GemmPlan{bn, s, tiles};
+        best = GemmPlan{bn, s, tiles, 0};
       }
     }
   }
   return best;
+}
+
+// fp32 partial slots a plan writes (after the counters); 0 when no tile is shared
+static size_t plan_part_bytes(const GemmPlan& p, int M) {
+  const size_t slot = static_cast<size_t>(kBM) * p.BN * sizeof(float);
+  if (p.groups > 0) {
+    const int tiles_m = (M + kBM - 1) / kBM;
+    return static_cast<size_t>(p.groups) * tiles_m * 2 * slot;
+  }
+  if (p.splits > 1) return static_cast<size_t>(p.tiles) * p.splits * slot;
+  return 0;
 }
 
 size_t gemm_workspace_size(int M, int N, int K) {
@@ -585,21 +762,23 @@ size_t gemm_workspace_size(int M, int N, int K) {
     for (int hd : {16, 64, 128}) {
       if (e != EPI_QKV_ROPE && hd != 16) continue;
       if (M <= 0 || N <= 0 || K <= 0 || N % 64 || K % 64) continue;
-      GemmPlan p = plan_gemm(M, N, K, e, hd);
-      if (p.splits > 1) {
-        const size_t b = align_up(static_cast<size_t>(p.tiles) * p.splits * kBM * p.BN * sizeof(float), 256) +
-                         align_up(static_cast<size_t>(p.tiles) * sizeof(unsigned int), 256);
-        need = b > need ? b : need;
-      }
+      const size_t b = plan_part_bytes(plan_gemm(M, N, K, e, hd), M);
+      need = b > need ? b : need;
     }
   }
-  return need + 256;
+  return kCntBytes + need + 256;
+}
+
+qcf_status gemm_ws_prepare(void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (!ws || ws_bytes < kCntBytes) return set_error(QCF_ERR_WORKSPACE, "gemm: workspace %zu < %zu", ws_bytes, kCntBytes);
+  const cudaError_t e = cudaMemsetAsync(ws, 0, kCntBytes, st);
+  return e == cudaSuccess ? QCF_OK : cuda_error(e, "gemm: counter reset");
 }
 
 template <int BN, int EPI, int HD, bool BMN = false>
 static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int splits,
-                             const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st, int units,
-                             bool pdl) {
+                             int groups, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
+                             int grid, bool pdl) {
   using Cfg = GemmCfg<BN>;
   auto kern = gemm_tcgen05_kernel<BN, EPI, HD, BMN>;
   static std::once_flag once;
@@ -608,13 +787,13 @@ static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "gemm: shared memory attribute");
-  const int grid = units < num_sms() ? units : num_sms();
   cudaError_t e = cudaSuccess;
   if (pdl) {
-    e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg::SMEM_BYTES, st, ta, tb, M, N, K, splits, ep, part, cnt,
-                   device_status_ptr());
+    e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg::SMEM_BYTES, st, ta, tb, M, N, K, splits, groups, ep, part,
+                   cnt, device_status_ptr());
   } else {
-    kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, st>>>(ta, tb, M, N, K, splits, ep, part, cnt, device_status_ptr());
+    kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, st>>>(ta, tb, M, N, K, splits, groups, ep, part, cnt,
+                                                       device_status_ptr());
     e = cudaGetLastError();
   }
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "gemm: launch");
@@ -622,32 +801,32 @@ static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M
 
 template <int BN>
 static qcf_status dispatch_kn(EpiKind epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
-                              int splits, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
-                              int units, bool pdl) {
+                              int splits, int groups, const EpiParams& ep, float* part, unsigned int* cnt,
+                              cudaStream_t st, int grid, bool pdl) {
   if constexpr (BN >= 64) {
     if (epi == EPI_STORE_BF16)
-      return launch_cfg<BN, EPI_STORE_BF16, 0, true>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
+      return launch_cfg<BN, EPI_STORE_BF16, 0, true>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
     if (epi == EPI_ADD_F32)
-      return launch_cfg<BN, EPI_ADD_F32, 0, true>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
+      return launch_cfg<BN, EPI_ADD_F32, 0, true>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
   }
   return set_error(QCF_ERR_UNSUPPORTED, "gemm: [K][N] weights support the store and add epilogues only");
 }
 
 template <int BN>
 static qcf_status dispatch_epi(EpiKind epi, int hd, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
-                               int splits, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
-                               int units, bool pdl) {
+                               int splits, int groups, const EpiParams& ep, float* part, unsigned int* cnt,
+                               cudaStream_t st, int grid, bool pdl) {
   switch (epi) {
-    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0, false>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
-    case EPI_ADD_F32: return launch_cfg<BN, EPI_ADD_F32, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
+    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+    case EPI_ADD_F32: return launch_cfg<BN, EPI_ADD_F32, 0, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
     case EPI_SWIGLU:
-      if constexpr (BN >= 128) return launch_cfg<BN, EPI_SWIGLU, 0>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
+      if constexpr (BN >= 128) return launch_cfg<BN, EPI_SWIGLU, 0, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
       break;
     case EPI_QKV_ROPE:
-      if (hd == 16) return launch_cfg<BN, EPI_QKV_ROPE, 16>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
-      if (hd == 64) return launch_cfg<BN, EPI_QKV_ROPE, 64>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
+      if (hd == 16) return launch_cfg<BN, EPI_QKV_ROPE, 16, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+      if (hd == 64) return launch_cfg<BN, EPI_QKV_ROPE, 64, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
       if constexpr (BN >= 128)
-        if (hd == 128) return launch_cfg<BN, EPI_QKV_ROPE, 128>(ta, tb, M, N, K, splits, ep, part, cnt, st, units, pdl);
+        if (hd == 128) return launch_cfg<BN, EPI_QKV_ROPE, 128, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
       break;
   }
   return set_error(QCF_ERR_UNSUPPORTED, "gemm: no kernel for epilogue %d, BN %d, head dim %d", epi, BN, hd);
@@ -655,40 +834,43 @@ static qcf_status dispatch_epi(EpiKind epi, int hd, const CUtensorMap& ta, const
 
 qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const __nv_bfloat16* W, int N,
                        const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc, bool w_kn,
-                       bool pdl) {
+                       bool pdl, bool ws_zeroed) {
   if (M <= 0) return QCF_OK;
   if (K % kBK || N % 64 || K <= 0 || N <= 0) return set_error(QCF_ERR_SHAPE, "gemm: K=%d N=%d (K%%64, N%%64 required)", K, N);
   const int hd = epi == EPI_QKV_ROPE ? ep.D : 16;
   GemmPlan p = plan_gemm(M, N, K, epi, hd);
   float* part = nullptr;
   unsigned int* cnt = nullptr;
-  if (p.splits > 1) {
-    const size_t pb = align_up(static_cast<size_t>(p.tiles) * p.splits * kBM * p.BN * sizeof(float), 256);
-    const size_t cb = align_up(static_cast<size_t>(p.tiles) * sizeof(unsigned int), 256);
-    if (!ws || ws_bytes < pb + cb) return set_error(QCF_ERR_WORKSPACE, "gemm: workspace %zu < %zu", ws_bytes, pb + cb);
-    part = static_cast<float*>(ws);
-    cnt = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + pb);
-    cudaError_t e = cudaMemsetAsync(cnt, 0, p.tiles * sizeof(unsigned int), st);
-    if (e != cudaSuccess) return cuda_error(e, "gemm: counter reset");
+  if (p.splits > 1 || p.groups > 0) {
+    const size_t need = kCntBytes + plan_part_bytes(p, M);
+    if (!ws || ws_bytes < need) return set_error(QCF_ERR_WORKSPACE, "gemm: workspace %zu < %zu", ws_bytes, need);
+    cnt = static_cast<unsigned int*>(ws);
+    part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCntBytes);
+    if (!ws_zeroed) {
+      const cudaError_t e = cudaMemsetAsync(cnt, 0, p.tiles * sizeof(unsigned int), st);
+      if (e != cudaSuccess) return cuda_error(e, "gemm: counter reset");
+    }
   }
   CUtensorMap ta, tb;
   const bool tb_ok = w_kn ? encode_tmap_2d(&tb, W, N, K, static_cast<uint64_t>(N) * 2, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B)
                           : encode_tmap_2d(&tb, W, K, N, static_cast<uint64_t>(K) * 2, kBK, p.BN, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!encode_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) || !tb_ok)
+  if (!encode_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tb_ok)
     return set_error(QCF_ERR_CUDA, "gemm: tensor map encoding failed");
   const int units = p.tiles * p.splits;
+  const int grid = p.groups > 0 ? p.groups * ((M + kBM - 1) / kBM) : (units < num_sms() ? units : num_sms());
   LaunchScope ls(kc, st);
   if (w_kn) {
     switch (p.BN) {
-      case 256: return dispatch_kn<256>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
-      case 128: return dispatch_kn<128>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
-      default: return dispatch_kn<64>(epi, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
+      case 256: return dispatch_kn<256>(epi, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+      case 128: return dispatch_kn<128>(epi, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+      default: return dispatch_kn<64>(epi, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
     }
   }
   switch (p.BN) {
-    case 256: return dispatch_epi<256>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
-    case 128: return dispatch_epi<128>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
-    default: return dispatch_epi<64>(epi, hd, ta, tb, M, N, K, p.splits, ep, part, cnt, st, units, pdl);
+    case 256: return dispatch_epi<256>(epi, hd, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+    case 128: return dispatch_epi<128>(epi, hd, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+    default: return dispatch_epi<64>(epi, hd, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
   }
 }
 

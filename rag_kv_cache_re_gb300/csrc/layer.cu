@@ -47,6 +47,7 @@ struct LayerBufs {
   __nv_bfloat16* act;
   void* gemm_ws;
   size_t gemm_ws_bytes;
+  bool gemm_zeroed = false;  // its GEMM counters were zeroed on the stream the GEMMs run on
   void* attn_ws;
   size_t attn_ws_bytes;
 };
@@ -131,7 +132,7 @@ static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, co
   ep.status = device_status_ptr();
   qcf_status s = gemm_launch(EPI_QKV_ROPE, b.h, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
                              (Hq + 2 * Hkv) * D, ep, b.gemm_ws, b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_QKV,
-                             false, pdl);
+                             false, pdl, b.gemm_zeroed);
   if (s != QCF_OK) return s;
   s = attn_launch(b.q, cache_row, n, Kc, Vc, T, Hq, Hkv, D, 1.0f / sqrtf(static_cast<float>(D)), b.o, nullptr, b.attn_ws,
                   b.attn_ws_bytes, st, probe ? KC_ATTN_PROBE : KC_ATTN, pdl);
@@ -140,7 +141,7 @@ static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, co
   eo.out = x;
   eo.ldo = d.d_model;
   s = gemm_launch(EPI_ADD_F32, b.o, n, Hq * D, reinterpret_cast<const __nv_bfloat16*>(w.w_o), d.d_model, eo, b.gemm_ws,
-                  b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_O, false, pdl);
+                  b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_O, false, pdl, b.gemm_zeroed);
   if (s != QCF_OK) return s;
   e = launch_rmsnorm(x, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_mlp), d.eps, b.h, st, pdl);
   if (e != cudaSuccess) return cuda_error(e, "layer: rmsnorm");
@@ -148,13 +149,13 @@ static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, co
   eg.out = b.act;
   eg.ldo = d.ffn_padded;
   s = gemm_launch(EPI_SWIGLU, b.h, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_gu), 2 * d.ffn_padded, eg,
-                  b.gemm_ws, b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_GU, false, pdl);
+                  b.gemm_ws, b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_GU, false, pdl, b.gemm_zeroed);
   if (s != QCF_OK) return s;
   EpiParams edn{};
   edn.out = x;
   edn.ldo = d.d_model;
   return gemm_launch(EPI_ADD_F32, b.act, n, d.ffn_padded, reinterpret_cast<const __nv_bfloat16*>(w.w_down), d.d_model,
-                     edn, b.gemm_ws, b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_DOWN, false, pdl);
+                     edn, b.gemm_ws, b.gemm_ws_bytes, st, probe ? KC_GEMM_PROBE : KC_GEMM_DOWN, false, pdl, b.gemm_zeroed);
 }
 
 // ------------------------------------------------------------------ small helper kernels
@@ -396,7 +397,8 @@ static qcf_status hkvd_layer(const qcf_model* m, int l, HkvdLayout& H, const flo
   ep.max_pos = m->rope.max_pos;
   ep.status = device_status_ptr();
   qcf_status s = gemm_launch(EPI_QKV_ROPE, H.h, n_prev, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
-                             (Hq + 2 * Hkv) * D, ep, H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_QKV);
+                             (Hq + 2 * Hkv) * D, ep, H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_QKV, false, false,
+                             H.lb.gemm_zeroed);
   if (s != QCF_OK) return s;
   float* dev = dev_out ? dev_out : H.dev;
   if ((e = launch_kv_deviation(H.k_tmp, H.v_tmp, rows_prev, n_ctx, Kl, Vl, T, HD, dev, st)) != cudaSuccess)
@@ -431,7 +433,7 @@ static qcf_status hkvd_layer(const qcf_model* m, int l, HkvdLayout& H, const flo
   eo.out = x_new;
   eo.ldo = d.d_model;
   s = gemm_launch(EPI_ADD_F32, H.lb.o, nk, QD, reinterpret_cast<const __nv_bfloat16*>(w.w_o), d.d_model, eo,
-                  H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_O);
+                  H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_O, false, false, H.lb.gemm_zeroed);
   if (s != QCF_OK) return s;
   if ((e = launch_rmsnorm(x_new, nk, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_mlp), d.eps, H.h, st)) !=
       cudaSuccess)
@@ -440,13 +442,13 @@ static qcf_status hkvd_layer(const qcf_model* m, int l, HkvdLayout& H, const flo
   eg.out = H.lb.act;
   eg.ldo = d.ffn_padded;
   s = gemm_launch(EPI_SWIGLU, H.h, nk, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_gu), 2 * d.ffn_padded, eg,
-                  H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_GU);
+                  H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_GU, false, false, H.lb.gemm_zeroed);
   if (s != QCF_OK) return s;
   EpiParams edn{};
   edn.out = x_new;
   edn.ldo = d.d_model;
   return gemm_launch(EPI_ADD_F32, H.lb.act, nk, d.ffn_padded, reinterpret_cast<const __nv_bfloat16*>(w.w_down),
-                     d.d_model, edn, H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_DOWN);
+                     d.d_model, edn, H.lb.gemm_ws, H.lb.gemm_ws_bytes, st, KC_GEMM_DOWN, false, false, H.lb.gemm_zeroed);
 }
 
 struct EventPool {
@@ -637,6 +639,9 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
   qcf_status s = QCF_OK;
   cudaError_t e = cudaSuccess;
   // ---- compute stream
+  LayerBufs& glb = hkvd ? H.lb : rl.lb;
+  if ((s = gemm_ws_prepare(glb.gemm_ws, glb.gemm_ws_bytes, cs)) != QCF_OK) return s;
+  glb.gemm_zeroed = true;
   const __nv_bfloat16* embed = reinterpret_cast<const __nv_bfloat16*>(m->embed);
   const float* x_final = nullptr;  // final hidden states of the recomputed rows [ns][d]
   int ns = 0;
@@ -728,7 +733,8 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
       ep.max_pos = m->rope.max_pos;
       ep.status = device_status_ptr();
       s = gemm_launch(EPI_QKV_ROPE, rl.lb.h, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
-                      d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_PROBE, false, Q <= kPdlMaxRows);
+                      d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_PROBE, false, Q <= kPdlMaxRows,
+                      rl.lb.gemm_zeroed);
       if (s != QCF_OK) return s;
     }
     // profile the re-rotated critical-layer keys and select
@@ -877,6 +883,8 @@ qcf_status qcf_fused_layer_forward(const qcf_model* m, int layer, float* x, cons
   Carve c{static_cast<uint8_t*>(ws), ws_bytes};
   LayerBufs b;
   if (!carve_layer(c, m->dims, n, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_fused_layer_forward: workspace");
+  if ((s = gemm_ws_prepare(b.gemm_ws, b.gemm_ws_bytes, static_cast<cudaStream_t>(stream))) != QCF_OK) return s;
+  b.gemm_zeroed = true;
   return layer_forward_impl(m, layer, x, rope_pos, cache_row, n, reinterpret_cast<__nv_bfloat16*>(K_cache),
                             reinterpret_cast<__nv_bfloat16*>(V_cache), T, b, static_cast<cudaStream_t>(stream));
 }
@@ -911,6 +919,8 @@ qcf_status qcf_full_prefill(const qcf_model* m, const int32_t* ids, int T, qcf_b
   void* lm_ws = c.take<uint8_t>(256);
   LayerBufs b;
   if (!carve_layer(c, m->dims, T, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_full_prefill: workspace");
+  if ((s = gemm_ws_prepare(b.gemm_ws, b.gemm_ws_bytes, st)) != QCF_OK) return s;
+  b.gemm_zeroed = true;
   cudaError_t e = launch_embed(reinterpret_cast<const __nv_bfloat16*>(m->embed), m->dims.vocab, m->dims.d_model, ids,
                                nullptr, 0, T, x, st);
   if (e != cudaSuccess) return cuda_error(e, "qcf_full_prefill: embed");

@@ -93,10 +93,14 @@ struct EpiParams {
   int Hq, Hkv, D, T, max_pos;
   unsigned int* status;    // device status word for index-check failures
 };
+// GEMM workspace: tile arrival counters (reset to zero by every completed launch)
+// followed by fp32 partial slots.  gemm_ws_prepare zeroes the counters once, after
+// which launches given ws_zeroed skip their own counter reset.
 size_t gemm_workspace_size(int M, int N, int K);
+qcf_status gemm_ws_prepare(void* ws, size_t ws_bytes, cudaStream_t st);
 qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const __nv_bfloat16* W, int N,
                        const EpiParams& ep, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc,
-                       bool w_kn = false, bool pdl = false);
+                       bool w_kn = false, bool pdl = false, bool ws_zeroed = false);
 
 // Row kernels (rows.cu).
 cudaError_t launch_embed(const __nv_bfloat16* embed, int vocab, int d, const int32_t* ids, const int32_t* rows,
@@ -188,6 +192,19 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+// Untiled bulk copies (cp.async.bulk): addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load_g2s(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_s2g(void* dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
