@@ -71,15 +71,19 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
   }
 }
 
-// fp32 partial tiles in the workspace are stored column-quad-major: element
-// (row, col) of a 128 x BN slot sits at ((col / 4) * 128 + row) * 4 + col % 4, so
-// a warp (32 consecutive rows) moving one float4 each touches 512 contiguous bytes.
+// fp32 partial tiles in the workspace: each epilogue warp's 32 rows form one
+// contiguous block of BN x 32 floats, column-quad-major inside it: element (row, col)
+// of a 128 x BN slot sits at (((row / 32) * (BN / 4) + col / 4) * 32 + row % 32) * 4
+// + col % 4.  A warp moving one float4 per lane touches 512 contiguous bytes, and a
+// warp's whole partial is one bulk copy.
+template <int BN>
 __device__ __forceinline__ size_t part_idx(int row, int quad) {
-  return (static_cast<size_t>(quad) * kBM + row) * 4;
+  return ((static_cast<size_t>(row >> 5) * (BN / 4) + quad) * 32 + (row & 31)) * 4;
 }
 
 // Loads 32 accumulator columns [32c, 32c+32) of this thread's row, either from
 // TMEM (direct) or as the in-order sum of the split-K partials in the workspace.
+template <int BN>
 struct ChunkLoader {
   uint32_t taddr;       // TMEM address of (row quarter, column 0) of the accumulator
   const float* part;    // the tile's first partial slot, or nullptr for TMEM
@@ -93,15 +97,74 @@ struct ChunkLoader {
     } else {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float4 t = __ldcg(reinterpret_cast<const float4*>(part + part_idx(row, c * 8 + q)));
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(part + part_idx<BN>(row, c * 8 + q)));
         v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
       }
-      for (int s = 1; s < splits; ++s) {
+      // two slots per round trip (the sum stays in slot order)
+      int s = 1;
+#pragma unroll 1
+      for (; s + 1 < splits; s += 2) {
+        const float* p = rest + static_cast<size_t>(s - 1) * part_stride;
+        float4 t0[8], t1[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          t0[q] = __ldcg(reinterpret_cast<const float4*>(p + part_idx<BN>(row, c * 8 + q)));
+          t1[q] = __ldcg(reinterpret_cast<const float4*>(p + part_stride + part_idx<BN>(row, c * 8 + q)));
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          v[4 * q] += t0[q].x; v[4 * q + 1] += t0[q].y; v[4 * q + 2] += t0[q].z; v[4 * q + 3] += t0[q].w;
+          v[4 * q] += t1[q].x; v[4 * q + 1] += t1[q].y; v[4 * q + 2] += t1[q].z; v[4 * q + 3] += t1[q].w;
+        }
+      }
+      if (s < splits) {
         const float* p = rest + static_cast<size_t>(s - 1) * part_stride;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const float4 t = __ldcg(reinterpret_cast<const float4*>(p + part_idx(row, c * 8 + q)));
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(p + part_idx<BN>(row, c * 8 + q)));
           v[4 * q] += t.x; v[4 * q + 1] += t.y; v[4 * q + 2] += t.z; v[4 * q + 3] += t.w;
+        }
+      }
+    }
+  }
+};
+
+// The last arriver's partial sums with the other units' partials staged in shared
+// memory: slot j of the tile (in slot order) is this unit's own accumulator in TMEM
+// when j == own, else staged part jj = j - (j > own) at smem[((jj * BN/4 + quad) * 32
+// + lane) * 4] (a warp's 32 rows of one column quad, as stored in the workspace).
+// Summing in slot order keeps the result independent of which unit arrives last.
+template <int BN>
+struct StagedPartLoader {
+  uint32_t taddr;
+  const float* smem;  // this warp's staged parts
+  int parts, own;
+  __device__ __forceinline__ void operator()(int c, float* v) const {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int j = 0; j < parts; ++j) {
+      if (j == own) {
+        if (j == 0) {
+          tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float t[16];
+            tmem_ld16(taddr + static_cast<uint32_t>(c * 32 + h * 16), t);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[h * 16 + i] += t[i];
+          }
+        }
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(smem) + (j - (j > own)) * (BN / 4) * 32 + c * 8 * 32 + lane;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = src[q * 32];
+          if (j == 0) {
+            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+          } else {
+            v[4 * q] += x.x; v[4 * q + 1] += x.y; v[4 * q + 2] += x.z; v[4 * q + 3] += x.w;
+          }
         }
       }
     }
@@ -126,8 +189,8 @@ __device__ __forceinline__ void load_f32x(const float* src, float* v, int n) {
 
 // Epilogue of one tile for the calling thread's row.  `row` < M is checked here.
 // `tile` is this warp's 32x33 fp32 staging area in shared memory.
-template <int BN, int EPI, int HD>
-__device__ __forceinline__ void tile_epilogue(const ChunkLoader& ld, const EpiParams& ep, int row, int M, int n0,
+template <int BN, int EPI, int HD, class Loader>
+__device__ __forceinline__ void tile_epilogue(const Loader& ld, const EpiParams& ep, int row, int M, int n0,
                                               float* tile) {
   const bool live = row < M;
   if constexpr (EPI == EPI_STORE_BF16) {
@@ -610,20 +673,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
       } else if (w.parts == 1) {
-        ChunkLoader ld{taddr, nullptr, nullptr, 1, 0, row_in_tile};
+        ChunkLoader<BN> ld{taddr, nullptr, nullptr, 1, 0, row_in_tile};
         tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
       } else {
         float* mine = ws_part + static_cast<size_t>(w.mine) * kSlot;
+        const bool warp_live = row - lane < M;  // rows past M are neither written nor summed
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < (warp_live ? BN / 32 : 0); ++c) {
           float v[32];
           tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(mine + part_idx(row_in_tile, c * 8 + q)) =
+            *reinterpret_cast<float4*>(mine + part_idx<BN>(row_in_tile, c * 8 + q)) =
                 make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
         tc_fence_before();
@@ -640,11 +704,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         epi_bar();
         const int last = *s_last;
         epi_bar();
-        if (last) {
+        if (last && warp_live) {
           __threadfence();
-          ChunkLoader ld{0u, ws_part + static_cast<size_t>(w.first) * kSlot, ws_part + static_cast<size_t>(w.rest) * kSlot,
-                         w.parts, w.step * kSlot, row_in_tile};
-          tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
+          // On the CTA's last unit the pipeline stages are idle and this unit's own
+          // accumulator stays in TMEM: stage the other partials there (one bulk copy
+          // per partial and warp) and sum from shared memory.  The residual-add
+          // epilogue keeps the global path: with this loader inlined its register
+          // demand spills and measured slower.
+          constexpr int kWarpPartBytes = BN * 32 * 4;  // a warp's rows of one partial
+          const int per_warp = (w.parts - 1) * kWarpPartBytes;
+          UnitWalk peek = walk;
+          Unit nx;
+          const bool stage = EPI != EPI_ADD_F32 && !peek.next(nx) && 4 * per_warp <= Cfg::STAGES * Cfg::STAGE_BYTES;
+          bool staged_ok = false;
+          const int own = w.mine == w.first ? 0 : (w.mine - w.rest) / w.step + 1;
+          float* sp = reinterpret_cast<float*>(smem + static_cast<size_t>(quarter) * per_warp);
+          if (stage) {
+            // the other units' partials were written with generic stores: order the
+            // async-proxy (bulk copy) reads below after them
+            asm volatile("fence.proxy.async;" ::: "memory");
+            if (lane == 0) mbar_arrive_expect_tx(&xbar[quarter], static_cast<uint32_t>(per_warp));
+            __syncwarp();
+            if (lane < w.parts) {
+              const int j = lane;
+              if (j != own) {
+                const float* src = ws_part + static_cast<size_t>(j == 0 ? w.first : w.rest + (j - 1) * w.step) * kSlot +
+                                   part_idx<BN>(quarter * 32, 0);
+                bulk_load_g2s(sp + static_cast<size_t>(j - (j > own)) * (kWarpPartBytes / 4), src, kWarpPartBytes,
+                              &xbar[quarter]);
+              }
+            }
+            staged_ok = mbar_wait(&xbar[quarter], 0);
+            if (!staged_ok) {
+              flag_status(status, QCF_DEV_TIMEOUT);
+              mbar_wait(&xbar[quarter], 0);  // once more, bounded, so no copy is left landing in smem
+            }
+          }
+          if constexpr (EPI != EPI_ADD_F32) {
+            if (staged_ok) {
+              tc_fence_after();
+              StagedPartLoader<BN> ld{taddr, sp, w.parts, own};
+              tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
+            }
+          }
+          if (!stage) {
+            ChunkLoader<BN> ld{0u, ws_part + static_cast<size_t>(w.first) * kSlot,
+                           ws_part + static_cast<size_t>(w.rest) * kSlot, w.parts, w.step * kSlot, row_in_tile};
+            tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
+          }
         }
       }
     }
@@ -686,9 +793,10 @@ constexpr int kSkFixupPerPart = 8;
 //    is cheaper than its share suggests, because the full rounds are slowed by the
 //    L2 bandwidth all SMs draw together (measured: 0.30 us per k block for a lone CTA,
 //    0.40 us with all 152 busy).
-//  * M <= 128 (the probe's query rows): weight-bound; one busy SM streams about
-//    45 GB/s of weights through the TMA ring, so time ~ rounds x bytes per unit /
-//    45 GB/s, plus ~10 us and the partial traffic when K is split.
+//  * M <= 128 (the probe's query rows): weight-bound.  Measured per-SM weight streams
+//    through the TMA ring are ~29 / 55 / 65 GB/s for BN = 64 / 128 / 256, under an
+//    aggregate of ~6.5 TB/s from HBM; a k split adds the last arriver's fixup, about
+//    0.6 us per 32-column chunk and pair of partials, plus 1 us.
 static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
   const int sms = num_sms();
   const int tiles_m = (M + kBM - 1) / kBM;
@@ -721,9 +829,10 @@ static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
   }
   GemmPlan best{64, 1, tiles_m * (N / 64), 0};
   double best_t = 1e30;
+  const double all_bytes = static_cast<double>(N) * K * 2.0;
   for (int bn : cands) {
     if (!valid(bn)) continue;
-    const double stream = bn == 64 ? 28.0e9 : 45.0e9;   // bytes/s one SM pulls with this tile's ring
+    const double stream = bn == 64 ? 29.0e9 : (bn == 128 ? 55.0e9 : 65.0e9);  // one SM's weight stream
     const int tiles = tiles_m * (N / bn);
     if (tiles > kCntCells) continue;
     for (int s = 1; s <= 8; ++s) {
@@ -732,8 +841,9 @@ static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
       const int rounds = (units + sms - 1) / sms;
       const double unit_bytes = static_cast<double>(bn) * (static_cast<double>(K) / s) * 2.0;
       const double unit_flops = 2.0 * kBM * bn * (static_cast<double>(K) / s);
-      double t = rounds * std::max(unit_bytes / stream, unit_flops / 11.0e12 + 1.0e-6);
-      if (s > 1) t += 10.0e-6 + units * (kBM * bn * 4.0 * 2.0) / 1.5e12;
+      double t = std::max(all_bytes / 6.5e12, rounds * std::max(unit_bytes / stream, unit_flops / 11.0e12));
+      const double chunks = bn / 32.0;
+      t += s > 1 ? 1.0e-6 + chunks * ((s + 1) / 2) * 0.6e-6 : chunks * 0.3e-6;
       if (t < best_t * 0.98) {
         best_t = t;
         best = GemmPlan{bn, s, tiles, 0};
