@@ -218,7 +218,7 @@ qcf_status qcf_rope_table_fill_host(float* cos_host, float* sin_host, int max_po
 namespace qcf {
 
 bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
-                    uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+                    uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle, CUtensorMapDataType dtype) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -234,7 +234,7 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

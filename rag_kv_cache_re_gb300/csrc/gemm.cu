@@ -37,11 +37,7 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = 2 * BN;
-  // the last unit's residual tile, staged in the (then idle) pipeline stages: 128 rows
-  // of BN floats, each row padded by 16 bytes so row-per-thread float4 reads spread
-  // over all banks
-  static constexpr int X_STRIDE = BN + 4;
-  static_assert(kBM * X_STRIDE * 4 <= STAGES * STAGE_BYTES, "residual tile must fit the stages");
+  static_assert(kBM * BN * 4 <= STAGES * STAGE_BYTES, "a residual tile must fit the stages");
   static constexpr int EPI_BYTES = 4 * 32 * 33 * 4;   // one 32x32 fp32 transpose tile per epilogue warp
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
 };
@@ -362,23 +358,33 @@ __device__ __forceinline__ void tile_epilogue(const Loader& ld, const EpiParams&
   }
 }
 
-// Residual add of one warp's 32 rows from a tile staged in shared memory: each lane
-// bulk-copies its row's BN floats of x into its padded smem row, adds its TMEM
-// accumulator row in place, and bulk-stores the row back.  All copies of the warp
-// complete on bar (one use per launch).  Rows >= M are skipped.
+// Residual add of one warp's 32 rows with everything staged in shared memory (the
+// pipeline stages, idle on the CTA's last unit).  Lane 0 loads the warp's x rows as
+// BN/32 TMA boxes of 32 rows x 32 fp32 (128-byte swizzle: row r keeps 16-byte
+// chunk j at j ^ (r % 8), so row-per-lane float4 accesses hit every bank once), and
+// lanes 1.. bulk-copy the other units' partials of a shared tile.  The accumulator
+// sum (slot order, this unit's own part from TMEM) is added into x in place and the
+// boxes are stored back by TMA, which leaves rows past M untouched.  All copies
+// complete on bar (one use per launch).
 template <int BN>
-__device__ __forceinline__ void add_epilogue_staged(uint32_t taddr, float* xs_warp, uint64_t* bar, float* x,
-                                                    int ldo, int row, int M, int n0, unsigned int* status) {
-  constexpr int kStride = BN + 4;
-  constexpr uint32_t kRowBytes = BN * 4;
+__device__ __forceinline__ void add_tile_staged(uint32_t taddr, const CUtensorMap* tmX, uint8_t* region,
+                                                const float* first, const float* rest, size_t step, int parts,
+                                                int own, uint64_t* bar, int row0, int n0, unsigned int* status) {
+  constexpr int kBox = 32 * 32 * 4;            // one x box
+  constexpr int kPart = BN * 32 * 4;           // a warp's rows of one partial
   const int lane = threadIdx.x & 31;
-  const bool live = row < M;
-  const unsigned nlive = __popc(__ballot_sync(0xffffffffu, live));
-  float* xs = xs_warp + lane * kStride;
-  float* xg = x + static_cast<size_t>(live ? row : 0) * ldo + n0;
-  if (lane == 0) mbar_arrive_expect_tx(bar, nlive * kRowBytes);
+  float* xs = reinterpret_cast<float*>(region);
+  const float* ps = reinterpret_cast<const float*>(region + (BN / 32) * kBox);
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>((BN / 32) * kBox + (parts - 1) * kPart));
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) tma_load_2d(xs + c * 1024, tmX, bar, n0 + c * 32, row0);
+  }
   __syncwarp();
-  if (live) bulk_load_g2s(xs, xg, kRowBytes, bar);
+  if (parts > 1 && lane < parts && lane != own) {
+    const float* src = lane == 0 ? first : rest + (lane - 1) * step;
+    bulk_load_g2s(region + (BN / 32) * kBox + (lane - (lane > own)) * kPart, src, kPart, bar);
+  }
   if (!mbar_wait(bar, 0)) {
     flag_status(status, QCF_DEV_TIMEOUT);
     mbar_wait(bar, 0);  // once more, bounded, so no copy is left landing in smem
@@ -387,18 +393,50 @@ __device__ __forceinline__ void add_epilogue_staged(uint32_t taddr, float* xs_wa
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     float v[32];
-    tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
-    float4* p = reinterpret_cast<float4*>(xs + c * 32);
+    if (parts == 1) {
+      tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
+    } else {
+#pragma unroll 1
+      for (int j = 0; j < parts; ++j) {
+        if (j == own) {
+          if (j == 0) {
+            tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float t[16];
+              tmem_ld16(taddr + static_cast<uint32_t>(c * 32 + h * 16), t);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[h * 16 + i] += t[i];
+            }
+          }
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(ps) + (j - (j > own)) * (BN / 4) * 32 + c * 8 * 32 + lane;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 x = src[q * 32];
+            if (j == 0) {
+              v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+            } else {
+              v[4 * q] += x.x; v[4 * q + 1] += x.y; v[4 * q + 2] += x.z; v[4 * q + 3] += x.w;
+            }
+          }
+        }
+      }
+    }
+    float4* row = reinterpret_cast<float4*>(xs + c * 1024 + lane * 32);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      float4 t = p[q];
+      float4 t = row[q ^ (lane & 7)];
       t.x += v[4 * q]; t.y += v[4 * q + 1]; t.z += v[4 * q + 2]; t.w += v[4 * q + 3];
-      p[q] = t;
+      row[q ^ (lane & 7)] = t;
     }
   }
-  fence_proxy_async_smem();  // the generic-proxy writes above, before the bulk store reads them
-  if (live) {
-    bulk_store_s2g(xg, xs, kRowBytes);
+  fence_proxy_async_smem();  // the generic-proxy writes above, before TMA reads them
+  __syncwarp();
+  if (lane == 0) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) tma_store_2d(tmX, xs + c * 1024, n0 + c * 32, row0);
     bulk_commit_group();
     bulk_wait_group0();
   }
@@ -490,8 +528,9 @@ struct UnitWalk {
 
 template <int BN, int EPI, int HD, bool BMN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
-                        int N, int K, int splits, int groups, const EpiParams ep, float* __restrict__ ws_part,
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmX, int M, int N, int K, int splits, int groups,
+                        const EpiParams ep, float* __restrict__ ws_part,
                         unsigned int* __restrict__ ws_cnt, unsigned int* status) {
   using Cfg = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -646,6 +685,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int local = 0; walk.next(w); ++local) {
       const int mt = w.mt, nt = w.nt;
       const int acc = local & 1;
+      if constexpr (EPI == EPI_ADD_F32) {
+        // the residual rows of the CTA's last unit: pull them into L2 (kept there
+        // ahead of the weight stream) while the main loop runs.  Only for GEMMs of up to
+        // 2048 rows: with many m tiles the kept lines cost the weight reuse more than
+        // they save (measured on the 5184-row full prefill).
+        UnitWalk peek = walk;
+        Unit nx;
+        const int r = mt * kBM + row_in_tile;
+        if (M <= 2048 && !peek.next(nx) && r < M) {
+          const char* xr = reinterpret_cast<const char*>(static_cast<const float*>(ep.out) + static_cast<size_t>(r) * ep.ldo +
+                                                         static_cast<size_t>(nt) * BN);
+#pragma unroll 1
+          for (int b = 0; b < BN * 4; b += 128) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xr + b));
+        }
+      }
       const bool got = mbar_wait(&tfull[acc], (local >> 1) & 1);
       if (!got) flag_status(status, QCF_DEV_TIMEOUT);
       if (shared_tiles) {
@@ -657,18 +711,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
       const int row = mt * kBM + row_in_tile;
       const int n0 = nt * BN;
-      bool staged = false;
-      if constexpr (EPI == EPI_ADD_F32) {
-        // On the CTA's last unit no stage will be loaded again and the MMAs that read
-        // them have completed (tfull), so the residual tile is staged there with one
-        // bulk copy per row: one load latency instead of one per 32-column chunk.
+      // On the CTA's last unit no stage will be loaded again and the MMAs that read
+      // them have completed (tfull): the residual-add epilogue stages there.
+      bool last_unit = false;
+      {
         UnitWalk peek = walk;
         Unit nx;
-        staged = w.parts == 1 && !peek.next(nx);
+        last_unit = !peek.next(nx);
       }
+      const bool warp_live = row - lane < M;  // rows past M are neither written nor summed
+      bool staged = false;
+      if constexpr (EPI == EPI_ADD_F32) staged = w.parts == 1 && last_unit;
       if (staged) {
-        add_epilogue_staged<BN>(taddr, reinterpret_cast<float*>(smem) + static_cast<size_t>(quarter) * 32 * Cfg::X_STRIDE,
-                                &xbar[quarter], static_cast<float*>(ep.out), ep.ldo, row, M, n0, status);
+        if (warp_live)
+          add_tile_staged<BN>(taddr, &tmX, smem + static_cast<size_t>(quarter) * BN * 32 * 4, nullptr, nullptr, 0, 1, 0,
+                              &xbar[quarter], row - lane, n0, status);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -680,7 +737,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) mbar_arrive(&tempty[acc]);
       } else {
         float* mine = ws_part + static_cast<size_t>(w.mine) * kSlot;
-        const bool warp_live = row - lane < M;  // rows past M are neither written nor summed
 #pragma unroll 1
         for (int c = 0; c < (warp_live ? BN / 32 : 0); ++c) {
           float v[32];
@@ -708,18 +764,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __threadfence();
           // On the CTA's last unit the pipeline stages are idle and this unit's own
           // accumulator stays in TMEM: stage the other partials there (one bulk copy
-          // per partial and warp) and sum from shared memory.  The residual-add
-          // epilogue keeps the global path: with this loader inlined its register
-          // demand spills and measured slower.
-          constexpr int kWarpPartBytes = BN * 32 * 4;  // a warp's rows of one partial
-          const int per_warp = (w.parts - 1) * kWarpPartBytes;
-          UnitWalk peek = walk;
-          Unit nx;
-          const bool stage = EPI != EPI_ADD_F32 && !peek.next(nx) && 4 * per_warp <= Cfg::STAGES * Cfg::STAGE_BYTES;
+          // per partial and warp; the residual add stages x beside them) and sum from
+          // shared memory.  Warp regions are laid out for the live warps only.
+          constexpr int kWarpPartBytes = BN * 32 * 4;  // a warp's rows of one partial (or its x rows)
+          const int per_warp = (EPI == EPI_ADD_F32 ? w.parts : w.parts - 1) * kWarpPartBytes;
+          const int live_warps = min(4, (M - mt * kBM + 31) / 32);
+          const bool stage = last_unit && w.parts <= 32 && live_warps * per_warp <= Cfg::STAGES * Cfg::STAGE_BYTES;
           bool staged_ok = false;
           const int own = w.mine == w.first ? 0 : (w.mine - w.rest) / w.step + 1;
           float* sp = reinterpret_cast<float*>(smem + static_cast<size_t>(quarter) * per_warp);
-          if (stage) {
+          if constexpr (EPI == EPI_ADD_F32) {
+            if (stage) {
+              asm volatile("fence.proxy.async;" ::: "memory");
+              tc_fence_after();
+              add_tile_staged<BN>(taddr, &tmX, reinterpret_cast<uint8_t*>(sp),
+                                  ws_part + static_cast<size_t>(w.first) * kSlot + part_idx<BN>(quarter * 32, 0),
+                                  ws_part + static_cast<size_t>(w.rest) * kSlot + part_idx<BN>(quarter * 32, 0),
+                                  w.step * kSlot, w.parts, own, &xbar[quarter], row - lane, n0, status);
+            }
+          } else if (stage) {
             // the other units' partials were written with generic stores: order the
             // async-proxy (bulk copy) reads below after them
             asm volatile("fence.proxy.async;" ::: "memory");
@@ -886,9 +949,9 @@ qcf_status gemm_ws_prepare(void* ws, size_t ws_bytes, cudaStream_t st) {
 }
 
 template <int BN, int EPI, int HD, bool BMN = false>
-static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int splits,
-                             int groups, const EpiParams& ep, float* part, unsigned int* cnt, cudaStream_t st,
-                             int grid, bool pdl) {
+static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tx, int M, int N,
+                             int K, int splits, int groups, const EpiParams& ep, float* part, unsigned int* cnt,
+                             cudaStream_t st, int grid, bool pdl) {
   using Cfg = GemmCfg<BN>;
   auto kern = gemm_tcgen05_kernel<BN, EPI, HD, BMN>;
   static std::once_flag once;
@@ -899,10 +962,10 @@ static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "gemm: shared memory attribute");
   cudaError_t e = cudaSuccess;
   if (pdl) {
-    e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg::SMEM_BYTES, st, ta, tb, M, N, K, splits, groups, ep, part,
-                   cnt, device_status_ptr());
+    e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Cfg::SMEM_BYTES, st, ta, tb, tx, M, N, K, splits, groups, ep,
+                   part, cnt, device_status_ptr());
   } else {
-    kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, st>>>(ta, tb, M, N, K, splits, groups, ep, part, cnt,
+    kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, st>>>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt,
                                                        device_status_ptr());
     e = cudaGetLastError();
   }
@@ -910,33 +973,35 @@ static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, int M
 }
 
 template <int BN>
-static qcf_status dispatch_kn(EpiKind epi, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+static qcf_status dispatch_kn(EpiKind epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tx, int M,
+                              int N, int K,
                               int splits, int groups, const EpiParams& ep, float* part, unsigned int* cnt,
                               cudaStream_t st, int grid, bool pdl) {
   if constexpr (BN >= 64) {
     if (epi == EPI_STORE_BF16)
-      return launch_cfg<BN, EPI_STORE_BF16, 0, true>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+      return launch_cfg<BN, EPI_STORE_BF16, 0, true>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
     if (epi == EPI_ADD_F32)
-      return launch_cfg<BN, EPI_ADD_F32, 0, true>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+      return launch_cfg<BN, EPI_ADD_F32, 0, true>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
   }
   return set_error(QCF_ERR_UNSUPPORTED, "gemm: [K][N] weights support the store and add epilogues only");
 }
 
 template <int BN>
-static qcf_status dispatch_epi(EpiKind epi, int hd, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+static qcf_status dispatch_epi(EpiKind epi, int hd, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tx,
+                               int M, int N, int K,
                                int splits, int groups, const EpiParams& ep, float* part, unsigned int* cnt,
                                cudaStream_t st, int grid, bool pdl) {
   switch (epi) {
-    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
-    case EPI_ADD_F32: return launch_cfg<BN, EPI_ADD_F32, 0, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+    case EPI_STORE_BF16: return launch_cfg<BN, EPI_STORE_BF16, 0, false>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+    case EPI_ADD_F32: return launch_cfg<BN, EPI_ADD_F32, 0, false>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
     case EPI_SWIGLU:
-      if constexpr (BN >= 128) return launch_cfg<BN, EPI_SWIGLU, 0, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+      if constexpr (BN >= 128) return launch_cfg<BN, EPI_SWIGLU, 0, false>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
       break;
     case EPI_QKV_ROPE:
-      if (hd == 16) return launch_cfg<BN, EPI_QKV_ROPE, 16, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
-      if (hd == 64) return launch_cfg<BN, EPI_QKV_ROPE, 64, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+      if (hd == 16) return launch_cfg<BN, EPI_QKV_ROPE, 16, false>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+      if (hd == 64) return launch_cfg<BN, EPI_QKV_ROPE, 64, false>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
       if constexpr (BN >= 128)
-        if (hd == 128) return launch_cfg<BN, EPI_QKV_ROPE, 128, false>(ta, tb, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
+        if (hd == 128) return launch_cfg<BN, EPI_QKV_ROPE, 128, false>(ta, tb, tx, M, N, K, splits, groups, ep, part, cnt, st, grid, pdl);
       break;
   }
   return set_error(QCF_ERR_UNSUPPORTED, "gemm: no kernel for epilogue %d, BN %d, head dim %d", epi, BN, hd);
@@ -961,26 +1026,31 @@ qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const 
       if (e != cudaSuccess) return cuda_error(e, "gemm: counter reset");
     }
   }
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tx;
+  // the residual-add epilogue stages x through TMA boxes of 32 rows x 32 fp32
+  const bool tx_ok = epi != EPI_ADD_F32 ||
+                     encode_tmap_2d(&tx, ep.out, N, M, static_cast<uint64_t>(ep.ldo) * 4, 32, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
   const bool tb_ok = w_kn ? encode_tmap_2d(&tb, W, N, K, static_cast<uint64_t>(N) * 2, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B)
                           : encode_tmap_2d(&tb, W, K, N, static_cast<uint64_t>(K) * 2, kBK, p.BN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!encode_tmap_2d(&ta, A, K, M, static_cast<uint64_t>(K) * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tb_ok)
+      !tb_ok || !tx_ok)
     return set_error(QCF_ERR_CUDA, "gemm: tensor map encoding failed");
+  if (epi != EPI_ADD_F32) tx = ta;  // unused by the other epilogues
   const int units = p.tiles * p.splits;
   const int grid = p.groups > 0 ? p.groups * ((M + kBM - 1) / kBM) : (units < num_sms() ? units : num_sms());
   LaunchScope ls(kc, st);
   if (w_kn) {
     switch (p.BN) {
-      case 256: return dispatch_kn<256>(epi, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
-      case 128: return dispatch_kn<128>(epi, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
-      default: return dispatch_kn<64>(epi, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+      case 256: return dispatch_kn<256>(epi, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+      case 128: return dispatch_kn<128>(epi, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+      default: return dispatch_kn<64>(epi, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
     }
   }
   switch (p.BN) {
-    case 256: return dispatch_epi<256>(epi, hd, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
-    case 128: return dispatch_epi<128>(epi, hd, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
-    default: return dispatch_epi<64>(epi, hd, ta, tb, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+    case 256: return dispatch_epi<256>(epi, hd, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+    case 128: return dispatch_epi<128>(epi, hd, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
+    default: return dispatch_epi<64>(epi, hd, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
   }
 }
 
