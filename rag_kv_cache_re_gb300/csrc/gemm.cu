@@ -369,7 +369,8 @@ __device__ __forceinline__ void tile_epilogue(const Loader& ld, const EpiParams&
 template <int BN>
 __device__ __forceinline__ void add_tile_staged(uint32_t taddr, const CUtensorMap* tmX, uint8_t* region,
                                                 const float* first, const float* rest, size_t step, int parts,
-                                                int own, uint64_t* bar, int row0, int n0, unsigned int* status) {
+                                                int own, uint64_t* bar, uint32_t phase, int row0, int n0,
+                                                unsigned int* status) {
   constexpr int kBox = 32 * 32 * 4;            // one x box
   constexpr int kPart = BN * 32 * 4;           // a warp's rows of one partial
   const int lane = threadIdx.x & 31;
@@ -385,9 +386,9 @@ __device__ __forceinline__ void add_tile_staged(uint32_t taddr, const CUtensorMa
     const float* src = lane == 0 ? first : rest + (lane - 1) * step;
     bulk_load_g2s(region + (BN / 32) * kBox + (lane - (lane > own)) * kPart, src, kPart, bar);
   }
-  if (!mbar_wait(bar, 0)) {
+  if (!mbar_wait(bar, phase)) {
     flag_status(status, QCF_DEV_TIMEOUT);
-    mbar_wait(bar, 0);  // once more, bounded, so no copy is left landing in smem
+    mbar_wait(bar, phase);  // once more, bounded, so no copy is left landing in smem
     return;
   }
 #pragma unroll 1
@@ -441,6 +442,40 @@ __device__ __forceinline__ void add_tile_staged(uint32_t taddr, const CUtensorMa
     bulk_wait_group0();
   }
   __syncwarp();
+}
+
+// One pass of a shared tile's staged fixup for the store / SwiGLU / QKV epilogues:
+// columns [h BNP, (h + 1) BNP) of the tile.  The other units' partials of those columns
+// (a contiguous BNP x 32-float block of each warp's slab) are bulk-copied to smem, then
+// the epilogue runs on their slot-ordered sum with this unit's own TMEM part.
+__host__ __device__ constexpr int passes_or1(int p) { return p > 0 ? p : 1; }
+
+template <int BNP, int EPI, int HD>
+__device__ __forceinline__ bool staged_fixup_pass(int h, uint32_t taddr, float* sp, const float* first,
+                                                  const float* rest, size_t step, int parts, int own, uint64_t* bar,
+                                                  const EpiParams& ep, int row, int M, int n0, float* tile,
+                                                  unsigned int* status) {
+  constexpr int kPassPart = BNP * 32 * 4;  // a warp's rows of one partial, these columns
+  const int lane = threadIdx.x & 31;
+  if (h > 0) {
+    fence_proxy_async_smem();  // the previous pass's generic reads, before these copies overwrite them
+    __syncwarp();
+  }
+  if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>((parts - 1) * kPassPart));
+  __syncwarp();
+  if (lane < parts && lane != own) {
+    const float* src = (lane == 0 ? first : rest + (lane - 1) * step) + static_cast<size_t>(h) * BNP * 32;
+    bulk_load_g2s(sp + static_cast<size_t>(lane - (lane > own)) * (kPassPart / 4), src, kPassPart, bar);
+  }
+  if (!mbar_wait(bar, static_cast<uint32_t>(h & 1))) {
+    flag_status(status, QCF_DEV_TIMEOUT);
+    mbar_wait(bar, static_cast<uint32_t>(h & 1));  // once more, bounded, so no copy is left landing in smem
+    return false;
+  }
+  tc_fence_after();
+  StagedPartLoader<BNP> ld{taddr + static_cast<uint32_t>(h * BNP), sp, parts, own};
+  tile_epilogue<BNP, EPI, HD>(ld, ep, row, M, n0 + h * BNP, tile);
+  return true;
 }
 
 // One work unit: k blocks [kb0, kb1) of output tile (mt, nt).  A tile whose k range
@@ -725,7 +760,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (staged) {
         if (warp_live)
           add_tile_staged<BN>(taddr, &tmX, smem + static_cast<size_t>(quarter) * BN * 32 * 4, nullptr, nullptr, 0, 1, 0,
-                              &xbar[quarter], row - lane, n0, status);
+                              &xbar[quarter], 0, row - lane, n0, status);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -765,49 +800,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // On the CTA's last unit the pipeline stages are idle and this unit's own
           // accumulator stays in TMEM: stage the other partials there (one bulk copy
           // per partial and warp; the residual add stages x beside them) and sum from
-          // shared memory.  Warp regions are laid out for the live warps only.
+          // shared memory.  Warp regions are laid out for the live warps only; a tile
+          // whose staging does not fit goes in two passes of BN / 2 columns.
           constexpr int kWarpPartBytes = BN * 32 * 4;  // a warp's rows of one partial (or its x rows)
           const int per_warp = (EPI == EPI_ADD_F32 ? w.parts : w.parts - 1) * kWarpPartBytes;
           const int live_warps = min(4, (M - mt * kBM + 31) / 32);
-          const bool stage = last_unit && w.parts <= 32 && live_warps * per_warp <= Cfg::STAGES * Cfg::STAGE_BYTES;
-          bool staged_ok = false;
+          constexpr int kStageBytes = Cfg::STAGES * Cfg::STAGE_BYTES;
+          int passes = 0;
+          if (last_unit && w.parts <= 32) {
+            if (live_warps * per_warp <= kStageBytes) passes = 1;
+            else if (BN == 256 && live_warps * (per_warp / 2) <= kStageBytes) passes = 2;
+          }
+          const bool stage = passes > 0;
           const int own = w.mine == w.first ? 0 : (w.mine - w.rest) / w.step + 1;
-          float* sp = reinterpret_cast<float*>(smem + static_cast<size_t>(quarter) * per_warp);
-          if constexpr (EPI == EPI_ADD_F32) {
-            if (stage) {
-              asm volatile("fence.proxy.async;" ::: "memory");
-              tc_fence_after();
-              add_tile_staged<BN>(taddr, &tmX, reinterpret_cast<uint8_t*>(sp),
-                                  ws_part + static_cast<size_t>(w.first) * kSlot + part_idx<BN>(quarter * 32, 0),
-                                  ws_part + static_cast<size_t>(w.rest) * kSlot + part_idx<BN>(quarter * 32, 0),
-                                  w.step * kSlot, w.parts, own, &xbar[quarter], row - lane, n0, status);
-            }
-          } else if (stage) {
+          float* sp = reinterpret_cast<float*>(smem + static_cast<size_t>(quarter) * (per_warp / passes_or1(passes)));
+          const float* pfirst = ws_part + static_cast<size_t>(w.first) * kSlot + part_idx<BN>(quarter * 32, 0);
+          const float* prest = ws_part + static_cast<size_t>(w.rest) * kSlot + part_idx<BN>(quarter * 32, 0);
+          if (stage) {
             // the other units' partials were written with generic stores: order the
             // async-proxy (bulk copy) reads below after them
             asm volatile("fence.proxy.async;" ::: "memory");
-            if (lane == 0) mbar_arrive_expect_tx(&xbar[quarter], static_cast<uint32_t>(per_warp));
-            __syncwarp();
-            if (lane < w.parts) {
-              const int j = lane;
-              if (j != own) {
-                const float* src = ws_part + static_cast<size_t>(j == 0 ? w.first : w.rest + (j - 1) * w.step) * kSlot +
-                                   part_idx<BN>(quarter * 32, 0);
-                bulk_load_g2s(sp + static_cast<size_t>(j - (j > own)) * (kWarpPartBytes / 4), src, kWarpPartBytes,
-                              &xbar[quarter]);
+            tc_fence_after();
+            if constexpr (EPI == EPI_ADD_F32) {
+              if (passes == 1) {
+                add_tile_staged<BN>(taddr, &tmX, reinterpret_cast<uint8_t*>(sp), pfirst, prest, w.step * kSlot, w.parts,
+                                    own, &xbar[quarter], 0, row - lane, n0, status);
+              } else if constexpr (BN == 256) {
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h)
+                  add_tile_staged<BN / 2>(taddr + static_cast<uint32_t>(h * BN / 2), &tmX, reinterpret_cast<uint8_t*>(sp),
+                                          pfirst + h * (BN / 2) * 32, prest + h * (BN / 2) * 32, w.step * kSlot,
+                                          w.parts, own, &xbar[quarter], static_cast<uint32_t>(h), row - lane,
+                                          n0 + h * (BN / 2), status);
               }
-            }
-            staged_ok = mbar_wait(&xbar[quarter], 0);
-            if (!staged_ok) {
-              flag_status(status, QCF_DEV_TIMEOUT);
-              mbar_wait(&xbar[quarter], 0);  // once more, bounded, so no copy is left landing in smem
-            }
-          }
-          if constexpr (EPI != EPI_ADD_F32) {
-            if (staged_ok) {
-              tc_fence_after();
-              StagedPartLoader<BN> ld{taddr, sp, w.parts, own};
-              tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
+            } else {
+              if (passes == 1) {
+                staged_fixup_pass<BN, EPI, HD>(0, taddr, sp, pfirst, prest, w.step * kSlot, w.parts, own,
+                                               &xbar[quarter], ep, row, M, n0, my_tile, status);
+              } else if constexpr (BN == 256) {
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h)
+                  if (!staged_fixup_pass<BN / 2, EPI, HD>(h, taddr, sp, pfirst, prest, w.step * kSlot, w.parts, own,
+                                                          &xbar[quarter], ep, row, M, n0, my_tile, status))
+                    break;
+              }
             }
           }
           if (!stage) {
