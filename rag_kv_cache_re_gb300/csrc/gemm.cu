@@ -877,21 +877,20 @@ struct GemmPlan {
 constexpr int kCntCells = 4096;
 constexpr size_t kCntBytes = kCntCells * sizeof(unsigned int);
 
-// Main-loop k blocks that a grouped stream-K CTA's shared-tile epilogues cost,
-// measured on GB300: about 10 for the partial write plus 8 per partial the last
-// arriver reads back (its fixup loads are latency-bound).
-constexpr int kSkFixupBase = 10;
-constexpr int kSkFixupPerPart = 8;
+// Main-loop k blocks a grouped stream-K plan must save over the lockstep grid before
+// its shared-tile fixups pay off, fitted to 16 layer-shape x M measurements on GB300
+// (M = 256 ... 1664): 40, plus 13 per partial beyond two.
+constexpr int kSkMinGain = 40;
+constexpr int kSkGainPerPart = 13;
 
 // Chooses the tile width BN, the k split and the schedule from measurements on GB300:
 //  * M > 128 (the recompute GEMMs): the widest tile (BN = 256).  The lockstep grid
 //    runs ceil(tiles / SMs) rounds of a whole k range each; grouped stream-K gives
 //    every CTA (SMs / tiles_m groups of tiles_m CTAs) an equal share of the
-//    (n tile, k block) space instead.  Costs are counted in k blocks per CTA plus the
-//    fixup, and stream-K must win by 10 %: a last lockstep round that runs part-empty
-//    is cheaper than its share suggests, because the full rounds are slowed by the
-//    L2 bandwidth all SMs draw together (measured: 0.30 us per k block for a lone CTA,
-//    0.40 us with all 152 busy).
+//    (n tile, k block) space instead.  Costs are counted in k blocks per CTA; a last
+//    lockstep round that runs part-empty costs less than its share suggests, because
+//    full rounds are slowed by the L2 bandwidth all SMs draw together (measured: 0.30
+//    us per k block for a lone CTA, 0.40 us with all 152 busy).
 //  * M <= 128 (the probe's query rows): weight-bound.  Measured per-SM weight streams
 //    through the TMA ring are ~29 / 55 / 65 GB/s for BN = 64 / 128 / 256, under an
 //    aggregate of ~6.5 TB/s from HBM; a k split adds the last arriver's fixup, about
@@ -921,8 +920,8 @@ static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
     if (groups >= 1 && tiles <= kCntCells && iters >= 4LL * groups && (iters + 1) * groups < (1LL << 31)) {
       const long long per = iters / groups;                                   // k blocks per CTA
       const long long parts = std::min<long long>(groups, (kb + per - 1) / per + 1);  // per shared tile, at most
-      const long long sk = per + 1 + kSkFixupBase + kSkFixupPerPart * parts;
-      if (sk * 10 < lockstep * 9) return GemmPlan{bn, 1, tiles, groups};
+      if (lockstep - per > kSkMinGain + kSkGainPerPart * std::max<long long>(0, parts - 2))
+        return GemmPlan{bn, 1, tiles, groups};
     }
     return GemmPlan{bn, 1, tiles, 0};
   }

@@ -279,13 +279,25 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
   for (int v = blockIdx.x * 8 + wid; v < vocab; v += nwarps) {
     const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(v) * d);
     float acc = 0.f;
-    for (int i = lane; i < d / 8; i += 32) {
-      float f[8];
-      bf16x8_to_f32(wr[i], f);
-      const float4 h0 = *reinterpret_cast<const float4*>(hs + 8 * i);
-      const float4 h1 = *reinterpret_cast<const float4*>(hs + 8 * i + 4);
-      acc += f[0] * h0.x + f[1] * h0.y + f[2] * h0.z + f[3] * h0.w + f[4] * h1.x + f[5] * h1.y + f[6] * h1.z +
-             f[7] * h1.w;
+    // four independent 16-byte weight loads per lane in flight before their FMAs
+    const int n8 = d / 8;
+    for (int i0 = lane; i0 < n8; i0 += 128) {
+      uint4 wv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + 32 * u < n8) wv[u] = __ldcs(wr + i0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + 32 * u;
+        if (i < n8) {
+          float f[8];
+          bf16x8_to_f32(wv[u], f);
+          const float4 h0 = *reinterpret_cast<const float4*>(hs + 8 * i);
+          const float4 h1 = *reinterpret_cast<const float4*>(hs + 8 * i + 4);
+          acc += f[0] * h0.x + f[1] * h0.y + f[2] * h0.z + f[3] * h0.w + f[4] * h1.x + f[5] * h1.y + f[6] * h1.z +
+                 f[7] * h1.w;
+        }
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
