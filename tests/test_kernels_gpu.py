@@ -203,7 +203,12 @@ def test_sparse_causal_attn(Q, T, n, Hq, Hkv, D, pattern):
 @pytest.mark.parametrize("M,N,K", [(23, 192, 64), (1, 64, 64), (300, 384, 192), (832, 6144, 4096), (832, 4096, 4096), (832, 28672, 4096),
                                    (64, 4096, 14336), (832, 4096, 14336), (200, 28672, 256),
                                    # two 128-row tiles, the second ragged
-                                   (129, 6144, 4096), (144, 28672, 4096), (144, 4096, 4096), (256, 4096, 14336)])
+                                   (129, 6144, 4096), (144, 28672, 4096), (144, 4096, 4096), (256, 4096, 14336),
+                                   # the 8B layer shapes at the recompute and probe row counts: grouped stream-K
+                                   # with staged fixups in one or two column passes, the lockstep staged
+                                   # residual add, k splits with staged partials
+                                   (832, 6144, 4096), (832, 28672, 4096), (832, 4096, 4096), (832, 4096, 14336),
+                                   (1664, 4096, 14336), (64, 6144, 4096), (64, 4096, 14336)])
 def test_linear_store_and_add(Q, M, N, K):
     A = qd.normal_bf16((M, K), 1.0, 31, DEV)
     W = qd.normal_bf16((N, K), 0.02, 32, DEV)
@@ -219,6 +224,23 @@ def test_linear_store_and_add(Q, M, N, K):
     # sum once (2^-23 relative); bound by the result's scale
     acc_tol = (K / 16) * 2.0 ** -22 * max(1.0, float(np.sqrt(np.mean(ref ** 2))))
     assert_close(base.cpu().numpy(), b0 + ref, atol=max(1e-5, acc_tol), rtol=1e-5, what="fp32 residual add")
+
+
+@pytest.mark.parametrize("M,N,K", [(832, 4096, 14336), (64, 4096, 14336), (832, 6144, 4096)])
+def test_linear_shared_tiles_deterministic(Q, M, N, K):
+    # shared tiles are summed in slot order whichever unit arrives last: repeated
+    # launches give the same bits
+    A = qd.normal_bf16((M, K), 1.0, 36, DEV)
+    W = qd.normal_bf16((N, K), 0.02, 37, DEV)
+    first = Q.qcf_linear(A, W)
+    x0 = torch.randn((M, N), device=DEV, dtype=torch.float32)
+    x1 = x0.clone()
+    Q.qcf_linear(A, W, out=x0, add=True)
+    for _ in range(3):
+        assert torch.equal(Q.qcf_linear(A, W), first)
+    Q.qcf_linear(A, W, out=x1, add=True)
+    torch.cuda.synchronize()
+    assert torch.equal(x0, x1)
 
 
 @pytest.mark.parametrize("M,N,K", [(23, 64, 64), (300, 384, 192), (832, 4096, 4096), (64, 4096, 14336)])
