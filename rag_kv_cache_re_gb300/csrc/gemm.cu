@@ -771,47 +771,73 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
       } else {
-        float* mine = ws_part + static_cast<size_t>(w.mine) * kSlot;
+        // On the CTA's last unit the pipeline stages are idle and this unit's own
+        // accumulator stays in TMEM: the last arriver stages the other partials there
+        // (one bulk copy per partial and warp; the residual add stages x beside them)
+        // and sums from shared memory.  Warp regions are laid out for the live warps
+        // only; a tile whose staging does not fit goes in two passes of BN / 2 columns.
+        constexpr int kWarpPartBytes = BN * 32 * 4;  // a warp's rows of one partial (or its x rows)
+        const int per_warp = (EPI == EPI_ADD_F32 ? w.parts : w.parts - 1) * kWarpPartBytes;
+        const int live_warps = min(4, (M - mt * kBM + 31) / 32);
+        constexpr int kStageBytes = Cfg::STAGES * Cfg::STAGE_BYTES;
+        int passes = 0;
+        if (last_unit && w.parts <= 32) {
+          if (live_warps * per_warp <= kStageBytes) passes = 1;
+          else if (BN == 256 && live_warps * (per_warp / 2) <= kStageBytes) passes = 2;
+        }
+        const bool stage = passes > 0;
+        // When staging is possible and every other unit of the tile has already arrived
+        // (the usual case under stream-K: the other pieces of a cut column come first
+        // in their groups' ranges), this unit is the last: it writes no partial.
+        // the accumulator goes back to the MMA warp as soon as nothing reads it any more:
+        // after the partial is written, or after a staged fixup that reads it in TMEM
+        bool released = false;
+        auto release_acc = [&] {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+          released = true;
+        };
+        int last = 0;
+        if (stage) {
+          if (threadIdx.x == 64) {
+            unsigned int c;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(&ws_cnt[w.cnt]) : "memory");
+            const int all_in = c == static_cast<unsigned int>(w.parts - 1);
+            if (all_in) ws_cnt[w.cnt] = 0u;  // no other unit of the tile remains: back to zero
+            *s_last = all_in;
+          }
+          epi_bar();
+          last = *s_last;
+          epi_bar();
+        }
+        if (!last) {
+          float* mine = ws_part + static_cast<size_t>(w.mine) * kSlot;
 #pragma unroll 1
-        for (int c = 0; c < (warp_live ? BN / 32 : 0); ++c) {
-          float v[32];
-          tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
+          for (int c = 0; c < (warp_live ? BN / 32 : 0); ++c) {
+            float v[32];
+            tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(mine + part_idx<BN>(row_in_tile, c * 8 + q)) =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<float4*>(mine + part_idx<BN>(row_in_tile, c * 8 + q)) =
+                  make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
+          if (!stage) release_acc();
+          __threadfence();
+          epi_bar();
+          if (threadIdx.x == 64) {
+            const unsigned int prev = atomicAdd(&ws_cnt[w.cnt], 1u);
+            const int is_last = prev == static_cast<unsigned int>(w.parts - 1);
+            if (is_last) ws_cnt[w.cnt] = 0u;  // back to zero for the next launch on this workspace
+            *s_last = is_last;
+          }
+          epi_bar();
+          last = *s_last;
+          epi_bar();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
-        __threadfence();
-        epi_bar();
-        if (threadIdx.x == 64) {
-          const unsigned int prev = atomicAdd(&ws_cnt[w.cnt], 1u);
-          const int last = prev == static_cast<unsigned int>(w.parts - 1);
-          if (last) ws_cnt[w.cnt] = 0u;  // back to zero for the next launch on this workspace
-          *s_last = last;
-        }
-        epi_bar();
-        const int last = *s_last;
-        epi_bar();
+        if (!(last && warp_live) && !released) release_acc();
         if (last && warp_live) {
           __threadfence();
-          // On the CTA's last unit the pipeline stages are idle and this unit's own
-          // accumulator stays in TMEM: stage the other partials there (one bulk copy
-          // per partial and warp; the residual add stages x beside them) and sum from
-          // shared memory.  Warp regions are laid out for the live warps only; a tile
-          // whose staging does not fit goes in two passes of BN / 2 columns.
-          constexpr int kWarpPartBytes = BN * 32 * 4;  // a warp's rows of one partial (or its x rows)
-          const int per_warp = (EPI == EPI_ADD_F32 ? w.parts : w.parts - 1) * kWarpPartBytes;
-          const int live_warps = min(4, (M - mt * kBM + 31) / 32);
-          constexpr int kStageBytes = Cfg::STAGES * Cfg::STAGE_BYTES;
-          int passes = 0;
-          if (last_unit && w.parts <= 32) {
-            if (live_warps * per_warp <= kStageBytes) passes = 1;
-            else if (BN == 256 && live_warps * (per_warp / 2) <= kStageBytes) passes = 2;
-          }
-          const bool stage = passes > 0;
           const int own = w.mine == w.first ? 0 : (w.mine - w.rest) / w.step + 1;
           float* sp = reinterpret_cast<float*>(smem + static_cast<size_t>(quarter) * (per_warp / passes_or1(passes)));
           const float* pfirst = ws_part + static_cast<size_t>(w.first) * kSlot + part_idx<BN>(quarter * 32, 0);
@@ -851,6 +877,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                            ws_part + static_cast<size_t>(w.rest) * kSlot, w.parts, w.step * kSlot, row_in_tile};
             tile_epilogue<BN, EPI, HD>(ld, ep, row, M, n0, my_tile);
           }
+          if (!released) release_acc();
         }
       }
     }
