@@ -448,8 +448,6 @@ __device__ __forceinline__ void add_tile_staged(uint32_t taddr, const CUtensorMa
 // columns [h BNP, (h + 1) BNP) of the tile.  The other units' partials of those columns
 // (a contiguous BNP x 32-float block of each warp's slab) are bulk-copied to smem, then
 // the epilogue runs on their slot-ordered sum with this unit's own TMEM part.
-__host__ __device__ constexpr int passes_or1(int p) { return p > 0 ? p : 1; }
-
 template <int BNP, int EPI, int HD>
 __device__ __forceinline__ bool staged_fixup_pass(int h, uint32_t taddr, float* sp, const float* first,
                                                   const float* rest, size_t step, int parts, int own, uint64_t* bar,
@@ -839,7 +837,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (last && warp_live) {
           __threadfence();
           const int own = w.mine == w.first ? 0 : (w.mine - w.rest) / w.step + 1;
-          float* sp = reinterpret_cast<float*>(smem + static_cast<size_t>(quarter) * (per_warp / passes_or1(passes)));
+          float* sp = reinterpret_cast<float*>(smem + static_cast<size_t>(quarter) * (per_warp / max(passes, 1)));
           const float* pfirst = ws_part + static_cast<size_t>(w.first) * kSlot + part_idx<BN>(quarter * 32, 0);
           const float* prest = ws_part + static_cast<size_t>(w.rest) * kSlot + part_idx<BN>(quarter * 32, 0);
           if (stage) {
