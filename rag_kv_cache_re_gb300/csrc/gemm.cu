@@ -6,11 +6,14 @@
 //   warp 1   TMEM allocator and single-thread tcgen05.mma issuer (M=128, N=BN, K=16 steps)
 //   warps 2-5 epilogue: tcgen05.ld of the accumulator (one row per thread), fused op, store
 // The accumulator is double-buffered in TMEM so the epilogue of one tile overlaps
-// the main loop of the next.  Work units are (m tile, n tile, k split); consecutive
-// units walk the m tiles of one weight tile so concurrently running CTAs share it
-// through L2.  With k splits > 1 every unit writes an fp32 partial to the
-// workspace and the last unit of a tile (counted with an atomic) sums the
-// partials in split order -- deterministic -- and runs the epilogue.
+// the main loop of the next.  Work units are k ranges of (m tile, n tile); a CTA
+// walks them on one of two schedules (UnitWalk): lockstep (units strided over the
+// grid, m tile fastest, so concurrently running CTAs share each weight tile through
+// L2; optionally k-split) or grouped stream-K (groups of tiles_m CTAs splitting the
+// (n tile, k block) space evenly).  A tile shared by several units is finished by
+// the last to arrive (counted with an atomic), which sums the fp32 partials in slot
+// order -- deterministic -- and runs the epilogue; on the CTA's last unit it stages
+// the partials (and, for the residual add, the x tile) in the idle pipeline stages.
 //
 // Fused epilogues:
 //   STORE_BF16  out[m][n] = acc
