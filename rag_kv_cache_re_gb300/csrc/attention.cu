@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
                                                           __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                                           int split_tiles, int max_splits, float* __restrict__ part_o,
                                                           float2* __restrict__ part_ml, unsigned int* status,
-                                                          int check) {
+                                                          int check, int heads_fast) {
   using Cfg = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -57,9 +57,12 @@ __global__ void __launch_bounds__(256) sparse_attn_kernel(const __grid_constant_
   const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_blocks = (n + BR - 1) / BR;
-  const int rb = n_blocks - 1 - static_cast<int>(blockIdx.x) / max_splits;
-  const int sp = static_cast<int>(blockIdx.x) % max_splits;
-  const int g = blockIdx.y;
+  // grid (row block x split, KV head), or (KV head, row block x split) when heads_fast:
+  // row blocks run heaviest first
+  const int rbsp = static_cast<int>(heads_fast ? blockIdx.y : blockIdx.x);
+  const int rb = n_blocks - 1 - rbsp / max_splits;
+  const int sp = rbsp % max_splits;
+  const int g = static_cast<int>(heads_fast ? blockIdx.x : blockIdx.y);
   const int row0 = rb * BR;
   const int row_end = min(n, row0 + BR);
   const int kmax = pos[row_end - 1];
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ pos, int n, int T, int Hq,
                           int Hkv, int G, int BRp, float scale_log2, __nv_bfloat16* __restrict__ o,
                           float* __restrict__ lse, int split_tiles, int max_splits, float* __restrict__ part_o,
-                          float2* __restrict__ part_ml, unsigned int* status, int check) {
+                          float2* __restrict__ part_ml, unsigned int* status, int check, int heads_fast) {
   constexpr int D = 128;
   pdl_wait();  // q, pos and the cache come from the kernels before this one
   pdl_launch_dependents();
@@ -348,9 +351,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_blocks = (n + BRp - 1) / BRp;
-  const int rb = n_blocks - 1 - static_cast<int>(blockIdx.x) / max_splits;
-  const int sp = static_cast<int>(blockIdx.x) % max_splits;
-  const int g = blockIdx.y;
+  // grid (row block x split, KV head), or (KV head, row block x split) when heads_fast:
+  // row blocks run heaviest first
+  const int rbsp = static_cast<int>(heads_fast ? blockIdx.y : blockIdx.x);
+  const int rb = n_blocks - 1 - rbsp / max_splits;
+  const int sp = rbsp % max_splits;
+  const int g = static_cast<int>(heads_fast ? blockIdx.x : blockIdx.y);
   const int row0 = rb * BRp;
   const int row_end = min(n, row0 + BRp);
   const int n_tiles_all = pos[row_end - 1] / kTcKeys + 1;
@@ -734,7 +740,14 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
     attr = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   });
   if (attr != cudaSuccess) return cuda_error(attr, "sparse_causal_attn: smem attribute");
-  dim3 grid(plan.n_blocks * plan.max_splits, Hkv);
+  // When every head's K and V fit in L2 together (the fused prefill's layers), the
+  // KV heads go fastest in launch order so each head's heaviest row blocks start in
+  // the first wave; larger caches keep head-major order, whose concurrent CTAs share
+  // one head's K/V stream in L2.
+  const int rbs = plan.n_blocks * plan.max_splits;
+  const int heads_fast =
+      static_cast<size_t>(T) * Hkv * D * 2 * 2 <= (static_cast<size_t>(64) << 20) && rbs <= 65535 ? 1 : 0;
+  dim3 grid = heads_fast ? dim3(Hkv, rbs) : dim3(rbs, Hkv);
   const float scale_log2 = scale * 1.4426950408889634f;
   if constexpr (D == 128) {
     static std::once_flag once_tc;
@@ -747,18 +760,18 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
     if (pdl) {
       cudaError_t e = launch_pdl(sparse_attn_tc_kernel, grid, dim3(kTcThreads), kTcSmem, st, tk, tv, q, pos, n, T, Hq,
                                  Hkv, G, BR, scale_log2, o, lse, plan.split_tiles, plan.max_splits, part_o, part_ml,
-                                 device_status_ptr(), check_enabled() ? 1 : 0);
+                                 device_status_ptr(), check_enabled() ? 1 : 0, heads_fast);
       if (e != cudaSuccess) return cuda_error(e, "sparse_causal_attn: launch");
     } else {
       sparse_attn_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o, lse,
                                                                 plan.split_tiles, plan.max_splits, part_o, part_ml,
-                                                                device_status_ptr(), check_enabled() ? 1 : 0);
+                                                                device_status_ptr(), check_enabled() ? 1 : 0, heads_fast);
     }
   } else {
     LaunchScope ls(kc, st);
     sparse_attn_kernel<D><<<grid, warps * 32, Cfg::SMEM_BYTES, st>>>(
         tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o, lse, plan.split_tiles, plan.max_splits, part_o, part_ml,
-        device_status_ptr(), check_enabled() ? 1 : 0);
+        device_status_ptr(), check_enabled() ? 1 : 0, heads_fast);
   }
   if (plan.max_splits > 1) {
     LaunchScope ls(kc == KC_ATTN ? KC_ATTN_COMBINE : kc, st);
