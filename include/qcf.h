@@ -216,7 +216,11 @@ qcf_status qcf_sparse_causal_attn(const qcf_bf16* q, const int32_t* pos, int n, 
  *   epilogue QCF_EPI_STORE_BF16: out is bf16 [M][N]
  *   epilogue QCF_EPI_ADD_F32:    out is fp32 [M][N] and receives out += A W^T
  *   | QCF_LINEAR_W_KN:           W is stored [K][N] instead (out = A * W)
- * K % 64 == 0, N % 64 == 0. */
+ * K % 64 == 0, N % 64 == 0.  ws: device scratch of qcf_linear_workspace_size
+ * bytes (tile counters and fp32 partial sums when the planner shares output
+ * tiles between CTAs); its contents need not survive between calls, but calls
+ * that share it must be ordered on one stream.  Results are bitwise repeatable
+ * for the same inputs and shapes (partial sums are added in a fixed order). */
 #define QCF_EPI_STORE_BF16 0
 #define QCF_EPI_ADD_F32 1
 #define QCF_LINEAR_W_KN 0x10
