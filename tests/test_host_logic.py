@@ -1,0 +1,83 @@
+"""Host-side logic the product and the bench rely on (CPU only): the seeded input
+generators, the KV-deviation selector's layer schedule, the content-keyed chunk
+store, and the guard that keeps recorded ncu traffic tied to the sources it
+describes."""
+import hashlib
+import json
+import os
+
+import numpy as np
+import pytest
+
+import qcfdata as qd
+import bench
+from rag_kv_cache_re_gb300.model import ChunkStore, StoredChunk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("n,frac", [(10, 0.70), (35, 0.70), (8, 0.5), (5, 1.0), (6, 0.0)])
+def test_shared_chunk_requests(n, frac):
+    a, b = qd.shared_chunk_requests(n, frac)
+    assert len(a) == n and len(b) == n
+    assert len(set(a.tolist())) == n and len(set(b.tolist())) == n   # no repeats inside a request
+    assert len(set(a.tolist()) & set(b.tolist())) == int(np.floor(frac * n + 0.5))
+    a2, b2 = qd.shared_chunk_requests(n, frac)                        # seeded: the same lists again
+    assert np.array_equal(a, a2) and np.array_equal(b, b2)
+
+
+@pytest.mark.parametrize("pattern", ["uniform", "clusters"])
+@pytest.mark.parametrize("C,N", [(100, 15), (4096, 410), (16, 16), (10, 0), (5120, 768)])
+def test_selected_indices(pattern, C, N):
+    idx = qd.selected_indices(C, N, pattern)
+    assert idx.dtype == np.int32 and len(idx) == N
+    if N:
+        assert idx[0] >= 0 and idx[-1] < C
+        assert np.all(np.diff(idx) > 0)                               # strictly ascending, distinct
+    assert np.array_equal(idx, qd.selected_indices(C, N, pattern))
+    if pattern == "clusters" and N:
+        runs = 1 + int(np.sum(np.diff(idx) > 1))
+        assert runs <= 8
+
+
+def test_selected_indices_rejects_unknown_pattern():
+    with pytest.raises(ValueError):
+        qd.selected_indices(100, 10, "stripes")
+
+
+@pytest.mark.parametrize("L,r", [(32, 1500), (32, 3000), (80, 5000), (2, 2500)])
+def test_hkvd_schedule(L, r):
+    s = bench.hkvd_schedule(L, r)
+    assert len(s) == L and s[0] == 2 * r and s[-1] == r
+    # what the library checks before a KV-deviation request runs
+    assert all(0 <= v <= 10000 for v in s)
+    assert all(x >= y for x, y in zip(s, s[1:]))
+
+
+def _chunk(tokens):
+    return StoredChunk(np.asarray(tokens, np.int32), None, None, np.zeros(0, np.int32), None, None)
+
+
+def test_chunk_store_keys_chunks_by_content():
+    store = ChunkStore(model=None, crit_layer=1, n_anchor=0)
+    t = np.arange(40, dtype=np.int64) * 7 % 101
+    assert ChunkStore.content_key(t) == ChunkStore.content_key(t.astype(np.int32))
+    assert ChunkStore.content_key(t) != ChunkStore.content_key(t[::-1].copy())
+    c = store._keep(3, _chunk(t))
+    # another id with the same tokens maps to the stored chunk; different tokens do not
+    assert store._known(9, t.astype(np.int32)) is c and store.chunks[9] is c
+    assert store._known(10, t + 1) is None and 10 not in store.chunks
+
+
+def test_recorded_traffic_follows_the_sources():
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    rec = json.load(open(path))["gemm_gate_up_swiglu"]
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    got = bench.recorded_traffic("gemm_gate_up_swiglu")
+    if h.hexdigest() == rec["sources_sha256"]:
+        assert got == rec["traffic_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    else:
+        assert got is None
+    assert bench.recorded_traffic("no_such_kernel") is None
