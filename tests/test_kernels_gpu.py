@@ -208,25 +208,33 @@ def test_sparse_causal_attn(Q, T, n, Hq, Hkv, D, pattern):
                                    # with staged fixups in one or two column passes, the lockstep staged
                                    # residual add, k splits with staged partials
                                    (832, 6144, 4096), (832, 28672, 4096), (832, 4096, 4096), (832, 4096, 14336),
-                                   (1664, 4096, 14336), (64, 6144, 4096), (64, 4096, 14336)])
+                                   (1664, 4096, 14336), (64, 6144, 4096), (64, 4096, 14336),
+                                   # tiles ending inside a warp's 32 rows (staged copies and stores past M)
+                                   (837, 4096, 14336), (837, 6144, 4096), (100, 4096, 14336)])
 def test_linear_store_and_add(Q, M, N, K):
     A = qd.normal_bf16((M, K), 1.0, 31, DEV)
     W = qd.normal_bf16((N, K), 0.02, 32, DEV)
     ref = (f32(A) @ f32(W).T).astype(np.float64)   # fp32 BLAS: error far below the tolerances used
-    out = Q.qcf_linear(A, W)
+    # outputs are the first M rows of buffers with 64 guard rows after them, which
+    # no epilogue path (direct, staged, TMA-stored) may touch
+    out_g = torch.full((M + 64, N), 7.0, device=DEV, dtype=torch.bfloat16)
+    Q.qcf_linear(A, W, out=out_g[:M])
     torch.cuda.synchronize()
-    assert_close(f32(out), ref, atol=1e-3, rtol=2.0 ** -8, what="bf16 out")
-    base = torch.randn((M, N), device=DEV, dtype=torch.float32)
-    b0 = base.cpu().numpy().astype(np.float64)
-    Q.qcf_linear(A, W, out=base, add=True)
+    assert_close(f32(out_g[:M]), ref, atol=1e-3, rtol=2.0 ** -8, what="bf16 out")
+    assert bool((out_g[M:] == 7.0).all()), "bf16 store wrote past row M"
+    base_g = torch.randn((M + 64, N), device=DEV, dtype=torch.float32)
+    b0 = base_g.cpu().numpy().astype(np.float64)
+    Q.qcf_linear(A, W, out=base_g[:M], add=True)
     torch.cuda.synchronize()
     # fp32 accumulation: each of the K/16 tensor-core steps may round the running
     # sum once (2^-23 relative); bound by the result's scale
     acc_tol = (K / 16) * 2.0 ** -22 * max(1.0, float(np.sqrt(np.mean(ref ** 2))))
-    assert_close(base.cpu().numpy(), b0 + ref, atol=max(1e-5, acc_tol), rtol=1e-5, what="fp32 residual add")
+    got = base_g.cpu().numpy()
+    assert_close(got[:M], b0[:M] + ref, atol=max(1e-5, acc_tol), rtol=1e-5, what="fp32 residual add")
+    assert np.array_equal(got[M:], b0[M:].astype(np.float32)), "residual add wrote past row M"
 
 
-@pytest.mark.parametrize("M,N,K", [(832, 4096, 14336), (64, 4096, 14336), (832, 6144, 4096)])
+@pytest.mark.parametrize("M,N,K", [(832, 4096, 14336), (64, 4096, 14336), (832, 6144, 4096), (837, 4096, 14336)])
 def test_linear_shared_tiles_deterministic(Q, M, N, K):
     # shared tiles are summed in slot order whichever unit arrives last: repeated
     # launches give the same bits
