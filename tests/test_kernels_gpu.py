@@ -198,6 +198,26 @@ def test_sparse_causal_attn(Q, T, n, Hq, Hkv, D, pattern):
     assert Q.qcf_query_status() == 0
 
 
+@pytest.mark.parametrize("T,n,Hq,Hkv,D", [(5184, 832, 32, 8, 128), (300, 45, 4, 4, 64), (96, 23, 4, 4, 16)])
+def test_sparse_causal_attn_writes_only_its_rows(Q, T, n, Hq, Hkv, D):
+    # the C ABI writes o [n][Hq][D]: rows after n in the caller's buffer stay as they were,
+    # and the result equals the binding's own allocation bit for bit
+    Cx = T - 64 if T > 600 else T - 8
+    pos = np.concatenate([qd.selected_indices(Cx, n - (T - Cx), "uniform"), np.arange(Cx, T)]).astype(np.int32)
+    K = qd.normal_bf16((T, Hkv, D), 1.0, 24, DEV)
+    V = qd.normal_bf16((T, Hkv, D), 1.0, 25, DEV)
+    q = qd.normal_bf16((n, Hq, D), 1.0, 26, DEV)
+    p = torch.from_numpy(pos).to(DEV)
+    o = Q.qcf_sparse_causal_attn(q, p, K, V, 1.0 / math.sqrt(D))
+    o_g = torch.full((n + 16, Hq, D), 3.0, device=DEV, dtype=torch.bfloat16)
+    ws = Q.workspace(Q._lib.lib().qcf_sparse_causal_attn_workspace_size(n, T, Hq, Hkv, D), q.device)
+    Q.call("qcf_sparse_causal_attn", Q._ptr(q), Q._ptr(p), n, Q._ptr(K), Q._ptr(V), T, Hq, Hkv, D,
+           float(1.0 / math.sqrt(D)), Q._ptr(o_g), None, Q._ptr(ws), ws.numel(), Q._stream(None))
+    torch.cuda.synchronize()
+    assert torch.equal(o_g[:n], o)
+    assert bool((o_g[n:] == 3.0).all()), "attention wrote past row n"
+
+
 # ----------------------------------------------------------------- dense pieces
 
 @pytest.mark.parametrize("M,N,K", [(23, 192, 64), (1, 64, 64), (300, 384, 192), (832, 6144, 4096), (832, 4096, 4096), (832, 28672, 4096),
