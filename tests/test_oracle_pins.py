@@ -450,3 +450,38 @@ def test_hkvd_gradual_filtering_nests(tiny):
     assert len(a) == O.num_selected(C, 5000) and len(b) == O.num_selected(C, 2000)
     assert np.all(np.diff(a) > 0) and np.all(np.diff(b) > 0) and set(b) <= set(a)
     assert len(out["layer_dev"][1]) == len(a)   # layer 1 measures only the rows kept after layer 0
+
+
+# ----------------------------------------------------------------- offsets in the probe and in profiling
+
+def test_multichunk_probe_and_scores_use_absolute_positions(tiny):
+    # Three chunks, critical layer 1, every token an anchor.  Layer-0 K depends only on the
+    # token and its position and layer-0 V only on the token, so the anchors' re-rotated
+    # layer-0 K/V are full prefill's, and the probe's q at layer 1 is full prefill's q of the
+    # query rows.  A probe that dropped (or negated) the chunks' offsets would see keys at the
+    # wrong positions and fail here; the single-chunk pins above cannot see that.
+    chunks, start, q = tiny_request()
+    C = int(start[-1])
+    kv = [O.chunk_precompute(tiny, c, store_bf16=False) for c in chunks]
+    ctx = np.concatenate(chunks)
+    fused = O.fused_prefill(tiny, kv, ctx, start, q, crit=1, ratio_bp=1500, n_anchor=len(chunks[0]))
+    full = O.full_prefill(tiny, np.concatenate([ctx, q]), capture_q_layer=1)
+    np.testing.assert_allclose(fused["q_crit"], full["q"][C:], atol=5e-5)
+    # The scores: each chunk prefilled alone at its absolute positions gives its layer-1 keys
+    # where the fused layout puts them (attention inside a chunk sees only relative
+    # positions); softmax of q_crit over them, summed by explicit loops.
+    s = qd.TINY
+    G = s.n_heads // s.n_kv_heads
+    K1 = np.concatenate([O.full_prefill(tiny, chunks[c], positions=start[c] + np.arange(len(chunks[c])))["K"][1]
+                         for c in range(len(chunks))]).astype(np.float64)
+    qc = fused["q_crit"].astype(np.float64)
+    want = np.zeros(C)
+    for r in range(len(q)):
+        for h in range(s.n_heads):
+            logit = [math.fsum(qc[r, h] * K1[j, h // G]) / math.sqrt(s.head_dim) for j in range(C)]
+            mx = max(logit)
+            e = [math.exp(v - mx) for v in logit]
+            tot = math.fsum(e)
+            for j in range(C):
+                want[j] += e[j] / tot
+    np.testing.assert_allclose(fused["scores"], want, rtol=1e-4, atol=1e-7)
