@@ -185,13 +185,19 @@ qcf_status qcf_kv_deviation(const qcf_bf16* k_new, const qcf_bf16* v_new, const 
                             const qcf_bf16* K_cache, const qcf_bf16* V_cache, int T, int Hkv, int D, float* dev,
                             void* stream);
 
-/* dst[i][:] = src[idx[i]][:] for i < n; rows of `width` bf16 (width % 8 == 0).
- * idx device [n], each in [0, src_rows). */
+/* Gathers the rows of the tokens chosen for recompute ("KVCache reuse 01" 1.3.4,
+ * selective recompute flow: the selected tokens are masked out of the full
+ * input and only they run through the layer): dst[i][:] = src[idx[i]][:] for i < n.
+ *   src  device [src_rows][width] bf16 (width % 8 == 0); dst device [n][width] bf16
+ *   idx  device [n], each in [0, src_rows); an index outside that range is not read:
+ *        its dst row is left as it was and QCF_DEV_BAD_INDEX is set in the status word. */
 qcf_status qcf_gather_rows(const qcf_bf16* src, int64_t src_rows, int width, const int32_t* idx, int n,
                            qcf_bf16* dst, void* stream);
 
 /* Writes fresh K/V rows of the recomputed tokens into the fused cache at their
- * positions: K_cache[pos[i]] = k_new[i], V_cache[pos[i]] = v_new[i].
+ * positions ("KVCache reuse 01" 1.3.4: the recomputed K_i, V_i extend the reused
+ * cache, and attention then runs over all tokens of the layer):
+ * K_cache[pos[i]] = k_new[i], V_cache[pos[i]] = v_new[i].
  *   k_new, v_new  device [n][Hkv][D] bf16; pos device [n] in [0, T), distinct. */
 qcf_status qcf_scatter_kv(const qcf_bf16* k_new, const qcf_bf16* v_new, const int32_t* pos, int n, int Hkv,
                           int D, qcf_bf16* K_cache, qcf_bf16* V_cache, int T, void* stream);

@@ -54,6 +54,11 @@ unsigned int* device_status_ptr() {
   return per_dev[dev];
 }
 
+int current_device() {
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
 int num_sms() {
   static std::mutex mu;
   static std::vector<int> per_dev;

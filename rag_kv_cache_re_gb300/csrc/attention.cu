@@ -734,10 +734,9 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
   if (!encode_tmap_2d(&tk, K, width, T, width * 2, box_cols, plan.tile, sw) ||
       !encode_tmap_2d(&tv, V, width, T, width * 2, box_cols, plan.tile, sw))
     return set_error(QCF_ERR_CUDA, "sparse_causal_attn: tensor map encoding failed");
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  static PerDevice<cudaError_t> smem_attr;
+  const cudaError_t attr = smem_attr.get(current_device(), [] {
+    return cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   });
   if (attr != cudaSuccess) return cuda_error(attr, "sparse_causal_attn: smem attribute");
   // When every head's K and V fit in L2 together (the fused prefill's layers), the
@@ -750,10 +749,9 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
   dim3 grid = heads_fast ? dim3(Hkv, rbs) : dim3(rbs, Hkv);
   const float scale_log2 = scale * 1.4426950408889634f;
   if constexpr (D == 128) {
-    static std::once_flag once_tc;
-    static cudaError_t attr_tc = cudaSuccess;
-    std::call_once(once_tc, [] {
-      attr_tc = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    static PerDevice<cudaError_t> smem_attr_tc;
+    const cudaError_t attr_tc = smem_attr_tc.get(current_device(), [] {
+      return cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     });
     if (attr_tc != cudaSuccess) return cuda_error(attr_tc, "sparse_causal_attn: smem attribute");
     LaunchScope ls(kc, st);

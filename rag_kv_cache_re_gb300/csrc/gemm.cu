@@ -1017,10 +1017,9 @@ static qcf_status launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const
                              cudaStream_t st, int grid, bool pdl) {
   using Cfg = GemmCfg<BN>;
   auto kern = gemm_tcgen05_kernel<BN, EPI, HD, BMN>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  static PerDevice<cudaError_t> smem_attr;
+  const cudaError_t attr_err = smem_attr.get(current_device(), [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "gemm: shared memory attribute");
   cudaError_t e = cudaSuccess;

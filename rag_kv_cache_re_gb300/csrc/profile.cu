@@ -329,12 +329,12 @@ static qcf_status profile_launch_d(const __nv_bfloat16* q, const __nv_bfloat16* 
                       D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
     return set_error(QCF_ERR_CUDA, "profile_scores: tensor map encoding failed");
   const int smem = kPStages * kPKeyTile * D * 2 + 64 + 8 * 64 * 4 + 1024;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [smem] {
-    attr = cudaFuncSetAttribute(profile_pass_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(profile_pass_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDevice<cudaError_t> smem_attr;
+  const cudaError_t attr = smem_attr.get(current_device(), [smem] {
+    cudaError_t e = cudaFuncSetAttribute(profile_pass_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(profile_pass_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return e;
   });
   if (attr != cudaSuccess) return cuda_error(attr, "profile_scores: smem attribute");
   const int G = Hq / Hkv;

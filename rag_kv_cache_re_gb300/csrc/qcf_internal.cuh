@@ -1,6 +1,7 @@
 // Internal helpers shared by the qcf CUDA sources (sm_103a only).
 #pragma once
 
+#include "per_device.h"
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -51,6 +52,9 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Device SM count (cached per device).
 int num_sms();
+
+// The current device, or -1 when it cannot be read (per-device set-up keys on it).
+int current_device();
 
 // Programmatic dependent launch.  A kernel launched this way may start while its
 // predecessor in the stream drains (set-up of barriers, tensor memory and constant

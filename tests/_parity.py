@@ -1,6 +1,8 @@
 """Comparison helpers for GPU-vs-oracle parity tests."""
 import numpy as np
 
+from oracle import qcf_oracle as O
+
 
 def assert_close(got, ref, atol, rtol, what="", rms_scaled=False):
     """|got - ref| <= atol + rtol*|ref| elementwise (allclose semantics).
@@ -42,3 +44,48 @@ def assert_same_selection(got_idx, ref_values, k, tie_tol, what=""):
     sym = set(got.tolist()) ^ set(ref.tolist())
     bad = [j for j in sym if abs(ref_values[j] - kth) > tie_tol]
     assert not bad, f"{what}: selection differs beyond ties at {bad[:8]} (kth={kth:.6g})"
+
+
+def error_stats(got, ref):
+    """(max-abs, RMS) of got - ref."""
+    d = np.asarray(got, np.float64) - np.asarray(ref, np.float64)
+    if d.size == 0:
+        return 0.0, 0.0
+    return float(np.max(np.abs(d))), float(np.sqrt(np.mean(d * d)))
+
+
+def assert_close_bf16_floor(got, ref, emu, what="", atol=2e-2, rtol=2e-2, rms_factor=1.25, max_factor=2.0):
+    """The RMS-scaled allclose bound of assert_close, or, where it fails, the error
+    bf16 storage alone forces as the bound.
+
+    emu is the oracle's arithmetic with every GEMM operand and cache entry stored as
+    bf16 (tests/_bf16_emulation.py).  Through many layers, or through one layer whose
+    activations are large (the 34B and 70B shapes), that unavoidable error exceeds the
+    fixed bound; the kernel's error must then stay within rms_factor times the
+    emulation's RMS error over the tensor and within max_factor times its largest
+    element's error (the extreme of millions of rounding errors is the noisier
+    statistic, so it gets the wider factor)."""
+    try:
+        assert_close(got, ref, atol, rtol, what=what, rms_scaled=True)
+        return "allclose"
+    except AssertionError as strict_fail:
+        g_max, g_rms = error_stats(got, ref)
+        e_max, e_rms = error_stats(emu, ref)
+        assert np.all(np.isfinite(np.asarray(got, np.float64))), f"{what}: non-finite values"
+        assert g_max <= max_factor * e_max and g_rms <= rms_factor * e_rms, (
+            f"{what}: beyond the allclose bound ({strict_fail}) and beyond the bf16-storage error "
+            f"(x{rms_factor} RMS, x{max_factor} max): "
+            f"max {g_max:.4g} vs {e_max:.4g}, RMS {g_rms:.4g} vs {e_rms:.4g}")
+        return f"bf16 floor: max {g_max:.4g} vs {e_max:.4g}, RMS {g_rms:.4g} vs {e_rms:.4g}"
+
+
+def oracle_layer_rows(x, W, spec, rows, Kc, Vc, smp, kv_projection=O.kv_projection, layer=O.layer_forward):
+    """One layer of recompute for the rows x at cache rows `rows`, output only for the
+    subset `smp` (indices into x): every row's fresh K/V is written into the cache first
+    (kv_projection), then the layer runs on the subset over that cache.  Rows do not
+    interact except through the cache, so the subset's outputs are those of the whole
+    layer.  Kc / Vc are updated in place."""
+    k, v = kv_projection(x, W, spec, rows)
+    Kc[rows] = k
+    Vc[rows] = v
+    return layer(x[smp], W, spec, rows[smp], rows[smp], Kc, Vc)

@@ -30,16 +30,18 @@ def world(M):
     dm = M.DeviceModel(weights, DEV, max_pos=256)
     om = O.OracleModel(weights)
     store = M.ChunkStore(dm, req.crit_layer, req.n_anchor)
+    kv = {}
     for c in range(4):
         t = qd.chunk_tokens(c, req.chunk_len, spec.vocab)
-        k = O.chunk_precompute(om, t)
+        k = kv[c] = O.chunk_precompute(om, t)
         store.add_precomputed(c, t, torch.from_numpy(k["K"]).to(torch.bfloat16), torch.from_numpy(k["V"]).to(torch.bfloat16))
     # chunk id 10 carries chunk 1's tokens: the content-keyed store maps it to the same stored chunk
     store.add_precomputed(10, qd.chunk_tokens(1, req.chunk_len, spec.vocab),
                           torch.zeros((spec.n_layers, req.chunk_len, spec.n_kv_heads, spec.head_dim), dtype=torch.bfloat16),
                           torch.zeros((spec.n_layers, req.chunk_len, spec.n_kv_heads, spec.head_dim), dtype=torch.bfloat16))
     assert store.chunks[10] is store.chunks[1]
-    return dict(spec=spec, req=req, dm=dm, store=store)
+    kv[10] = kv[1]
+    return dict(spec=spec, req=req, dm=dm, store=store, om=om, kv=kv)
 
 
 def _requests(M, w, kinds):
@@ -100,3 +102,36 @@ def test_batch_equals_requests_alone(M, world, kinds):
     assert h2d == want
     sequential = sum(len(s) for s in ids) * chunk_layer * 2 * spec.n_layers
     assert h2d < sequential
+
+
+def test_batch_matches_the_oracle_per_request(M, world):
+    """Each request of a batch against the oracle's fused prefill of that request alone, with
+    the shared chunks at different offsets in the two requests (chunk 2 is third in one and
+    first in the other; chunk id 10 is chunk 1's content in second place).  Selections are
+    the oracle's, forced, so every output can be compared element by element."""
+    from _parity import assert_close
+    w = world
+    spec, req = w["spec"], w["req"]
+    sets = [[0, 1, 2], [2, 10, 3]]
+    refs, batch = [], []
+    for i, ids in enumerate(sets):
+        q = qd.query_tokens(i, req.query_len, spec.vocab)
+        toks = np.concatenate([qd.chunk_tokens(1 if c == 10 else c, req.chunk_len, spec.vocab) for c in ids])
+        start = np.arange(len(ids) + 1) * req.chunk_len
+        ref = O.fused_prefill(w["om"], [w["kv"][c] for c in ids], toks, start, q, req.crit_layer, req.ratio_bp,
+                              req.n_anchor)
+        refs.append(ref)
+        batch.append(M.FusedRequest(w["dm"], w["store"], ids, q, req.ratio_bp, forced_sel=ref["sel"]))
+    cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
+    M.run_batch(batch, cs, xs)
+    torch.cuda.synchronize()
+    tol = dict(atol=2e-2, rtol=2e-2, rms_scaled=True)
+    for i, (fr, ref) in enumerate(zip(batch, refs)):
+        assert np.array_equal(np.sort(fr.selected.cpu().numpy()), ref["sel"])
+        assert_close(fr.q_crit.float().cpu().numpy(), ref["q_crit"], what=f"request {i} q_crit", **tol)
+        assert_close(fr.scores.cpu().numpy(), ref["scores"], atol=2e-2, rtol=2e-2, what=f"request {i} scores")
+        for l in range(spec.n_layers):
+            assert_close(fr.K[l].float().cpu().numpy(), ref["K"][l], what=f"request {i} K layer {l}", **tol)
+            assert_close(fr.V[l].float().cpu().numpy(), ref["V"][l], what=f"request {i} V layer {l}", **tol)
+        assert_close(fr.x_rows.cpu().numpy(), ref["x"], what=f"request {i} recomputed rows", **tol)
+        assert_close(fr.logits.cpu().numpy(), ref["logits"], what=f"request {i} logits", **tol)

@@ -81,3 +81,53 @@ def test_recorded_traffic_follows_the_sources():
     else:
         assert got is None
     assert bench.recorded_traffic("no_such_kernel") is None
+
+
+def test_per_device_setup_runs_once_for_each_device(tmp_path):
+    """Kernel attributes (the dynamic shared-memory limit) and symbol addresses belong to
+    one device: the library's set-up helper must run once per device, keep each device's
+    result apart, and survive concurrent first calls.  Compiled from the library's own
+    header with the host compiler and driven with fake device indices (no GPU)."""
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("no host C++ compiler")
+    hdr = os.path.join(ROOT, "rag_kv_cache_re_gb300", "csrc")
+    src = tmp_path / "per_device_test.cpp"
+    src.write_text(r'''
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <thread>
+#include <vector>
+#include "per_device.h"
+int main() {
+  qcf::PerDevice<int> pd;
+  std::atomic<int> calls[4] = {};
+  std::vector<std::thread> th;
+  for (int t = 0; t < 16; ++t)
+    th.emplace_back([&, t] {
+      const int dev = t % 3;
+      for (int k = 0; k < 100; ++k) {
+        const int v = pd.get(dev, [&] { calls[dev]++; return 100 + dev; });
+        if (v != 100 + dev) { std::printf("wrong value %d on device %d\n", v, dev); std::_Exit(2); }
+      }
+    });
+  for (auto& x : th) x.join();
+  for (int d = 0; d < 3; ++d)
+    if (calls[d] != 1) { std::printf("device %d set up %d times\n", d, calls[d].load()); return 3; }
+  int uncached = 0;   // an unreadable device (-1) is never cached
+  pd.get(-1, [&] { return ++uncached; });
+  pd.get(-1, [&] { return ++uncached; });
+  if (uncached != 2) return 4;
+  // device 7 first: the table grows, earlier devices keep their values
+  if (pd.get(7, [] { return 7; }) != 7 || pd.get(1, [] { return -1; }) != 101) return 5;
+  std::puts("ok");
+  return 0;
+}
+''')
+    exe = tmp_path / "per_device_test"
+    subprocess.run([gxx, "-std=c++17", "-O1", "-pthread", "-I", hdr, str(src), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr

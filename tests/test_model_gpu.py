@@ -131,7 +131,14 @@ def _check_fused(w, fr, ref):
         assert int(fr.token.item()) == ref["token"] == int(fr.token_host.item())
 
 
-def test_tiny_request_anchors_and_probe(M, Q, tiny_world):
+def _streams(two):
+    """One stream (copies and compute in order) or two (the layer copies and re-rotations on
+    a copy stream, ordered against the compute stream by events only)."""
+    return (torch.cuda.Stream(), torch.cuda.Stream()) if two else (None, None)
+
+
+@pytest.mark.parametrize("two_streams", [False, True], ids=["one_stream", "two_streams"])
+def test_tiny_request_anchors_and_probe(M, Q, tiny_world, two_streams):
     w = tiny_world
     ref = _oracle_fused(w, w["req"].ratio_bp)
     for c in w["ids"]:
@@ -139,7 +146,7 @@ def test_tiny_request_anchors_and_probe(M, Q, tiny_world):
         nrm = np.sqrt(np.sum(Kc.reshape(Kc.shape[0], -1) ** 2, axis=1))
         assert_same_selection(w["store"].chunks[c].anchor_idx, nrm, w["req"].n_anchor, 1e-5 * nrm.max(), "anchors")
     fr = M.FusedRequest(w["dm"], w["store"], w["ids"], w["query"], w["req"].ratio_bp)
-    fr.run()
+    fr.run(*_streams(two_streams))
     torch.cuda.synchronize()
     assert Q.qcf_query_status() == 0
     assert_close(f32(fr.q_crit), ref["q_crit"], what="q_crit", **TOL)
@@ -154,22 +161,24 @@ def test_tiny_request_anchors_and_probe(M, Q, tiny_world):
         _check_fused(w, fr, ref)
 
 
-def test_tiny_request_forced_selection(M, Q, tiny_world):
+@pytest.mark.parametrize("two_streams", [False, True], ids=["one_stream", "two_streams"])
+def test_tiny_request_forced_selection(M, Q, tiny_world, two_streams):
     w = tiny_world
     ref = _oracle_fused(w, w["req"].ratio_bp)
     fr = M.FusedRequest(w["dm"], w["store"], w["ids"], w["query"], w["req"].ratio_bp, forced_sel=ref["sel"])
-    fr.run(ids_from_host=True)
+    fr.run(*_streams(two_streams), ids_from_host=True)
     torch.cuda.synchronize()
     assert np.array_equal(np.sort(fr.selected.cpu().numpy()), ref["sel"])
     _check_fused(w, fr, ref)
 
 
+@pytest.mark.parametrize("two_streams", [False, True], ids=["one_stream", "two_streams"])
 @pytest.mark.parametrize("ratio_bp", [0, 10000])
-def test_tiny_request_special_ratios(M, Q, tiny_world, ratio_bp):
+def test_tiny_request_special_ratios(M, Q, tiny_world, ratio_bp, two_streams):
     w = tiny_world
     ref = _oracle_fused(w, ratio_bp)
     fr = M.FusedRequest(w["dm"], w["store"], w["ids"], w["query"], ratio_bp)
-    fr.run()
+    fr.run(*_streams(two_streams))
     torch.cuda.synchronize()
     assert fr.N == ref["N"]
     _check_fused(w, fr, ref)

@@ -4,8 +4,9 @@ Some callers have no device allocator available when they need the scores (a
 serving loop whose free memory all went to its KV-cache pool, or a fixed memory
 budget that forbids cudaMalloc on the request path).  The no-allocation entry
 point runs the same kernels with a fixed device array as scratch.  This test
-calls it through the C ABI twice in a row, on different shapes, and compares
-each result with qcf_profile_scores run with a caller workspace.  It also checks
+calls it through the C ABI three times in a row, on different shapes, and
+checks each result is bit for bit what qcf_profile_scores gives with a caller
+workspace.  It also checks
 that a shape needing more scratch than the fixed array is refused up front.
 """
 import ctypes as C
@@ -15,7 +16,6 @@ import pytest
 import torch
 
 import qcfdata as qd
-from _parity import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -30,18 +30,37 @@ def _noalloc(lib, q, K, scale):
     return st, out
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+def _with_dirty_workspace(lib, q, K, scale):
+    """qcf_profile_scores through the C ABI with a caller workspace that starts full of NaN bytes."""
+    nq, Hq, D = q.shape
+    Cn, Hkv, _ = K.shape
+    nb = lib.qcf_profile_scores_workspace_size(nq, Cn, Hq, Hkv, D)
+    ws = torch.full((max(256, nb),), 0xFF, dtype=torch.uint8, device=q.device)
+    out = torch.full((Cn,), float("nan"), dtype=torch.float32, device=q.device)
+    st = lib.qcf_profile_scores(C.c_void_p(q.data_ptr()), C.c_void_p(K.data_ptr()), nq, Cn, Hq, Hkv, D,
+                                C.c_float(scale), C.c_void_p(out.data_ptr()), C.c_void_p(ws.data_ptr()),
+                                C.c_size_t(ws.numel()), C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, lib.qcf_last_error()
+    return out
+
+
+def test_noalloc_matches_workspace_entry_point_bitwise():
+    """Three calls in a row, the largest scratch footprint first: a later, smaller call that
+    read anything the earlier call left in the shared array would differ from the
+    workspace entry point, whose own workspace starts full of NaN bytes."""
     from rag_kv_cache_re_gb300 import _lib, qcf as Q
     lib = _lib.lib()
-    cases = [dict(C=5120, nq=64, Hq=32, Hkv=8, D=128, scale=1.0 / np.sqrt(128)),   # the 8B request's profile
-             dict(C=1000, nq=8, Hq=4, Hkv=4, D=16, scale=0.25)]                     # a smaller second call
+    cases = [dict(C=131072, nq=64, Hq=32, Hkv=8, D=128, scale=1.0),                 # 128k-token sweep context
+             dict(C=5120, nq=64, Hq=32, Hkv=8, D=128, scale=1.0 / np.sqrt(128)),   # the 8B request's profile
+             dict(C=1000, nq=8, Hq=4, Hkv=4, D=16, scale=0.25)]                     # a small ragged call
     for i, c in enumerate(cases):
         t = qd.sweep_tensors(c["C"], n_query=c["nq"], Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"], seed=100 + i, device="cuda")
         st, got = _noalloc(lib, t["Q"], t["K"], c["scale"])
         assert st == 0, lib.qcf_last_error()
-        ref = Q.qcf_profile_scores(t["Q"], t["K"], c["scale"])
+        ref = _with_dirty_workspace(lib, t["Q"], t["K"], c["scale"])
         torch.cuda.synchronize()
-        assert_close(got.cpu().numpy(), ref.cpu().numpy(), atol=1e-3, rtol=1e-3, what=f"call {i + 1}")
+        assert torch.equal(got, ref), f"call {i + 1}: differs from the workspace entry point"
+        assert abs(got.double().sum().item() - c["Hq"] * c["nq"]) < 1e-3 * c["Hq"] * c["nq"]
     assert Q.qcf_query_status() == 0
 
 
