@@ -399,9 +399,11 @@ using namespace qcf;
 
 extern "C" {
 
+static bool use_tc_profile(int Hq, int Hkv, int D) { return D == 128 && Hq / Hkv <= kProfileTcMaxGroup; }
+
 size_t qcf_profile_scores_workspace_size(int nq, int C, int Hq, int Hkv, int D) {
-  (void)D;
   if (nq <= 0 || C <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return 0;
+  if (use_tc_profile(Hq, Hkv, D)) return profile_tc_workspace_size(nq, C, Hq, Hkv);
   const ProfilePlan p = plan_profile(nq, C, Hq, Hkv);
   return p.stats_bytes + p.fstats_bytes + p.part_bytes;
 }
@@ -411,6 +413,8 @@ qcf_status qcf_profile_scores(const qcf_bf16* q, const qcf_bf16* K, int nq, int 
   if (!q || !K || !scores || !ws) return set_error(QCF_ERR_INVALID_ARG, "qcf_profile_scores: NULL pointer");
   if (nq <= 0 || C <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || (D != 16 && D != 64 && D != 128))
     return set_error(QCF_ERR_SHAPE, "qcf_profile_scores: nq=%d C=%d Hq=%d Hkv=%d D=%d", nq, C, Hq, Hkv, D);
+  if (!(scale > 0.f) || !isfinite(scale))
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_profile_scores: scale must be positive and finite");
   if (take_fault(4) || !aligned16(q) || !aligned16(K) || !aligned16(scores) || !aligned16(ws))
     return set_error(QCF_ERR_ALIGN, "qcf_profile_scores: pointers must be 16-byte aligned");
   if (take_fault(2) || ws_bytes < qcf_profile_scores_workspace_size(nq, C, Hq, Hkv, D))
@@ -419,6 +423,7 @@ qcf_status qcf_profile_scores(const qcf_bf16* q, const qcf_bf16* K, int nq, int 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* qq = reinterpret_cast<const __nv_bfloat16*>(q);
   const __nv_bfloat16* kk = reinterpret_cast<const __nv_bfloat16*>(K);
+  if (use_tc_profile(Hq, Hkv, D)) return profile_tc_launch(qq, kk, nq, C, Hq, Hkv, scale, scores, ws, st);
   switch (D) {
     case 16: return profile_launch_d<16>(qq, kk, nq, C, Hq, Hkv, scale, scores, ws, st);
     case 64: return profile_launch_d<64>(qq, kk, nq, C, Hq, Hkv, scale, scores, ws, st);
@@ -431,6 +436,8 @@ qcf_status qcf_profile_scores_noalloc(const qcf_bf16* q, const qcf_bf16* K, int 
   if (!q || !K || !scores) return set_error(QCF_ERR_INVALID_ARG, "qcf_profile_scores_noalloc: NULL pointer");
   if (nq <= 0 || C <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || (D != 16 && D != 64 && D != 128))
     return set_error(QCF_ERR_SHAPE, "qcf_profile_scores_noalloc: nq=%d C=%d Hq=%d Hkv=%d D=%d", nq, C, Hq, Hkv, D);
+  if (!(scale > 0.f) || !isfinite(scale))
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_profile_scores_noalloc: scale must be positive and finite");
   if (!aligned16(q) || !aligned16(K) || !aligned16(scores))
     return set_error(QCF_ERR_ALIGN, "qcf_profile_scores_noalloc: pointers must be 16-byte aligned");
   const size_t need = qcf_profile_scores_workspace_size(nq, C, Hq, Hkv, D);
@@ -445,6 +452,7 @@ qcf_status qcf_profile_scores_noalloc(const qcf_bf16* q, const qcf_bf16* K, int 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* qq = reinterpret_cast<const __nv_bfloat16*>(q);
   const __nv_bfloat16* kk = reinterpret_cast<const __nv_bfloat16*>(K);
+  if (use_tc_profile(Hq, Hkv, D)) return profile_tc_launch(qq, kk, nq, C, Hq, Hkv, scale, scores, scratch, cs);
   switch (D) {
     case 16: return profile_launch_d<16>(qq, kk, nq, C, Hq, Hkv, scale, scores, scratch, cs);
     case 64: return profile_launch_d<64>(qq, kk, nq, C, Hq, Hkv, scale, scores, scratch, cs);

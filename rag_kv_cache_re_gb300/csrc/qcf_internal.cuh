@@ -48,6 +48,11 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                     CUtensorMapSwizzle swizzle, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
+// Rank-3 tiled map: dims innermost first, strides of dims 1 and 2 in bytes.
+bool encode_tmap_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const uint64_t strides_bytes[2],
+                    const uint32_t box[3], CUtensorMapSwizzle swizzle,
+                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Device SM count (cached per device).
@@ -125,6 +130,12 @@ cudaError_t launch_kv_deviation(const __nv_bfloat16* k_new, const __nv_bfloat16*
                                 const __nv_bfloat16* K, const __nv_bfloat16* V, int T, int width, float* dev,
                                 cudaStream_t st);
 
+// Critical-layer profiling on tcgen05 for head dim 128 (profile_tc.cu).
+size_t profile_tc_workspace_size(int nq, int C, int Hq, int Hkv);
+qcf_status profile_tc_launch(const __nv_bfloat16* q, const __nv_bfloat16* K, int nq, int C, int Hq, int Hkv,
+                             float scale, float* scores, void* ws, cudaStream_t st);
+constexpr int kProfileTcMaxGroup = 16;  // heads per KV head served by the tensor-core profile
+
 // Attention internals (attention.cu).
 size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D);
 qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,
@@ -150,6 +161,17 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Named barrier `id` over `count` threads that also returns whether any of them passed true.
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ void flag_status(unsigned int* st, unsigned int bits) {
@@ -194,6 +216,13 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
       ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 // Untiled bulk copies (cp.async.bulk): addresses 16-byte aligned, size a multiple of 16.

@@ -86,6 +86,12 @@ def test_anchor_keynorm_topk(Q, D, Hkv, lens, A):
     (5120, 64, 32, 8, 128, 1.0 / math.sqrt(128)),  # 8B request shape
     (16384, 64, 32, 8, 128, 1.0),  # sweep 16k
     (2000, 128, 56, 8, 128, 1.0),  # 34B head layout (7 heads per KV head, 4 row groups)
+    (3000, 64, 64, 8, 128, 1.0),   # 70B head layout (8 heads per KV head, 2 row groups)
+    (129, 50, 32, 8, 128, 1.0),    # ragged keys, a partial row tile
+    (1, 64, 32, 8, 128, 1.0),      # a single key
+    (777, 100, 8, 8, 128, 1.0),    # no grouping: one row tile of 100 rows
+    (1500, 20, 128, 8, 128, 1.0),  # 16 heads per KV head: 3 row tiles, the second group has one
+    (4096, 64, 32, 8, 128, 8.0),   # a sharp softmax (a few keys carry each row)
 ])
 def test_profile_scores(Q, C, nq, Hq, Hkv, D, scale):
     t = qd.sweep_tensors(C, n_query=nq, Hq=Hq, Hkv=Hkv, D=D, device=DEV)
