@@ -589,7 +589,9 @@ def run_kernel(args):
     """Repeats one hot kernel on its bench shape (the target of the committed ncu captures):
     gate_up -- one 8B-shaped decoder layer over 832 recomputed rows of a 5184-row cache (its
     third GEMM launch is the gate/up projection with the SwiGLU epilogue);
-    attention -- sparse causal attention at the 16k-context, 20 %-selected sweep point."""
+    attention -- sparse causal attention at the 16k-context, 20 %-selected sweep point;
+    profile -- critical-layer profiling at the 128k-context sweep point (64 query rows);
+    topn -- top-N of the 128k profile scores at 15 %."""
     import dataclasses
     from rag_kv_cache_re_gb300 import model as M
     from rag_kv_cache_re_gb300 import qcf as Q
@@ -606,6 +608,13 @@ def run_kernel(args):
         K = qd.normal_bf16((C + Qn, spec.n_kv_heads, spec.head_dim), 1.0, 71, "cuda")
         V = qd.normal_bf16((C + Qn, spec.n_kv_heads, spec.head_dim), 1.0, 72, "cuda")
         fn = lambda: Q.qcf_fused_layer_forward(dm, 0, x0.clone(), rows, rows, K, V)
+    elif args.kernel in ("profile", "topn"):
+        t = qd.sweep_tensors(131072, device="cuda")
+        if args.kernel == "profile":
+            fn = lambda: Q.qcf_profile_scores(t["Q"], t["K"], 1.0)
+        else:
+            sc = Q.qcf_profile_scores(t["Q"], t["K"], 1.0)
+            fn = lambda: Q.qcf_topn_select(sc, (1500 * 131072 + 9999) // 10000)
     else:
         Hq, Hkv, D = qd.SWEEP_HEADS
         C, N = 16384, 3277
@@ -633,7 +642,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-selectors", action="store_true", help="skip timing the QCLast, QCAll and HKVD variants")
     ap.add_argument("--sweep", action="store_true", help="time the kernel-sweep shapes instead of the request")
-    ap.add_argument("--kernel", choices=["gate_up", "attention"], help="repeat one hot kernel (for ncu captures)")
+    ap.add_argument("--kernel", choices=["gate_up", "attention", "profile", "topn"],
+                    help="repeat one hot kernel (for ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

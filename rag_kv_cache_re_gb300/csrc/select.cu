@@ -105,102 +105,281 @@ __global__ void __launch_bounds__(256) anchor_keynorm_kernel(const __nv_bfloat16
   }
 }
 
-// Exact top-N in one CTA of 1024 threads.
-// (1) Radix select, 8 bits at a time from the top, finds the key K* of the N-th
-//     largest value and `need`, how many elements equal to K* are taken.
-// (2) Compaction in index order: an element is selected if key > K*, or if key == K*
-//     and fewer than `need` equal keys precede it.  Output is ascending.
+// ------------------------------------------------------------------ top-N
+//
+// Exact top-N in one CTA of 1024 threads, ties to the lower index, output ascending.
+// Keys are the fp32 bit patterns mapped to an order-preserving unsigned integer; K* is
+// the N-th largest key and `need` how many keys equal to K* are taken (the lowest
+// indices among them).
+//   A  histogram passes over the scores, 11, 11 and 10 key bits from the top, each
+//      restricted to the bucket chosen so far, until the bucket holding the N-th largest
+//      key has at most kTopnCap keys (one pass for most score distributions; for
+//      C <= kTopnCap none: every score is a candidate)
+//   B  one more pass appends that bucket's keys, with their indices, to a candidate list
+//      in shared memory
+//   R  in shared memory: the remaining key bits give K* and `need`; two 12-bit rounds
+//      over the indices of the K*-valued candidates give idx*, the largest index taken
+//   C  a last pass writes, in index order, every j with key > K* or (key == K* and
+//      j <= idx*): a block-wide scan per 4096 scores
+// When all 32 bits are fixed and more than kTopnCap keys still equal K*, the last pass
+// instead ranks the K*-valued keys in index order with the same block-wide scans.
 constexpr int kTopnThreads = 1024;
-__global__ void __launch_bounds__(kTopnThreads) topn_kernel(const float* __restrict__ scores, int C, int N,
-                                                            int32_t* __restrict__ sel) {
-  __shared__ unsigned int hist[32][256];
-  __shared__ unsigned int tot[256];
-  __shared__ unsigned int s_prefix, s_need;
-  __shared__ unsigned int wsum_a[32], wsum_b[32];
+constexpr int kTopnCap = 16384;                               // candidates held in shared memory
+constexpr int kTopnSmem = 2 * kTopnCap * 4 + 4096 * 4;       // keys, indices, one 4096-bin histogram
+
+__device__ __forceinline__ unsigned int topn_scan_excl(unsigned int v, unsigned int* wsum, unsigned int* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  unsigned int prefix = 0u, mask = 0u, need = static_cast<unsigned int>(N);
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 32 * 256; i += kTopnThreads) (&hist[0][0])[i] = 0u;
-    __syncthreads();
-    for (int base = 0; base < C; base += kTopnThreads) {
-      const int j = base + threadIdx.x;
-      const bool valid = j < C;
-      const unsigned int k = valid ? order_key(scores[j]) : 0u;
-      const bool part = valid && ((k & mask) == prefix);
-      const unsigned int digit = (k >> shift) & 255u;
-      // warp-aggregated increment: one atomic per distinct digit in the warp
-      const unsigned int peers = __match_any_sync(0xffffffffu, part ? digit : 0x100u);
-      if (part && (__ffs(peers) - 1) == lane) atomicAdd(&hist[wid][digit], __popc(peers));
-    }
-    __syncthreads();
-    if (threadIdx.x < 256) {
-      unsigned int t = 0u;
-      for (int w = 0; w < 32; ++w) t += hist[w][threadIdx.x];
-      tot[threadIdx.x] = t;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned int cum = 0u;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (cum + tot[d] >= need) break;
-        cum += tot[d];
-      }
-      s_prefix = prefix | (static_cast<unsigned int>(d) << shift);
-      s_need = need - cum;
-    }
-    __syncthreads();
-    prefix = s_prefix;
-    need = s_need;
-    mask |= 255u << shift;
-    __syncthreads();
+  unsigned int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  // prefix == K*, need = number of K*-valued elements to take (lowest indices first)
-  unsigned int eq_seen = 0u, out_seen = 0u;
-  for (int base = 0; base < C; base += kTopnThreads) {
-    const int j = base + threadIdx.x;
-    const bool valid = j < C;
-    const unsigned int k = valid ? order_key(scores[j]) : 0u;
-    const bool gt = valid && k > prefix;
-    const bool eq = valid && k == prefix;
-    const unsigned int eq_b = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) wsum_a[wid] = __popc(eq_b);
-    __syncthreads();
-    if (wid == 0) {   // exclusive scan of per-warp equal counts
-      const unsigned int v = wsum_a[lane];
-      unsigned int x = v;
+  if (lane == 31) wsum[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    const unsigned int w = wsum[lane];
+    unsigned int z = w;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
+    }
+    wsum[lane] = z - w;
+    if (lane == 31) wsum[32] = z;
+  }
+  __syncthreads();
+  const unsigned int r = wsum[wid] + x - v;
+  *total = wsum[32];
+  __syncthreads();
+  return r;
+}
+
+// The bin holding the need-th element counted from the top bin down (desc) or from bin 0
+// up (asc): out = {bin, elements still needed from it, the bin's count}.
+// nbins in {1024, 2048, 4096}.
+__device__ void topn_pick_bin(const unsigned int* h, int nbins, bool desc, unsigned int need, unsigned int* wsum,
+                              unsigned int* out) {
+  const int k = nbins / kTopnThreads;
+  const int p0 = threadIdx.x * k;
+  unsigned int local = 0u;
+  for (int i = 0; i < k; ++i) local += h[desc ? nbins - 1 - (p0 + i) : p0 + i];
+  unsigned int tot;
+  unsigned int before = topn_scan_excl(local, wsum, &tot);
+  if (before < need && need <= before + local) {
+    for (int i = 0; i < k; ++i) {
+      const int bin = desc ? nbins - 1 - (p0 + i) : p0 + i;
+      const unsigned int c = h[bin];
+      if (before + c >= need) {
+        out[0] = static_cast<unsigned int>(bin);
+        out[1] = need - before;
+        out[2] = c;
+        break;
       }
-      wsum_a[lane] = x - v;
-      if (lane == 31) wsum_b[0] = x;   // tile total of equals (temporarily)
+      before += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Sixteen consecutive scores from j0 as keys; keys past C are reported by the count n
+// (all loads are issued before any key is used, so a thread keeps four in flight).
+constexpr int kTopnPer = 16;
+__device__ __forceinline__ void topn_load16(const float* __restrict__ s, int j0, int C, unsigned int* k, int* n) {
+  if (j0 + kTopnPer <= C) {
+    const float4* p = reinterpret_cast<const float4*>(s + j0);
+    float4 f[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) f[u] = __ldg(p + u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      k[4 * u] = order_key(f[u].x);
+      k[4 * u + 1] = order_key(f[u].y);
+      k[4 * u + 2] = order_key(f[u].z);
+      k[4 * u + 3] = order_key(f[u].w);
+    }
+    *n = kTopnPer;
+  } else {
+    const int m = max(0, C - j0);
+#pragma unroll
+    for (int e = 0; e < kTopnPer; ++e) k[e] = e < m ? order_key(s[j0 + e]) : 0u;
+    *n = m;
+  }
+}
+
+__device__ __forceinline__ int topn_level_shift(int lv) { return lv == 0 ? 21 : (lv == 1 ? 10 : 0); }
+__device__ __forceinline__ int topn_level_bins(int lv) { return lv == 2 ? 1024 : 2048; }
+
+__global__ void __launch_bounds__(kTopnThreads, 1) topn_kernel(const float* __restrict__ scores, int C, int N,
+                                                            int32_t* __restrict__ sel) {
+  extern __shared__ __align__(16) unsigned int tsm[];
+  unsigned int* ckey = tsm;                                 // [kTopnCap] candidate keys
+  int* cidx = reinterpret_cast<int*>(tsm + kTopnCap);       // [kTopnCap] candidate indices
+  unsigned int* h = tsm + 2 * kTopnCap;                     // [4096] histogram
+  unsigned int* hist8 = tsm;                                // passes A: [8][2048] over the candidate list
+  __shared__ unsigned int wsum[33];
+  __shared__ unsigned int pick[3];
+  __shared__ unsigned int s_cnt;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  unsigned int need = static_cast<unsigned int>(N);
+  unsigned int prefix = 0u, fmask = 0u;  // key bits fixed so far
+  int lv = 0;
+  int n_c = C;
+  const bool all_in_smem = C <= kTopnCap;
+  if (all_in_smem) {
+    for (int j = tid; j < C; j += kTopnThreads) {
+      ckey[j] = order_key(scores[j]);
+      cidx[j] = j;
     }
     __syncthreads();
-    const unsigned int eq_rank = eq_seen + wsum_a[wid] + __popc(eq_b & ((1u << lane) - 1u));
-    const unsigned int eq_tile = wsum_b[0];
-    const bool take = gt || (eq && eq_rank < need);
-    const unsigned int tk_b = __ballot_sync(0xffffffffu, take);
-    __syncthreads();
-    if (lane == 0) wsum_a[wid] = __popc(tk_b);
-    __syncthreads();
-    if (wid == 0) {
-      const unsigned int v = wsum_a[lane];
-      unsigned int x = v;
+  } else {
+    // ---- A: narrow to a bucket of at most kTopnCap keys
+    unsigned int bucket = 0u;
+    while (true) {
+      const int shift = topn_level_shift(lv), nb = topn_level_bins(lv);
+      for (int i = tid; i < 8 * 2048; i += kTopnThreads) hist8[i] = 0u;
+      __syncthreads();
+      unsigned int* myh = hist8 + (wid & 7) * 2048;
+      for (int base = 0; base < C; base += kTopnPer * kTopnThreads) {
+        unsigned int k[kTopnPer];
+        int n;
+        topn_load16(scores, base + kTopnPer * tid, C, k, &n);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        for (int e = 0; e < kTopnPer; ++e)
+          if (e < n && (k[e] & fmask) == prefix) atomicAdd(&myh[(k[e] >> shift) & (nb - 1)], 1u);
       }
-      wsum_a[lane] = x - v;
-      if (lane == 31) wsum_b[1] = x;
+      __syncthreads();
+      for (int b = tid; b < nb; b += kTopnThreads) {
+        unsigned int t = 0u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) t += hist8[c * 2048 + b];
+        h[b] = t;
+      }
+      __syncthreads();
+      topn_pick_bin(h, nb, true, need, wsum, pick);
+      prefix |= pick[0] << shift;
+      fmask |= static_cast<unsigned int>(nb - 1) << shift;
+      need = pick[1];
+      bucket = pick[2];
+      ++lv;
+      if (bucket <= static_cast<unsigned int>(kTopnCap) || lv == 3) break;
+    }
+    if (bucket > static_cast<unsigned int>(kTopnCap)) {
+      // ---- every key bit is fixed and too many keys equal K*: rank them in index order
+      const unsigned int kstar = prefix;
+      unsigned int out = 0u, eq_seen = 0u;
+      for (int base = 0; base < C; base += kTopnPer * kTopnThreads) {
+        const int j0 = base + kTopnPer * tid;
+        unsigned int k[kTopnPer];
+        int n;
+        topn_load16(scores, j0, C, k, &n);
+        unsigned int n_eq = 0u;
+#pragma unroll
+        for (int e = 0; e < kTopnPer; ++e) n_eq += (e < n && k[e] == kstar) ? 1u : 0u;
+        unsigned int eq_tot;
+        unsigned int r = eq_seen + topn_scan_excl(n_eq, wsum, &eq_tot);
+        unsigned int fbits = 0u;
+#pragma unroll
+        for (int e = 0; e < kTopnPer; ++e) {
+          const bool eq = e < n && k[e] == kstar;
+          if ((e < n && k[e] > kstar) || (eq && r < need)) fbits |= 1u << e;
+          r += eq ? 1u : 0u;
+        }
+        unsigned int tot;
+        unsigned int pos = out + topn_scan_excl(__popc(fbits), wsum, &tot);
+#pragma unroll
+        for (int e = 0; e < kTopnPer; ++e)
+          if (((fbits >> e) & 1u) && pos < static_cast<unsigned int>(N)) sel[pos++] = j0 + e;
+        out += tot;
+        eq_seen += eq_tot;
+      }
+      return;
+    }
+    // ---- B: that bucket's keys, with their indices, into the candidate list
+    if (tid == 0) s_cnt = 0u;
+    __syncthreads();
+    for (int base = 0; base < C; base += kTopnPer * kTopnThreads) {
+      unsigned int k[kTopnPer];
+      int n;
+      topn_load16(scores, base + kTopnPer * tid, C, k, &n);
+#pragma unroll
+      for (int e = 0; e < kTopnPer; ++e) {
+        const bool m = e < n && (k[e] & fmask) == prefix;
+        const unsigned int bal = __ballot_sync(0xffffffffu, m);
+        if (bal) {
+          const int leader = __ffs(bal) - 1;
+          unsigned int b0 = 0u;
+          if (lane == leader) b0 = atomicAdd(&s_cnt, static_cast<unsigned int>(__popc(bal)));
+          b0 = __shfl_sync(0xffffffffu, b0, leader);
+          if (m) {
+            const unsigned int pos = b0 + __popc(bal & ((1u << lane) - 1u));
+            if (pos < static_cast<unsigned int>(kTopnCap)) {
+              ckey[pos] = k[e];
+              cidx[pos] = base + kTopnPer * tid + e;
+            }
+          }
+        }
+      }
     }
     __syncthreads();
-    if (take) sel[out_seen + wsum_a[wid] + __popc(tk_b & ((1u << lane) - 1u))] = j;
-    eq_seen += eq_tile;
-    out_seen += wsum_b[1];
+    n_c = min(static_cast<int>(s_cnt), kTopnCap);
+  }
+  // ---- R: the remaining key bits over the candidates give K* and `need`
+  for (; lv < 3; ++lv) {
+    const int shift = topn_level_shift(lv), nb = topn_level_bins(lv);
+    for (int i = tid; i < nb; i += kTopnThreads) h[i] = 0u;
     __syncthreads();
+    for (int i = tid; i < n_c; i += kTopnThreads) {
+      const unsigned int key = ckey[i];
+      if ((key & fmask) == prefix) atomicAdd(&h[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    topn_pick_bin(h, nb, true, need, wsum, pick);
+    prefix |= pick[0] << shift;
+    fmask |= static_cast<unsigned int>(nb - 1) << shift;
+    need = pick[1];
+  }
+  const unsigned int kstar = prefix;
+  // ---- the need-th smallest index among the K*-valued candidates (C <= 2^24)
+  unsigned int ip = 0u, im = 0u;
+  for (int il = 0; il < 2; ++il) {
+    const int shift = il == 0 ? 12 : 0;
+    for (int i = tid; i < 4096; i += kTopnThreads) h[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n_c; i += kTopnThreads) {
+      const unsigned int idx = static_cast<unsigned int>(cidx[i]);
+      if (ckey[i] == kstar && (idx & im) == ip) atomicAdd(&h[(idx >> shift) & 4095u], 1u);
+    }
+    __syncthreads();
+    topn_pick_bin(h, 4096, false, need, wsum, pick);
+    ip |= pick[0] << shift;
+    im |= 4095u << shift;
+    need = pick[1];
+  }
+  const unsigned int idx_star = ip;
+  // ---- C: every j with key > K*, or key == K* and j <= idx*, in index order
+  unsigned int out = 0u;
+  for (int base = 0; base < C; base += kTopnPer * kTopnThreads) {
+    const int j0 = base + kTopnPer * tid;
+    unsigned int k[kTopnPer];
+    int n;
+    if (all_in_smem) {
+      n = max(0, min(kTopnPer, C - j0));
+#pragma unroll
+      for (int e = 0; e < kTopnPer; ++e) k[e] = e < n ? ckey[j0 + e] : 0u;
+    } else {
+      topn_load16(scores, j0, C, k, &n);
+    }
+    unsigned int fbits = 0u;
+#pragma unroll
+    for (int e = 0; e < kTopnPer; ++e)
+      if (e < n && (k[e] > kstar || (k[e] == kstar && static_cast<unsigned int>(j0 + e) <= idx_star))) fbits |= 1u << e;
+    unsigned int tot;
+    unsigned int pos = out + topn_scan_excl(__popc(fbits), wsum, &tot);
+#pragma unroll
+    for (int e = 0; e < kTopnPer; ++e)
+      if (((fbits >> e) & 1u) && pos < static_cast<unsigned int>(N)) sel[pos++] = j0 + e;
+    out += tot;
   }
 }
 
@@ -322,8 +501,13 @@ qcf_status qcf_topn_select(const float* scores, int C, int N, int32_t* sel, void
   if (take_fault(4) || !aligned16(scores)) return set_error(QCF_ERR_ALIGN, "qcf_topn_select: scores not 16-byte aligned");
   if (N == 0) return QCF_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  static PerDevice<cudaError_t> smem_attr;
+  const cudaError_t attr = smem_attr.get(current_device(), [] {
+    return cudaFuncSetAttribute(topn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopnSmem);
+  });
+  if (attr != cudaSuccess) return cuda_error(attr, "qcf_topn_select: smem attribute");
   LaunchScope ls(KC_TOPN, st);
-  topn_kernel<<<1, kTopnThreads, 0, st>>>(scores, C, N, sel);
+  topn_kernel<<<1, kTopnThreads, kTopnSmem, st>>>(scores, C, N, sel);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_topn_select: launch");
 }

@@ -119,13 +119,21 @@ def test_profile_scores_full_size_properties(Q, C):
 
 # ----------------------------------------------------------------- top-N
 
-@pytest.mark.parametrize("C", [1, 7, 1000, 5120, 20480, 131072])
+@pytest.mark.parametrize("C", [1, 7, 1000, 5120, 16384, 16385, 20480, 131072, 1 << 20])
 def test_topn_select_exact(Q, C):
+    # 16384 scores or fewer are resolved in shared memory alone; above that a histogram
+    # pass narrows them to one bucket first; one value repeated 20000+ times overflows the
+    # bucket list and takes the all-global radix path
     rng = np.random.default_rng(C)
-    for kind in ("ties", "continuous"):
+    for kind in ("ties", "continuous", "negative", "one_value"):
         if kind == "ties":
             v = (rng.integers(0, 9, C) * 0.125).astype(np.float32)
             v[rng.integers(0, C, max(1, C // 10))] = -0.0
+        elif kind == "negative":
+            v = (rng.standard_normal(C) * 1e3).astype(np.float32)
+        elif kind == "one_value":
+            v = np.full(C, 0.375, np.float32)
+            v[rng.integers(0, C, max(1, C // 100))] = 1.5
         else:
             v = rng.random(C, dtype=np.float32) * 2.0
         s = torch.from_numpy(v).to(DEV)
