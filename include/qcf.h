@@ -89,6 +89,13 @@ int64_t qcf_launch_count(void);
 qcf_status qcf_timing_enable(int on);
 qcf_status qcf_timing_read(int max, const char** names, double* ms, int64_t* launches, int* n_classes);
 
+/* Measures the special-function unit's exp2 throughput of the current device (exp2 per
+ * second over all SMs): eight independent chains of ex2.approx per thread, the best of
+ * two timed launches after one warm-up.  The ceiling of the critical-layer profile, which
+ * evaluates two exponentials per score-row element.  scratch: device memory of at least
+ * num_SMs * 8 * 256 * 4 bytes (the kernel's outputs).  Synchronises the stream. */
+qcf_status qcf_calibrate_exp2_rate(float* scratch, size_t scratch_bytes, double* per_second, void* stream);
+
 /* ------------------------------------------------------------------ shapes */
 
 /* N = ceil(ratio * C) for a recompute ratio in basis points (1500 = 15 %),

@@ -76,6 +76,7 @@ PROTOTYPES = {
     "qcf_launch_count": (I64, []),
     "qcf_timing_enable": (I, [I]),
     "qcf_timing_read": (I, [I, C.POINTER(C.c_char_p), C.POINTER(D64), C.POINTER(I64), C.POINTER(I)]),
+    "qcf_calibrate_exp2_rate": (I, [P, SZ, C.POINTER(D64), P]),
     "qcf_num_selected": (I, [I, I, C.POINTER(I)]),
     "qcf_rope_table_fill_host": (I, [P, P, I, I, D64]),
     "qcf_anchor_keynorm_topk": (I, [P, PI32, I, I, I, I, P, P, P]),

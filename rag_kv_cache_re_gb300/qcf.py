@@ -97,6 +97,15 @@ def qcf_timing_read() -> Dict[str, Tuple[float, int]]:
     return {names[i].decode(): (float(ms[i]), int(cnt[i])) for i in range(k.value)}
 
 
+def qcf_calibrate_exp2_rate(device=None) -> float:
+    """exp2 evaluations per second of the special-function units of the device (measured)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    scratch = torch.empty(1 << 22, dtype=torch.float32, device=dev)
+    rate = C.c_double(0.0)
+    call("qcf_calibrate_exp2_rate", _ptr(scratch), scratch.numel() * 4, C.byref(rate), _stream(None))
+    return float(rate.value)
+
+
 def qcf_num_selected(C_len: int, ratio_bp: int) -> int:
     out = C.c_int(0)
     call("qcf_num_selected", int(C_len), int(ratio_bp), C.byref(out))
