@@ -679,6 +679,8 @@ def run_kernel(args):
     gate_up -- one 8B-shaped decoder layer over 832 recomputed rows of a 5184-row cache (its
     third GEMM launch is the gate/up projection with the SwiGLU epilogue);
     attention -- sparse causal attention at the 16k-context, 20 %-selected sweep point;
+    attention8b -- sparse causal attention of one 8B recompute layer: 832 rows (768 selected of
+    5120 context tokens, uniform, and the 64 query rows) over a 5184-row cache, scale 1/sqrt(128);
     profile -- critical-layer profiling at the 128k-context sweep point (64 query rows);
     topn -- top-N of the 128k profile scores at 15 %."""
     import dataclasses
@@ -697,6 +699,12 @@ def run_kernel(args):
         K = qd.normal_bf16((C + Qn, spec.n_kv_heads, spec.head_dim), 1.0, 71, "cuda")
         V = qd.normal_bf16((C + Qn, spec.n_kv_heads, spec.head_dim), 1.0, 72, "cuda")
         fn = lambda: Q.qcf_fused_layer_forward(dm, 0, x0.clone(), rows, rows, K, V)
+    elif args.kernel == "attention8b":
+        C, N = 5120, 768
+        pos = torch.as_tensor(np.concatenate([qd.selected_indices(C, N, "uniform"), np.arange(C, C + 64)]).astype(np.int32),
+                              device=device)
+        t = qd.sweep_tensors(C + 64, n_query=len(pos), device="cuda")
+        fn = lambda: Q.qcf_sparse_causal_attn(t["Q"], pos, t["K"], t["V"], 1.0 / math.sqrt(128))
     elif args.kernel in ("profile", "topn"):
         t = qd.sweep_tensors(131072, device="cuda")
         if args.kernel == "profile":
@@ -733,7 +741,7 @@ def main(argv=None):
     ap.add_argument("--no-selectors", action="store_true", help="skip timing the QCLast, QCAll and HKVD variants")
     ap.add_argument("--sweep", action="store_true", help="time the kernel-sweep shapes instead of the request")
     ap.add_argument("--oracle-e2e", action="store_true", help="time the oracle end to end (tiny and 8B, fused and full)")
-    ap.add_argument("--kernel", choices=["gate_up", "attention", "profile", "topn"],
+    ap.add_argument("--kernel", choices=["gate_up", "attention", "attention8b", "profile", "topn"],
                     help="repeat one hot kernel (for ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
