@@ -257,6 +257,46 @@ def time_dedupe(dm, store, fr, spec, req, cs, xs, reps):
     return out
 
 
+def time_storage_tier(dm, store, fr, cs, xs, reps):
+    """TTFT of the same request with the chunks' K/V read from files layer by layer (the
+    storage tier) instead of pinned host memory: O_DIRECT reads where the file system
+    takes them (the device's own bandwidth), else buffered reads (page cache)."""
+    from rag_kv_cache_re_gb300 import model as M
+    from rag_kv_cache_re_gb300 import qcf as Q
+    d = tempfile.mkdtemp(prefix="qcf_chunks_")
+    out = {}
+    try:
+        for mode in ("o_direct", "buffered"):
+            files = M.ChunkFiles(store, d, o_direct=mode == "o_direct")
+            written = files.write(fr.chunk_ids)
+            files.files_for(fr)
+            if mode == "o_direct" and not files.o_direct:
+                out["o_direct"] = {"unavailable": "the file system refused O_DIRECT"}
+                files.close()
+                continue
+            fr.run_from_storage(files, cs, xs)
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                a.record(cs)
+                fr.run_from_storage(files, cs, xs)
+                b.record(cs)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            err = Q.qcf_storage_status()
+            read = sum(c.K.numel() * 2 + c.V.numel() * 2 for c in fr.chunks)
+            ms = statistics.median(ts)
+            out[mode] = {"ttft_ms": round(ms, 3), "bytes_read": int(read), "read_gb_per_s": round(read / (ms * 1e-3) / 1e9, 2),
+                         "read_error": err, "bytes_on_storage": int(written) if written else None}
+            files.close()
+    finally:
+        import shutil
+        shutil.rmtree(d, ignore_errors=True)
+    return out
+
+
 def run_gpu(args):
     from rag_kv_cache_re_gb300 import qcf as Q
     world, rank, local = _dist_env()
@@ -373,6 +413,7 @@ def run_gpu(args):
     # ---- the selector variants on the same request: QCLast, QCAll, CacheBlend HKVD
     selectors = None if args.no_selectors else time_selectors(dm, store, fr, spec, req, cs, xs, max(2, min(5, args.steps)))
     dedupe = None if args.no_selectors else time_dedupe(dm, store, fr, spec, req, cs, xs, max(2, min(5, args.steps)))
+    storage = None if args.no_storage else time_storage_tier(dm, store, fr, cs, xs, 5)
 
     # ---- roofline of the dominant kernel (gate/up GEMM with SwiGLU epilogue)
     peaks = load_peaks()
@@ -430,6 +471,8 @@ def run_gpu(args):
         out["selectors"] = selectors
     if dedupe:
         out["shared_chunks"] = dedupe
+    if storage:
+        out["storage_tier"] = storage
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(dm, fr, budget_s=args.cpu_budget)
     if rank == 0:
@@ -739,6 +782,7 @@ def main(argv=None):
     ap.add_argument("--ttft-requests", type=int, default=20, help="synchronised single requests per TTFT median")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-selectors", action="store_true", help="skip timing the QCLast, QCAll and HKVD variants")
+    ap.add_argument("--no-storage", action="store_true", help="skip timing the request served from files")
     ap.add_argument("--sweep", action="store_true", help="time the kernel-sweep shapes instead of the request")
     ap.add_argument("--oracle-e2e", action="store_true", help="time the oracle end to end (tiny and 8B, fused and full)")
     ap.add_argument("--kernel", choices=["gate_up", "attention", "attention8b", "profile", "topn"],

@@ -387,6 +387,35 @@ size_t qcf_request_workspace_size_for(const qcf_dims* dims, const qcf_request* r
 qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, void* ws,
                                size_t ws_bytes, void* compute_stream, void* copy_stream);
 
+/* Storage tier (QCFuse 2.A: chunk KV kept on SSD, layer i+1 loaded while layer i is
+ * recomputed; anchors stay in CPU memory).  qcf_request_prefill with the chunks' K/V read
+ * from files instead of pinned host arrays (r->chunk_K_host / chunk_V_host are ignored;
+ * the anchor stores are still host memory).  Per layer, a host function on the copy stream
+ * reads that layer's keys and values of every chunk into one half of `staging` (pinned
+ * host memory of qcf_storage_staging_bytes, page-aligned for files opened with O_DIRECT),
+ * and the copy stream then copies them into the fused cache and re-rotates the keys; the
+ * critical layer's keys are read first.  The read of layer l+2 reuses the half of layer l
+ * after its copies completed, so reading overlaps the recompute of the layers already
+ * landed, as in qcf_request_prefill.
+ *   files[c]  chunk c's file: fd open for reading (not closed by the library); the keys of
+ *             layer l, [len][Hkv][D] bf16, at k_offset + l * layer_stride, the values at
+ *             v_offset + l * layer_stride.  With O_DIRECT, offsets and block sizes must
+ *             meet the file system's alignment.
+ * A failed or short read leaves that layer's rows undefined (no device fault) and is
+ * reported, once the copy stream has run past it, by qcf_storage_status (the first
+ * failure's errno since the last call, then cleared; 0 when none). */
+typedef struct qcf_chunk_file {
+  int fd;
+  int64_t k_offset;
+  int64_t v_offset;
+  int64_t layer_stride;
+} qcf_chunk_file;
+size_t qcf_storage_staging_bytes(const qcf_dims* dims, const qcf_request* r);
+qcf_status qcf_request_prefill_storage(const qcf_model* m, const qcf_request* r, const qcf_chunk_file* files,
+                                       void* staging, size_t staging_bytes, const qcf_outputs* out, void* ws,
+                                       size_t ws_bytes, void* compute_stream, void* copy_stream);
+qcf_status qcf_storage_status(int* err);
+
 /* Several requests whose retrieved chunks overlap (QCFuse 1: retrieved context chunks of
  * different queries overlap by more than 70 %; 2.B: a position-independent cache index
  * with content-based hash search).  A chunk is the same chunk when two requests pass the

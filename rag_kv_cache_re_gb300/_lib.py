@@ -56,6 +56,10 @@ class Request(C.Structure):
                 ("forced_sel", C.c_void_p), ("selector", C.c_int), ("layer_ratio_bp", C.POINTER(C.c_int32))]
 
 
+class ChunkFile(C.Structure):
+    _fields_ = [("fd", C.c_int), ("k_offset", C.c_int64), ("v_offset", C.c_int64), ("layer_stride", C.c_int64)]
+
+
 class Outputs(C.Structure):
     _fields_ = [("K_layers", C.POINTER(C.c_void_p)), ("V_layers", C.POINTER(C.c_void_p)), ("sel", C.c_void_p),
                 ("scores", C.c_void_p), ("q_crit", C.c_void_p), ("last_logits", C.c_void_p),
@@ -99,6 +103,10 @@ PROTOTYPES = {
     "qcf_request_workspace_size": (SZ, [C.POINTER(Dims), I, I, I, I]),
     "qcf_request_workspace_size_for": (SZ, [C.POINTER(Dims), C.POINTER(Request)]),
     "qcf_kv_deviation": (I, [P, P, P, I, P, P, I, I, I, P, P]),
+    "qcf_storage_staging_bytes": (SZ, [C.POINTER(Dims), C.POINTER(Request)]),
+    "qcf_request_prefill_storage": (I, [C.POINTER(Model), C.POINTER(Request), C.POINTER(ChunkFile), P, SZ,
+                                        C.POINTER(Outputs), P, SZ, P, P]),
+    "qcf_storage_status": (I, [C.POINTER(I)]),
     "qcf_batch_workspace_size": (SZ, [C.POINTER(Dims), C.POINTER(Request), I]),
     "qcf_batch_prefill": (I, [C.POINTER(Model), C.POINTER(Request), C.POINTER(Outputs), I, P, SZ, P, P,
                               C.POINTER(C.c_int64)]),

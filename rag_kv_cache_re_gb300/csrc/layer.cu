@@ -1,6 +1,10 @@
 // Decoder layer forward for recomputed rows, full prefill, and the per-request
 // fused-prefill driver (probe -> profile -> top-N -> pipelined per-layer recompute).
+#include <errno.h>
+#include <unistd.h>
+
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <map>
 #include <mutex>
@@ -620,6 +624,121 @@ static qcf_status request_copy_layers(const qcf_model* m, const qcf_request* r, 
   return QCF_OK;
 }
 
+// ------------------------------------------------------------------ storage tier
+//
+// Chunk K/V read from files layer by layer (QCFuse 2.A keeps chunk KV on SSD and loads
+// layer i+1 while layer i is recomputed).  Reads run as host functions on the copy
+// stream, so each one starts once the copy stream reaches it: it fills one half of a
+// pinned double buffer, the next operations copy that half to the fused cache, and
+// the read two layers later reuses it only after those copies completed (stream
+// order).  Meanwhile the compute stream recomputes the layers already landed.
+struct StorageCtx {
+  std::vector<qcf_chunk_file> files;
+  std::vector<int32_t> len;
+  size_t row_bytes = 0;
+  size_t C = 0;
+  uint8_t* buf[2] = {nullptr, nullptr};   // each: C rows of keys, then C rows of values
+  int err = 0;                            // first failure (errno, or EIO for a short read)
+};
+struct StorageRead {
+  StorageCtx* ctx;
+  int layer, buf;
+  bool keys, values, last;
+};
+static std::atomic<int> g_storage_err{0};
+
+static int read_full(int fd, uint8_t* dst, size_t bytes, int64_t offset) {
+  while (bytes > 0) {
+    const ssize_t got = pread(fd, dst, bytes, static_cast<off_t>(offset));
+    if (got < 0) {
+      if (errno == EINTR) continue;
+      return errno ? errno : EIO;
+    }
+    if (got == 0) return EIO;  // the file ends before the block
+    dst += got;
+    bytes -= static_cast<size_t>(got);
+    offset += got;
+  }
+  return 0;
+}
+
+static void CUDART_CB storage_read_fn(void* arg) {
+  StorageRead* rd = static_cast<StorageRead*>(arg);
+  StorageCtx* c = rd->ctx;
+  if (c->err == 0 && (rd->keys || rd->values)) {
+    size_t row0 = 0;
+    for (size_t i = 0; i < c->files.size() && c->err == 0; ++i) {
+      const qcf_chunk_file& f = c->files[i];
+      const size_t bytes = static_cast<size_t>(c->len[i]) * c->row_bytes;
+      const int64_t layer_off = static_cast<int64_t>(rd->layer) * f.layer_stride;
+      if (rd->keys) c->err = read_full(f.fd, c->buf[rd->buf] + row0 * c->row_bytes, bytes, f.k_offset + layer_off);
+      if (c->err == 0 && rd->values)
+        c->err = read_full(f.fd, c->buf[rd->buf] + (c->C + row0) * c->row_bytes, bytes, f.v_offset + layer_off);
+      row0 += static_cast<size_t>(c->len[i]);
+    }
+  }
+  if (rd->last) {
+    if (c->err) {
+      int expected = 0;
+      g_storage_err.compare_exchange_strong(expected, c->err);
+    }
+    delete c;
+  }
+  delete rd;
+}
+
+// request_copy_layers with the chunk K/V coming from files through the pinned double buffer.
+static qcf_status request_copy_layers_storage(const qcf_model* m, const qcf_outputs* out, const ReqPlan& P,
+                                              StorageCtx* ctx, cudaStream_t xs, cudaEvent_t ev_crit,
+                                              const cudaEvent_t* ev_layer) {
+  const qcf_dims& d = m->dims;
+  const int L = d.n_layers, C = P.C, crit = P.crit;
+  const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim;
+  const size_t bytes = static_cast<size_t>(C) * HD * sizeof(qcf_bf16);
+  int b = 0;
+  bool enqueued = false;  // host functions holding ctx are in the stream
+  auto enqueue_read = [&](int layer, bool keys, bool values, bool last) -> cudaError_t {
+    StorageRead* rd = new StorageRead{ctx, layer, b, keys, values, last};
+    const cudaError_t e = cudaLaunchHostFunc(xs, storage_read_fn, rd);
+    if (e != cudaSuccess) delete rd;
+    else enqueued = true;
+    return e;
+  };
+  // On a failed enqueue: with no host function holding ctx it is freed here; otherwise the
+  // final host function frees it after the ones before (if even that cannot be enqueued,
+  // ctx is left allocated rather than freed under a pending host function).
+  auto fail = [&](cudaError_t e, const char* what) {
+    if (!enqueued) delete ctx;
+    else enqueue_read(0, false, false, true);
+    return cuda_error(e, what);
+  };
+  auto rotate = [&](int l) -> cudaError_t {
+    __nv_bfloat16* Kl = reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]);
+    return launch_reposition(Kl, Kl, C, d.n_kv_heads, d.head_dim, P.seg_start.data(), P.seg_delta.data(),
+                             static_cast<int>(P.seg_start.size()) - 1, &m->rope, xs);
+  };
+  cudaError_t e;
+  if ((e = enqueue_read(crit, true, false, false)) != cudaSuccess) return fail(e, "storage: read");
+  if ((e = cudaMemcpyAsync(out->K_layers[crit], ctx->buf[b], bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+    return fail(e, "storage: copy");
+  if ((e = rotate(crit)) != cudaSuccess) return fail(e, "storage: reposition");
+  if ((e = cudaEventRecord(ev_crit, xs)) != cudaSuccess) return fail(e, "storage: record");
+  for (int l = 0; l < L; ++l) {
+    b ^= 1;
+    const bool keys = l != crit;
+    if ((e = enqueue_read(l, keys, true, false)) != cudaSuccess) return fail(e, "storage: read");
+    if (keys && (e = cudaMemcpyAsync(out->K_layers[l], ctx->buf[b], bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+      return fail(e, "storage: copy");
+    if ((e = cudaMemcpyAsync(out->V_layers[l], ctx->buf[b] + bytes, bytes, cudaMemcpyHostToDevice, xs)) != cudaSuccess)
+      return fail(e, "storage: copy");
+    if (keys && (e = rotate(l)) != cudaSuccess) return fail(e, "storage: reposition");
+    if ((e = cudaEventRecord(ev_layer[l], xs)) != cudaSuccess) return fail(e, "storage: record");
+  }
+  // the last host function reports a failed read and frees the context
+  if ((e = enqueue_read(0, false, false, true)) != cudaSuccess) return fail(e, "storage: read");
+  return QCF_OK;
+}
+
 // The compute stream of one request: probe, profile and selection (or the
 // KV-deviation filter), the per-layer recompute waiting on ev_layer[l], LM head.
 static qcf_status request_compute(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, ReqPlan& P,
@@ -999,6 +1118,70 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
   if ((e = cudaEventRecord(ev_anchor, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
   if ((s = request_copy_layers(m, r, out, P, xs, ev_crit, ev_layer)) != QCF_OK) return s;
   return request_compute(m, r, out, P, cs, ev_anchor, ev_crit, ev_layer);
+}
+
+size_t qcf_storage_staging_bytes(const qcf_dims* dims, const qcf_request* r) {
+  if (!dims || !r || !r->chunk_len || r->n_chunks <= 0) return 0;
+  int64_t C = 0;
+  for (int c = 0; c < r->n_chunks; ++c) {
+    if (r->chunk_len[c] <= 0) return 0;
+    C += r->chunk_len[c];
+  }
+  return static_cast<size_t>(4 * C) * dims->n_kv_heads * dims->head_dim * sizeof(qcf_bf16);
+}
+
+qcf_status qcf_request_prefill_storage(const qcf_model* m, const qcf_request* r, const qcf_chunk_file* files,
+                                       void* staging, size_t staging_bytes, const qcf_outputs* out, void* ws,
+                                       size_t ws_bytes, void* compute_stream, void* copy_stream) {
+  if (!m || !r || !files || !staging || !r->chunk_len)
+    return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill_storage: NULL pointer");
+  if (r->n_chunks <= 0 || r->n_chunks > kMaxReqChunks)
+    return set_error(QCF_ERR_SHAPE, "qcf_request_prefill_storage: n_chunks=%d", r->n_chunks);
+  const size_t need = qcf_storage_staging_bytes(&m->dims, r);
+  if (need == 0 || staging_bytes < need)
+    return set_error(QCF_ERR_WORKSPACE, "qcf_request_prefill_storage: staging %zu < %zu bytes", staging_bytes, need);
+  for (int c = 0; c < r->n_chunks; ++c)
+    if (files[c].fd < 0 || files[c].k_offset < 0 || files[c].v_offset < 0 || files[c].layer_stride < 0)
+      return set_error(QCF_ERR_INVALID_ARG, "qcf_request_prefill_storage: chunk %d file", c);
+  // the chunk host pointers are not read on this path: point them at the staging buffer
+  // so the shared validation accepts the request
+  std::vector<const qcf_bf16*> host_ptrs(r->n_chunks, static_cast<const qcf_bf16*>(staging));
+  qcf_request rr = *r;
+  rr.chunk_K_host = host_ptrs.data();
+  rr.chunk_V_host = host_ptrs.data();
+  ReqPlan P;
+  qcf_status s = request_plan(m, &rr, out, ws, ws_bytes, &P);
+  if (s != QCF_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream);
+  cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+  const int L = m->dims.n_layers;
+  EventPool& pool = event_pool();
+  std::lock_guard<std::mutex> lk(pool.mu);
+  cudaEvent_t* ev = nullptr;
+  if (!pool.get(static_cast<size_t>(L) + 3, &ev)) return set_error(QCF_ERR_CUDA, "qcf_request_prefill_storage: events");
+  cudaEvent_t ev_start = ev[0], ev_anchor = ev[1], ev_crit = ev[2];
+  cudaEvent_t* ev_layer = ev + 3;
+  cudaError_t e = cudaEventRecord(ev_start, cs);
+  if (e != cudaSuccess) return cuda_error(e, "qcf_request_prefill_storage: record start");
+  if ((e = cudaStreamWaitEvent(xs, ev_start, 0)) != cudaSuccess)
+    return cuda_error(e, "qcf_request_prefill_storage: copy wait");
+  if ((s = request_copy_anchors(m, &rr, P, xs)) != QCF_OK) return s;
+  if ((e = cudaEventRecord(ev_anchor, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill_storage: record");
+  StorageCtx* ctx = new StorageCtx;
+  ctx->files.assign(files, files + r->n_chunks);
+  ctx->len.assign(r->chunk_len, r->chunk_len + r->n_chunks);
+  ctx->row_bytes = static_cast<size_t>(m->dims.n_kv_heads) * m->dims.head_dim * sizeof(qcf_bf16);
+  ctx->C = static_cast<size_t>(P.C);
+  ctx->buf[0] = static_cast<uint8_t*>(staging);
+  ctx->buf[1] = static_cast<uint8_t*>(staging) + 2 * ctx->C * ctx->row_bytes;
+  if ((s = request_copy_layers_storage(m, out, P, ctx, xs, ev_crit, ev_layer)) != QCF_OK) return s;
+  return request_compute(m, &rr, out, P, cs, ev_anchor, ev_crit, ev_layer);
+}
+
+qcf_status qcf_storage_status(int* err) {
+  if (!err) return set_error(QCF_ERR_INVALID_ARG, "qcf_storage_status: NULL pointer");
+  *err = g_storage_err.exchange(0);
+  return QCF_OK;
 }
 
 size_t qcf_batch_workspace_size(const qcf_dims* dims, const qcf_request* reqs, int n_req) {

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes as C
 import hashlib
+import os
 from typing import Dict, List, Optional, Sequence
 
 import numpy as np
@@ -144,6 +145,83 @@ class ChunkStore:
                                                 V.to(torch.bfloat16).cpu().contiguous().pin_memory(), idx, aK, aV))
 
 
+class ChunkFiles:
+    """A storage tier for a chunk store: every stored chunk's per-layer K and V in a file
+    (QCFuse 2.A keeps chunk KV on SSD and the anchors in CPU memory).
+
+    File layout, raw bf16: the keys [L][len][Hkv][D], then the values [L][len][Hkv][D].
+    Files are named by the chunk's content hash, so a chunk shared by requests is stored
+    once.  With o_direct the reads bypass the page cache (where the file system supports
+    it and every block is 4096-byte aligned); otherwise they are plain buffered reads.
+    """
+
+    ALIGN = 4096
+
+    def __init__(self, store: "ChunkStore", directory: str, o_direct: bool = True):
+        self.store, self.directory = store, directory
+        os.makedirs(directory, exist_ok=True)
+        self.paths: Dict[bytes, str] = {}
+        self.fds: Dict[bytes, int] = {}
+        self.o_direct_requested = o_direct
+        self.o_direct = False
+
+    def write(self, chunk_ids: Sequence[int]) -> int:
+        """Writes the chunks not yet on storage; returns the bytes written."""
+        written = 0
+        for cid in chunk_ids:
+            c = self.store.chunks[int(cid)]
+            key = ChunkStore.content_key(c.tokens)
+            if key in self.paths:
+                continue
+            path = os.path.join(self.directory, key.hex()[:32] + ".kv")
+            with open(path, "wb") as f:
+                for t in (c.K, c.V):
+                    b = t.contiguous().view(torch.int16).numpy().tobytes()
+                    f.write(b)
+                    written += len(b)
+            self.paths[key] = path
+        return written
+
+    def _fd(self, key: bytes) -> int:
+        if key not in self.fds:
+            flags = os.O_RDONLY
+            fd = -1
+            if self.o_direct_requested and hasattr(os, "O_DIRECT"):
+                try:
+                    fd = os.open(self.paths[key], flags | os.O_DIRECT)
+                    self.o_direct = True
+                except OSError:
+                    fd = -1
+            if fd < 0:
+                fd = os.open(self.paths[key], flags)
+                self.o_direct = False
+            self.fds[key] = fd
+        return self.fds[key]
+
+    def files_for(self, request: "FusedRequest"):
+        """qcf_chunk_file entries for the request's chunks, in its retrieval order."""
+        s = request.model.spec
+        row = s.n_kv_heads * s.head_dim * 2
+        arr = (_lib.ChunkFile * len(request.chunks))()
+        for i, c in enumerate(request.chunks):
+            key = ChunkStore.content_key(c.tokens)
+            block = len(c.tokens) * row
+            arr[i] = _lib.ChunkFile(self._fd(key), 0, s.n_layers * block, block)
+        return arr
+
+    def aligned_for_direct(self, request: "FusedRequest") -> bool:
+        s = request.model.spec
+        row = s.n_kv_heads * s.head_dim * 2
+        starts = np.cumsum([0] + [len(c.tokens) for c in request.chunks])
+        sizes = [len(c.tokens) * row for c in request.chunks]
+        return all(v % self.ALIGN == 0 for v in sizes + [int(x) * row for x in starts])
+
+    def close(self):
+        for fd in self.fds.values():
+            os.close(fd)
+        self.fds.clear()
+
+
 SELECT_CRITICAL, SELECT_ALL_LAYERS, SELECT_HKVD = 0, 1, 2
 
 
@@ -228,6 +306,25 @@ class FusedRequest:
             with torch.cuda.stream(cs):
                 self.ids.copy_(self.ids_host, non_blocking=True)
         Q.qcf_request_prefill(self.model, self.req, self.outs, self.ws, cs, xs)
+
+    def run_from_storage(self, files: "ChunkFiles", compute_stream=None, copy_stream=None) -> None:
+        """Enqueue the fused prefill with the chunks' K/V read layer by layer from `files`
+        (a storage tier) through a pinned double buffer; anchors stay in host memory."""
+        cs = compute_stream or torch.cuda.current_stream()
+        xs = copy_stream or cs
+        nb = _lib.lib().qcf_storage_staging_bytes(C.byref(self.model.struct.dims), C.byref(self.req))
+        if nb == 0:
+            raise ValueError("malformed request (staging size 0)")
+        if getattr(self, "_staging", None) is None or self._staging.numel() < nb + ChunkFiles.ALIGN:
+            self._staging = torch.empty(nb + ChunkFiles.ALIGN, dtype=torch.uint8).pin_memory()
+        base = self._staging.data_ptr()
+        aligned = (base + ChunkFiles.ALIGN - 1) // ChunkFiles.ALIGN * ChunkFiles.ALIGN
+        if files.o_direct_requested and not files.aligned_for_direct(self):
+            raise ValueError("O_DIRECT reads need 4096-byte aligned chunk blocks; open ChunkFiles with o_direct=False")
+        self._files = files.files_for(self)
+        Q.call("qcf_request_prefill_storage", C.byref(self.model.struct), C.byref(self.req), self._files,
+               C.c_void_p(aligned), nb, C.byref(self.outs), Q._ptr(self.ws), self.ws.numel(), Q._stream(cs),
+               Q._stream(xs))
 
     @property
     def selected(self) -> torch.Tensor:

@@ -106,6 +106,14 @@ def qcf_calibrate_exp2_rate(device=None) -> float:
     return float(rate.value)
 
 
+def qcf_storage_status() -> int:
+    """errno of the first failed storage read since the last call (0 when none); the copy
+    stream must have run past the reads (synchronise first)."""
+    v = C.c_int(0)
+    call("qcf_storage_status", C.byref(v))
+    return int(v.value)
+
+
 def qcf_num_selected(C_len: int, ratio_bp: int) -> int:
     out = C.c_int(0)
     call("qcf_num_selected", int(C_len), int(ratio_bp), C.byref(out))

@@ -131,3 +131,33 @@ int main() {
     subprocess.run([gxx, "-std=c++17", "-O1", "-pthread", "-I", hdr, str(src), "-o", str(exe)], check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_chunk_files_layout(tmp_path):
+    """ChunkFiles writes a chunk as raw bf16 keys [L][len][Hkv][D] then values, named by
+    content, once per content; the offsets it hands the library address those blocks."""
+    import torch
+    from rag_kv_cache_re_gb300.model import ChunkFiles
+    L, n, Hkv, D = 3, 8, 2, 16
+    g = torch.Generator().manual_seed(0)
+
+    def chunk(seed):
+        K = torch.randn((L, n, Hkv, D), generator=g).to(torch.bfloat16)
+        V = torch.randn((L, n, Hkv, D), generator=g).to(torch.bfloat16)
+        return StoredChunk(np.arange(n, dtype=np.int32) + seed, K, V, np.zeros(0, np.int32), None, None)
+
+    class _Store:
+        chunks = {0: chunk(0), 1: chunk(100)}
+
+    _Store.chunks[2] = _Store.chunks[0]            # same content: one file
+    files = ChunkFiles(_Store, str(tmp_path), o_direct=False)
+    assert files.write([0, 1, 2]) == 2 * 2 * L * n * Hkv * D * 2
+    assert len(os.listdir(tmp_path)) == 2
+    c = _Store.chunks[1]
+    raw = open(files.paths[ChunkStore.content_key(c.tokens)], "rb").read()
+    block = n * Hkv * D * 2
+    for l in range(L):
+        k = np.frombuffer(raw[l * block:(l + 1) * block], dtype=np.int16)
+        v = np.frombuffer(raw[(L + l) * block:(L + l + 1) * block], dtype=np.int16)
+        assert np.array_equal(k, c.K[l].contiguous().view(torch.int16).numpy().ravel())
+        assert np.array_equal(v, c.V[l].contiguous().view(torch.int16).numpy().ravel())
