@@ -6,7 +6,10 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <condition_variable>
+#include <functional>
 #include <map>
+#include <thread>
 #include <mutex>
 #include <tuple>
 #include <vector>
@@ -662,20 +665,79 @@ static int read_full(int fd, uint8_t* dst, size_t bytes, int64_t offset) {
   return 0;
 }
 
+// A small pool of reader threads: one layer's blocks (a chunk's keys or values each)
+// are read concurrently, so a storage device sees several requests in flight.
+class ReadPool {
+ public:
+  static ReadPool& get() {
+    static ReadPool pool;
+    return pool;
+  }
+  // Runs every task on the pool and returns when all are done.
+  void run(std::vector<std::function<void()>>& tasks) {
+    std::unique_lock<std::mutex> lk(mu_);
+    for (auto& t : tasks) queue_.push_back(&t);
+    pending_ += tasks.size();
+    cv_.notify_all();
+    done_cv_.wait(lk, [&] { return pending_ == 0; });
+  }
+
+ private:
+  static constexpr int kThreads = 8;
+  ReadPool() {
+    for (int i = 0; i < kThreads; ++i) threads_.emplace_back([this] { work(); });
+  }
+  ~ReadPool() {
+    {
+      std::lock_guard<std::mutex> lk(mu_);
+      stop_ = true;
+    }
+    cv_.notify_all();
+    for (auto& t : threads_) t.join();
+  }
+  void work() {
+    std::unique_lock<std::mutex> lk(mu_);
+    while (true) {
+      cv_.wait(lk, [&] { return stop_ || !queue_.empty(); });
+      if (stop_ && queue_.empty()) return;
+      std::function<void()>* t = queue_.back();
+      queue_.pop_back();
+      lk.unlock();
+      (*t)();
+      lk.lock();
+      if (--pending_ == 0) done_cv_.notify_all();
+    }
+  }
+  std::mutex mu_;
+  std::condition_variable cv_, done_cv_;
+  std::vector<std::function<void()>*> queue_;
+  size_t pending_ = 0;
+  bool stop_ = false;
+  std::vector<std::thread> threads_;
+};
+
 static void CUDART_CB storage_read_fn(void* arg) {
   StorageRead* rd = static_cast<StorageRead*>(arg);
   StorageCtx* c = rd->ctx;
   if (c->err == 0 && (rd->keys || rd->values)) {
+    std::vector<std::function<void()>> tasks;
+    std::vector<int> errs(2 * c->files.size(), 0);
     size_t row0 = 0;
-    for (size_t i = 0; i < c->files.size() && c->err == 0; ++i) {
-      const qcf_chunk_file& f = c->files[i];
+    for (size_t i = 0; i < c->files.size(); ++i) {
+      const qcf_chunk_file f = c->files[i];
       const size_t bytes = static_cast<size_t>(c->len[i]) * c->row_bytes;
       const int64_t layer_off = static_cast<int64_t>(rd->layer) * f.layer_stride;
-      if (rd->keys) c->err = read_full(f.fd, c->buf[rd->buf] + row0 * c->row_bytes, bytes, f.k_offset + layer_off);
-      if (c->err == 0 && rd->values)
-        c->err = read_full(f.fd, c->buf[rd->buf] + (c->C + row0) * c->row_bytes, bytes, f.v_offset + layer_off);
+      uint8_t* kdst = c->buf[rd->buf] + row0 * c->row_bytes;
+      uint8_t* vdst = c->buf[rd->buf] + (c->C + row0) * c->row_bytes;
+      int* ek = &errs[2 * i];
+      int* ev = &errs[2 * i + 1];
+      if (rd->keys) tasks.emplace_back([=] { *ek = read_full(f.fd, kdst, bytes, f.k_offset + layer_off); });
+      if (rd->values) tasks.emplace_back([=] { *ev = read_full(f.fd, vdst, bytes, f.v_offset + layer_off); });
       row0 += static_cast<size_t>(c->len[i]);
     }
+    ReadPool::get().run(tasks);
+    for (int e : errs)
+      if (e && c->err == 0) c->err = e;
   }
   if (rd->last) {
     if (c->err) {
