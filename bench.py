@@ -688,12 +688,14 @@ def run_sweep(args):
         Kc = K[:C]
         ms_prof = timed(lambda: Q.qcf_profile_scores(q, Kc, 1.0))
         scores = Q.qcf_profile_scores(q, Kc, 1.0)
+        ws_topn = Q.workspace(Q._lib.lib().qcf_topn_select_workspace_size(C), device, "topn")
         kbytes = C * Hkv * D * 2
         exps = 2.0 * nq * Hq * C                 # two passes, one exp2 per score-row element each
         pflops = 2.0 * 2.0 * nq * Hq * C * D     # two passes of Q K^T
         for frac_bp in qd.SWEEP_FRACTIONS_BP:
             N = (frac_bp * C + 9999) // 10000
-            ms_topn = timed(lambda: Q.qcf_topn_select(scores, N))
+            ms_topn = timed(lambda: Q.qcf_topn_select_ws(scores, N, ws_topn))
+            ms_topn_one = timed(lambda: Q.qcf_topn_select(scores, N))
             for pattern in ("uniform", "clusters"):
                 pos = np.concatenate([qd.selected_indices(C, N, pattern), np.arange(C, C + nq)]).astype(np.int32)
                 pos_d = torch.from_numpy(pos).to(device)
@@ -704,7 +706,7 @@ def run_sweep(args):
                 print(json.dumps({
                     "sweep": {"context": C, "selected_bp": frac_bp, "pattern": pattern, "N": int(N), "query_rows": nq},
                     "profile_topn_ms": round(ms_prof + ms_topn, 4), "profile_ms": round(ms_prof, 4),
-                    "topn_ms": round(ms_topn, 4),
+                    "topn_ms": round(ms_topn, 4), "topn_one_cta_ms": round(ms_topn_one, 4),
                     "profile_roofline": profile_ceilings(ms_prof, kbytes, pflops, exps, peaks, exp_rate),
                     "attn_ms": round(ms_attn, 4),
                     "attn_roofline": {"bound": "tensor", "achieved": round(aflops / (ms_attn * 1e-3) / 1e12, 1),
@@ -725,7 +727,7 @@ def run_kernel(args):
     attention8b -- sparse causal attention of one 8B recompute layer: 832 rows (768 selected of
     5120 context tokens, uniform, and the 64 query rows) over a 5184-row cache, scale 1/sqrt(128);
     profile -- critical-layer profiling at the 128k-context sweep point (64 query rows);
-    topn -- top-N of the 128k profile scores at 15 %."""
+    topn -- top-N of the 128k profile scores at 15 % (the workspace entry point: cooperative grid)."""
     import dataclasses
     from rag_kv_cache_re_gb300 import model as M
     from rag_kv_cache_re_gb300 import qcf as Q
@@ -754,7 +756,8 @@ def run_kernel(args):
             fn = lambda: Q.qcf_profile_scores(t["Q"], t["K"], 1.0)
         else:
             sc = Q.qcf_profile_scores(t["Q"], t["K"], 1.0)
-            fn = lambda: Q.qcf_topn_select(sc, (1500 * 131072 + 9999) // 10000)
+            ws_topn = Q.workspace(Q._lib.lib().qcf_topn_select_workspace_size(131072), device, "topn")
+            fn = lambda: Q.qcf_topn_select_ws(sc, (1500 * 131072 + 9999) // 10000, ws_topn)
     else:
         Hq, Hkv, D = qd.SWEEP_HEADS
         C, N = 16384, 3277

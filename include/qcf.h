@@ -182,6 +182,19 @@ qcf_status qcf_profile_scores_noalloc(const qcf_bf16* q, const qcf_bf16* K, int 
  * Exact on the fp32 bit patterns; -0.0 counts as +0.0; scores must not be NaN. */
 qcf_status qcf_topn_select(const float* scores, int C, int N, int32_t* sel, void* stream);
 
+/* Top-N selection with scratch, for long score vectors: the same result as
+ * qcf_topn_select.  Above 16384 scores the work spreads over a cooperative grid of
+ * up to one CTA per SM (4096 scores each) that reads the scores once and meets at
+ * bounded grid barriers (a barrier that runs out sets QCF_DEV_TIMEOUT and leaves sel
+ * incomplete); at or below 16384 scores, or beyond what one resident grid covers,
+ * this is qcf_topn_select and ws is not touched.
+ *   ws  device scratch of qcf_topn_select_workspace_size(C) bytes (0 for C <= 16384,
+ *       then ws may be NULL), cleared by the call itself; calls that overlap on the
+ *       GPU need separate scratch. */
+size_t qcf_topn_select_workspace_size(int C);
+qcf_status qcf_topn_select_ws(const float* scores, int C, int N, int32_t* sel, void* ws, size_t ws_bytes,
+                              void* stream);
+
 /* KV deviation of recomputed rows ("KVCache reuse 01" 1.3.2, "KV Deviation"): for i < n,
  * dev[i] = sum over the Hkv*D entries of (k_new[i] - K_cache[pos[i]])^2 + (v_new[i] - V_cache[pos[i]])^2,
  * fp32 accumulation of bf16 inputs.

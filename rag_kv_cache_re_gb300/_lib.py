@@ -89,6 +89,8 @@ PROTOTYPES = {
     "qcf_profile_scores": (I, [P, P, I, I, I, I, I, F, P, P, SZ, P]),
     "qcf_profile_scores_noalloc": (I, [P, P, I, I, I, I, I, F, P, P]),
     "qcf_topn_select": (I, [P, I, I, P, P]),
+    "qcf_topn_select_workspace_size": (SZ, [I]),
+    "qcf_topn_select_ws": (I, [P, I, I, P, P, SZ, P]),
     "qcf_gather_rows": (I, [P, I64, I, P, I, P, P]),
     "qcf_scatter_kv": (I, [P, P, P, I, I, I, P, P, I, P]),
     "qcf_sparse_causal_attn_workspace_size": (SZ, [I, I, I, I, I]),

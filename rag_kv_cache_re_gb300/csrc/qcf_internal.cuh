@@ -135,6 +135,10 @@ size_t profile_tc_workspace_size(int nq, int C, int Hq, int Hkv);
 qcf_status profile_tc_launch(const __nv_bfloat16* q, const __nv_bfloat16* K, int nq, int C, int Hq, int Hkv,
                              float scale, float* scores, void* ws, cudaStream_t st);
 constexpr int kProfileTcMaxGroup = 16;  // heads per KV head served by the tensor-core profile
+// exact top-N over a cooperative grid (topn_grid.cu); workspace and launch
+size_t topn_grid_workspace_size(int C);
+int topn_grid_max_scores();  // largest C whose CTAs all stay resident on the current device (0 if unknown)
+qcf_status topn_grid_launch(const float* scores, int C, int N, int32_t* sel, void* ws, cudaStream_t st);
 
 // Attention internals (attention.cu).
 size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D);

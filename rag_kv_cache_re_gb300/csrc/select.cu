@@ -512,4 +512,26 @@ qcf_status qcf_topn_select(const float* scores, int C, int N, int32_t* sel, void
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_topn_select: launch");
 }
 
+size_t qcf_topn_select_workspace_size(int C) {
+  return C > kTopnCap ? topn_grid_workspace_size(C) : 0;
+}
+
+qcf_status qcf_topn_select_ws(const float* scores, int C, int N, int32_t* sel, void* ws, size_t ws_bytes,
+                              void* stream) {
+  if (!scores || (!sel && N > 0)) return set_error(QCF_ERR_INVALID_ARG, "qcf_topn_select_ws: NULL pointer");
+  if (C < 0 || C > (1 << 24) || N < 0 || N > C)
+    return set_error(QCF_ERR_SHAPE, "qcf_topn_select_ws: C=%d N=%d", C, N);
+  const size_t need = qcf_topn_select_workspace_size(C);
+  if (need > 0 && !ws) return set_error(QCF_ERR_INVALID_ARG, "qcf_topn_select_ws: NULL workspace");
+  if (take_fault(4) || !aligned16(scores) || !aligned16(ws))
+    return set_error(QCF_ERR_ALIGN, "qcf_topn_select_ws: alignment");
+  if (take_fault(2) || ws_bytes < need)
+    return set_error(QCF_ERR_WORKSPACE, "qcf_topn_select_ws: workspace %zu < %zu", ws_bytes, need);
+  if (N == 0) return QCF_OK;
+  // one CTA holds up to kTopnCap scores in shared memory; larger vectors spread over a
+  // cooperative grid while all its CTAs fit on the device at once
+  if (C <= kTopnCap || C > topn_grid_max_scores()) return qcf_topn_select(scores, C, N, sel, stream);
+  return topn_grid_launch(scores, C, N, sel, ws, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

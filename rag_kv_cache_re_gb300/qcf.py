@@ -176,6 +176,16 @@ def qcf_topn_select(scores: torch.Tensor, N: int, stream=None) -> torch.Tensor:
     return sel[:N]
 
 
+def qcf_topn_select_ws(scores: torch.Tensor, N: int, ws: torch.Tensor = None, stream=None) -> torch.Tensor:
+    _need_cuda(scores)
+    sel = torch.empty(max(int(N), 1), dtype=torch.int32, device=scores.device)
+    if ws is None:
+        ws = workspace(_lib.lib().qcf_topn_select_workspace_size(scores.numel()), scores.device, "topn")
+    call("qcf_topn_select_ws", _ptr(scores), scores.numel(), int(N), _ptr(sel), _ptr(ws), ws.numel(),
+         _stream(stream))
+    return sel[:N]
+
+
 def qcf_gather_rows(src: torch.Tensor, idx: torch.Tensor, stream=None) -> torch.Tensor:
     _need_cuda(src, idx)
     rows = src.shape[0]

@@ -64,6 +64,13 @@ def test_argument_errors_are_synchronous(lib):
     fake = C.c_void_p(0x100000)  # aligned, never dereferenced: validation fails first
     assert lib.qcf_topn_select(None, 10, 3, fake, None) == 1
     assert lib.qcf_topn_select(fake, 10, 11, fake, None) == 2            # N > C
+    assert lib.qcf_topn_select_workspace_size(16384) == 0
+    need = lib.qcf_topn_select_workspace_size(131072)
+    assert need >= 2 * 16384 * 4 and need % 4 == 0
+    assert lib.qcf_topn_select_ws(fake, 131072, 10, fake, None, 0, None) == 1      # no scratch
+    assert lib.qcf_topn_select_ws(fake, 131072, 10, fake, fake, need - 4, None) == 4
+    assert lib.qcf_topn_select_ws(fake, 131072, 10, fake, C.c_void_p(0x100008), need, None) == 3
+    assert lib.qcf_topn_select_ws(fake, 100, 0, fake, None, 0, None) == 0           # nothing to select
     assert lib.qcf_linear(fake, 4, 65, fake, 64, 0, fake, None, 0, None) == 2   # K % 64
     assert lib.qcf_linear(C.c_void_p(0x100004), 4, 64, fake, 64, 0, fake, None, 0, None) == 3  # misaligned
     assert b"16-byte" in lib.qcf_last_error()

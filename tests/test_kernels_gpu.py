@@ -145,6 +145,35 @@ def test_topn_select_exact(Q, C):
             assert np.array_equal(got, want), f"C={C} N={N} {kind}"
 
 
+@pytest.mark.parametrize("C", [100, 16385, 20480, 131072, 300001, 152 * 4096, 1 << 20])
+def test_topn_select_grid_exact(Q, C):
+    # above 16384 scores the workspace entry point spreads over a cooperative grid (4096
+    # scores per CTA); uniform [1, 2) shares its top 11 key bits, so it needs a second
+    # global level; one value repeated fixes every key bit and ranks the equal keys by
+    # index across CTAs; beyond one resident grid the call is the one-CTA kernel
+    rng = np.random.default_rng(C + 1)
+    ws = Q.workspace(Q._lib.lib().qcf_topn_select_workspace_size(C), DEV, "topn_test")
+    for kind in ("ties", "continuous", "unit_interval", "one_value", "negative"):
+        if kind == "ties":
+            v = (rng.integers(0, 9, C) * 0.125).astype(np.float32)
+            v[rng.integers(0, C, max(1, C // 10))] = -0.0
+        elif kind == "unit_interval":
+            v = (1.0 + rng.random(C, dtype=np.float32)).astype(np.float32)
+        elif kind == "one_value":
+            v = np.full(C, 0.375, np.float32)
+            v[rng.integers(0, C, max(1, C // 100))] = 1.5
+        elif kind == "negative":
+            v = (rng.standard_normal(C) * 1e3).astype(np.float32)
+        else:
+            v = rng.random(C, dtype=np.float32) * 2.0
+        s = torch.from_numpy(v).to(DEV)
+        for N in sorted({1, 7, O.num_selected(C, 1500), C // 2 + 3, C}):
+            got = Q.qcf_topn_select_ws(s, N, ws).cpu().numpy()
+            want = O.topn_select(v.astype(np.float64), N)
+            assert np.array_equal(got, want), f"C={C} N={N} {kind}"
+    assert Q.qcf_query_status() == 0
+
+
 # ----------------------------------------------------------------- gather / scatter
 
 def test_gather_and_scatter_exact(Q):
