@@ -581,12 +581,13 @@ static qcf_status request_copy_anchors(const qcf_model* m, const qcf_request* r,
   return QCF_OK;
 }
 
-// The request's chunk K/V of every layer straight into its fused cache: the critical
-// layer's keys first (ev_crit), then layer by layer (ev_layer[l]), each layer's keys
-// re-rotated to their offsets on the copy stream right after they land.
+// The request's chunk K/V of every layer straight into its fused cache, each layer's
+// keys re-rotated to their offsets on the copy stream right after they land: with
+// crit_part the critical layer's keys (then ev_crit), else every layer in order (the
+// critical layer's values only), each followed by ev_layer[l].
 static qcf_status request_copy_layers(const qcf_model* m, const qcf_request* r, const qcf_outputs* out,
                                       const ReqPlan& P, cudaStream_t xs, cudaEvent_t ev_crit,
-                                      const cudaEvent_t* ev_layer) {
+                                      const cudaEvent_t* ev_layer, bool crit_part) {
   const qcf_dims& d = m->dims;
   const int L = d.n_layers, C = P.C, crit = P.crit;
   const std::vector<int32_t>& seg_start = P.seg_start;
@@ -615,9 +616,12 @@ static qcf_status request_copy_layers(const qcf_model* m, const qcf_request* r, 
     return launch_reposition(Kl, Kl, C, d.n_kv_heads, d.head_dim, seg_start.data(), seg_delta.data(), r->n_chunks,
                              &m->rope, xs);
   };
-  if ((e = copy_layer(crit, true, false)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: critical-layer copy");
-  if ((e = rotate_layer(crit)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: reposition");
-  if ((e = cudaEventRecord(ev_crit, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
+  if (crit_part) {
+    if ((e = copy_layer(crit, true, false)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: critical-layer copy");
+    if ((e = rotate_layer(crit)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: reposition");
+    if ((e = cudaEventRecord(ev_crit, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
+    return QCF_OK;
+  }
   for (int l = 0; l < L; ++l) {
     if ((e = copy_layer(l, l != crit, true)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: layer copy");
     if (l != crit && (e = rotate_layer(l)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: reposition");
@@ -803,9 +807,14 @@ static qcf_status request_copy_layers_storage(const qcf_model* m, const qcf_outp
 
 // The compute stream of one request: probe, profile and selection (or the
 // KV-deviation filter), the per-layer recompute waiting on ev_layer[l], LM head.
+// enqueue_layers (may be empty) puts the per-layer copies, and their ev_layer records, on
+// the copy stream; it runs once, before the first wait on any ev_layer[l] is enqueued, and
+// as late as that allows: after the probe, whose launches then reach the GPU without
+// waiting behind the host's many copy calls.
 static qcf_status request_compute(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, ReqPlan& P,
                                   cudaStream_t cs, cudaEvent_t ev_anchor, cudaEvent_t ev_crit,
-                                  const cudaEvent_t* ev_layer) {
+                                  const cudaEvent_t* ev_layer,
+                                  const std::function<qcf_status()>& enqueue_layers = {}) {
   const qcf_dims& d = m->dims;
   const int L = d.n_layers;
   const bool all_layers = P.all_layers, hkvd = P.hkvd;
@@ -826,7 +835,14 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
   const __nv_bfloat16* embed = reinterpret_cast<const __nv_bfloat16*>(m->embed);
   const float* x_final = nullptr;  // final hidden states of the recomputed rows [ns][d]
   int ns = 0;
+  bool layers_enqueued = !enqueue_layers;
+  auto layers_now = [&]() -> qcf_status {
+    if (layers_enqueued) return QCF_OK;
+    layers_enqueued = true;
+    return enqueue_layers();
+  };
   if (hkvd) {
+    if ((s = layers_now()) != QCF_OK) return s;
     // every context row and the query enter layer 0; the kept set shrinks layer by layer
     {
       LaunchScope ls(KC_MISC, cs);
@@ -873,6 +889,7 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
     const float scale = 1.0f / sqrtf(static_cast<float>(d.head_dim));
     if (all_layers && (e = cudaMemsetAsync(rl.scores_acc, 0, static_cast<size_t>(C) * sizeof(float), cs)) != cudaSuccess)
       return cuda_error(e, "qcf_request_prefill: clear scores");
+    if (all_layers && (s = layers_now()) != QCF_OK) return s;   // the probe profiles every layer
     if (crit > 0) {
       if ((e = cudaStreamWaitEvent(cs, ev_anchor, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
       for (int l = 0; l < crit; ++l) {
@@ -918,6 +935,7 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
                       rl.lb.gemm_zeroed);
       if (s != QCF_OK) return s;
     }
+    if ((s = layers_now()) != QCF_OK) return s;
     // profile the re-rotated critical-layer keys and select
     if ((e = cudaStreamWaitEvent(cs, ev_crit, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
     __nv_bfloat16* Kcrit = reinterpret_cast<__nv_bfloat16*>(out->K_layers[crit]);
@@ -1174,12 +1192,14 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
   cudaError_t e = cudaEventRecord(ev_start, cs);
   if (e != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record start");
   if ((e = cudaStreamWaitEvent(xs, ev_start, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: copy wait");
-  // ---- copy stream: anchors of the probe layers, the critical layer's keys, then every layer in order
+  // ---- copy stream: anchors of the probe layers, the critical layer's keys, then every layer in
+  // order; the per-layer copies (most of the host's calls) are enqueued after the probe's launches
   if (take_fault(3)) return set_error(QCF_ERR_CUDA, "qcf_request_prefill: injected host-to-device copy failure");
   if ((s = request_copy_anchors(m, r, P, xs)) != QCF_OK) return s;
   if ((e = cudaEventRecord(ev_anchor, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
-  if ((s = request_copy_layers(m, r, out, P, xs, ev_crit, ev_layer)) != QCF_OK) return s;
-  return request_compute(m, r, out, P, cs, ev_anchor, ev_crit, ev_layer);
+  if ((s = request_copy_layers(m, r, out, P, xs, ev_crit, ev_layer, true)) != QCF_OK) return s;
+  return request_compute(m, r, out, P, cs, ev_anchor, ev_crit, ev_layer,
+                         [&] { return request_copy_layers(m, r, out, P, xs, ev_crit, ev_layer, false); });
 }
 
 size_t qcf_storage_staging_bytes(const qcf_dims* dims, const qcf_request* r) {
