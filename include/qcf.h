@@ -189,8 +189,8 @@ qcf_status qcf_topn_select(const float* scores, int C, int N, int32_t* sel, void
  * incomplete); at or below 16384 scores, or beyond what one resident grid covers,
  * this is qcf_topn_select and ws is not touched.
  *   ws  device scratch of qcf_topn_select_workspace_size(C) bytes (0 for C <= 16384,
- *       then ws may be NULL), cleared by the call itself; calls that overlap on the
- *       GPU need separate scratch. */
+ *       then ws may be NULL); it needs no clearing (each call resets the state it
+ *       uses, on the GPU); calls that overlap on the GPU need separate scratch. */
 size_t qcf_topn_select_workspace_size(int C);
 qcf_status qcf_topn_select_ws(const float* scores, int C, int N, int32_t* sel, void* ws, size_t ws_bytes,
                               void* stream);

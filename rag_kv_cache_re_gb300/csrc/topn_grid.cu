@@ -6,7 +6,9 @@
 // Each CTA keeps four scores per thread in registers (its slice of 4096) through every
 // phase; the phases meet at grid barriers (bounded waits, so a CTA that never arrives
 // turns into QCF_DEV_TIMEOUT instead of a hang; the cooperative launch guarantees every
-// CTA is resident):
+// CTA is resident).  The scratch needs no clearing between calls: CTA 0 clears the
+// counters and histograms and then publishes the call's 64-bit tag (a per-process
+// sequence number), and every CTA waits for that tag before its first global update.
 //   levels   histograms of 11, 11 and 10 key bits from the top, each restricted to the
 //            bucket chosen so far, added into global bins; after each barrier every CTA
 //            reads the bins and picks the bucket of the N-th largest key, until that
@@ -21,6 +23,9 @@
 // When every key bit is fixed and still more than kGridCap keys equal K*, the CTAs
 // publish their counts of greater and of equal keys instead and rank the equal ones
 // by index across CTAs.
+#include <atomic>
+#include <chrono>
+
 #include "qcf_internal.cuh"
 
 namespace qcf {
@@ -30,12 +35,14 @@ constexpr int kGridPer = 4;                               // scores per thread
 constexpr int kGridSlice = kGridThreads * kGridPer;       // scores per CTA
 constexpr int kGridCap = 16384;                           // candidates one CTA resolves in shared memory
 constexpr int kGridTarget = 4096;                         // another global level while the bucket is larger
-constexpr int kGridSmem = 2 * kGridCap * 4 + 4096 * 4;    // candidate keys, indices, one histogram
+constexpr int kGridHistMax = 4096;                        // bins of the widest histogram (index rounds)
+constexpr int kGridSmem = 2 * kGridCap * 4 + kGridHistMax * 4;   // candidate keys, indices, one histogram
 
-// Workspace: [0] barrier arrivals, [1] candidate count, then three 2048-bin histograms
-// (zeroed before each call), then the candidate list, then per-CTA counts.
+// Workspace: [0] barrier arrivals, [1] candidate count, [2..3] the tag of the call that
+// last cleared it, then the three levels' histograms (2048, 2048 and 1024 bins), the
+// candidate list and per-CTA counts.
 constexpr size_t kGridCtlWords = 64;
-constexpr size_t kGridHistWords = 3 * 2048;
+constexpr size_t kGridHistWords = 2048 + 2048 + 1024;
 constexpr size_t kGridZeroBytes = (kGridCtlWords + kGridHistWords) * 4;
 
 __device__ __forceinline__ unsigned int grid_order_key(float f) {
@@ -49,14 +56,20 @@ __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 
-// Barrier over the grid: the k-th barrier waits for k * gridDim.x arrivals.  Returns false
-// (every thread of the CTA) when the wait gave up.
+// Barrier over the grid: the k-th barrier waits for k * gridDim.x arrivals.  The CTA's
+// writes before it are ordered by the CTA barrier and released at GPU scope by thread 0's
+// arrival; after it, the CTA reads other CTAs' data with L2 loads.  Returns false (every
+// thread of the CTA) when the wait gave up.
 __device__ bool grid_barrier(unsigned int* bar, unsigned int target, unsigned int* status, int* s_ok) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(bar, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
     const uint64_t t0 = globaltimer();
     bool ok = true;
     while (ld_acquire_u32(bar) < target) {
@@ -102,17 +115,18 @@ __device__ __forceinline__ unsigned int grid_scan_excl(unsigned int v, unsigned 
 }
 
 // out = {bin, still needed from it, the bin's count} for the need-th element from the top
-// (desc) or bottom of h[nbins]; nbins in {1024, 2048, 4096}.
+// (desc) or bottom of h[nbins]; nbins a power of two from 512 to 8192.
 __device__ void grid_pick_bin(const unsigned int* h, int nbins, bool desc, unsigned int need, unsigned int* wsum,
                               unsigned int* out) {
-  const int k = nbins / kGridThreads;
+  const int k = nbins >= kGridThreads ? nbins / kGridThreads : 1;
   const int p0 = threadIdx.x * k;
+  const int kk = p0 < nbins ? k : 0;   // threads past the last bin hold none
   unsigned int local = 0u;
-  for (int i = 0; i < k; ++i) local += h[desc ? nbins - 1 - (p0 + i) : p0 + i];
+  for (int i = 0; i < kk; ++i) local += h[desc ? nbins - 1 - (p0 + i) : p0 + i];
   unsigned int tot;
   unsigned int before = grid_scan_excl(local, wsum, &tot);
   if (before < need && need <= before + local) {
-    for (int i = 0; i < k; ++i) {
+    for (int i = 0; i < kk; ++i) {
       const int bin = desc ? nbins - 1 - (p0 + i) : p0 + i;
       const unsigned int c = h[bin];
       if (before + c >= need) {
@@ -129,20 +143,22 @@ __device__ void grid_pick_bin(const unsigned int* h, int nbins, bool desc, unsig
 
 __device__ __forceinline__ int grid_level_shift(int lv) { return lv == 0 ? 21 : (lv == 1 ? 10 : 0); }
 __device__ __forceinline__ int grid_level_bins(int lv) { return lv == 2 ? 1024 : 2048; }
+__device__ __forceinline__ int grid_level_offset(int lv) { return lv * 2048; }
 
 __global__ void __launch_bounds__(kGridThreads, 1)
     topn_grid_kernel(const float* __restrict__ scores, int C, int N, int32_t* __restrict__ sel,
-                     unsigned int* __restrict__ ws, unsigned int* status) {
+                     unsigned int* __restrict__ ws, unsigned long long tag, unsigned int* status) {
   extern __shared__ __align__(16) unsigned int gsm[];
   unsigned int* ckey = gsm;                                  // [kGridCap]
   int* cidx = reinterpret_cast<int*>(gsm + kGridCap);        // [kGridCap]
-  unsigned int* h = gsm + 2 * kGridCap;                      // [4096]
+  unsigned int* h = gsm + 2 * kGridCap;                      // [kGridHistMax]
   __shared__ unsigned int wsum[33];
   __shared__ unsigned int pick[3];
   __shared__ int s_ok;
   unsigned int* bar = ws;
   unsigned int* cand_n = ws + 1;
-  unsigned int* ghist = ws + kGridCtlWords;                  // [3][2048]
+  unsigned long long* ready = reinterpret_cast<unsigned long long*>(ws + 2);
+  unsigned int* ghist = ws + kGridCtlWords;                  // the levels' bins, back to back
   unsigned int* gkey = ws + kGridCtlWords + kGridHistWords;  // [kGridCap]
   int* gidx = reinterpret_cast<int*>(gkey + kGridCap);       // [kGridCap]
   unsigned int* counts = gkey + 2 * kGridCap;                // [gridDim.x][2]
@@ -167,6 +183,17 @@ __global__ void __launch_bounds__(kGridThreads, 1)
     for (int e = 0; e < kGridPer; ++e) k[e] = e < n ? grid_order_key(scores[j0 + e]) : 0u;
   }
 
+  // ---- set-up: CTA 0 clears the counters and histograms, then publishes this call's tag
+  if (blockIdx.x == 0) {
+    for (size_t i = tid; i < kGridHistWords; i += kGridThreads) ghist[i] = 0u;
+    if (tid == 0) {
+      *bar = 0u;
+      *cand_n = 0u;
+    }
+    __syncthreads();
+    if (tid == 0) asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ready), "l"(tag) : "memory");
+  }
+
   // ---- levels
   unsigned int need = static_cast<unsigned int>(N), prefix = 0u, fmask = 0u, bucket = 0u;
   int lv = 0;
@@ -177,11 +204,25 @@ __global__ void __launch_bounds__(kGridThreads, 1)
 #pragma unroll
     for (int e = 0; e < kGridPer; ++e)
       if (e < n && (k[e] & fmask) == prefix) atomicAdd(&h[(k[e] >> shift) & (nb - 1)], 1u);
+    if (lv == 0 && tid == 0) {   // the scratch is cleared for this call before the first global update
+      const uint64_t t0 = globaltimer();
+      bool ok = true;
+      while (ld_acquire_u64(ready) != tag) {
+        if (globaltimer() - t0 > QCF_WAIT_NS) {
+          ok = false;
+          flag_status(status, QCF_DEV_TIMEOUT);
+          break;
+        }
+        __nanosleep(32);
+      }
+      s_ok = ok ? 1 : 0;
+    }
     __syncthreads();
+    if (!s_ok) return;
     for (int i = tid; i < nb; i += kGridThreads)
-      if (h[i]) atomicAdd(&ghist[lv * 2048 + i], h[i]);
+      if (h[i]) atomicAdd(&ghist[grid_level_offset(lv) + i], h[i]);
     if (!grid_barrier(bar, (++n_bar) * G, status, &s_ok)) return;
-    for (int i = tid; i < nb; i += kGridThreads) h[i] = ld_acquire_u32(&ghist[lv * 2048 + i]);
+    for (int i = tid; i < nb; i += kGridThreads) h[i] = __ldcg(&ghist[grid_level_offset(lv) + i]);
     __syncthreads();
     grid_pick_bin(h, nb, true, need, wsum, pick);
     prefix |= pick[0] << shift;
@@ -222,6 +263,7 @@ __global__ void __launch_bounds__(kGridThreads, 1)
       cidx[i] = __ldcg(gidx + i);
     }
     __syncthreads();
+    unsigned int n_eq = bucket;   // keys in the current bucket; all equal K* once every bit is fixed
     for (; lv < 3; ++lv) {
       const int shift = grid_level_shift(lv), nb = grid_level_bins(lv);
       for (int i = tid; i < nb; i += kGridThreads) h[i] = 0u;
@@ -235,10 +277,32 @@ __global__ void __launch_bounds__(kGridThreads, 1)
       prefix |= pick[0] << shift;
       fmask |= static_cast<unsigned int>(nb - 1) << shift;
       need = pick[1];
+      n_eq = pick[2];
     }
     kstar = prefix;
     unsigned int ip = 0u, im = 0u;
-    for (int il = 0; il < 2; ++il) {
+    if (n_eq <= 32u) {
+      // few keys equal K* (one, for most score vectors): one warp ranks their indices
+      unsigned int* lst = h;        // [32] indices, then the count
+      if (tid == 0) lst[32] = 0u;
+      __syncthreads();
+      for (int i = tid; i < n_c; i += kGridThreads)
+        if (ckey[i] == kstar) {
+          const unsigned int slot = atomicAdd(&lst[32], 1u);
+          if (slot < 32u) lst[slot] = static_cast<unsigned int>(cidx[i]);
+        }
+      __syncthreads();
+      if (tid < 32) {
+        const unsigned int cnt = min(lst[32], 32u);
+        const unsigned int mine_idx = static_cast<unsigned int>(tid) < cnt ? lst[tid] : 0xFFFFFFFFu;
+        unsigned int rank = 0u;
+        for (int j = 0; j < 32; ++j) rank += __shfl_sync(0xffffffffu, mine_idx, j) < mine_idx ? 1u : 0u;
+        if (static_cast<unsigned int>(tid) < cnt && rank == need - 1u) pick[0] = mine_idx;
+      }
+      __syncthreads();
+      ip = pick[0];
+    }
+    for (int il = 0; il < 2 && n_eq > 32u; ++il) {
       const int shift = il == 0 ? 12 : 0;
       for (int i = tid; i < 4096; i += kGridThreads) h[i] = 0u;
       __syncthreads();
@@ -278,8 +342,8 @@ __global__ void __launch_bounds__(kGridThreads, 1)
   if (tid < 32) {
     unsigned int a = 0u, b = 0u;
     for (unsigned int c = lane; c < blockIdx.x; c += 32) {
-      a += ld_acquire_u32(&counts[2 * c]);
-      b += ld_acquire_u32(&counts[2 * c + 1]);
+      a += __ldcg(&counts[2 * c]);
+      b += __ldcg(&counts[2 * c + 1]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -336,19 +400,33 @@ int topn_grid_max_scores() {
   return static_cast<int>(n < (1 << 24) ? n : (1 << 24));
 }
 
+// Call tags: a process-wide sequence under a high half drawn from the clock and an
+// address, so a tag left in a workspace by an earlier call (or another process) never
+// equals the current call's.
+static unsigned long long next_call_tag() {
+  static std::atomic<unsigned long long> seq{0};
+  static const unsigned long long hi = [] {
+    unsigned long long x = static_cast<unsigned long long>(
+        std::chrono::steady_clock::now().time_since_epoch().count());
+    x ^= reinterpret_cast<uintptr_t>(&seq) * 0x9E3779B97F4A7C15ull;
+    x ^= x >> 29;
+    return (x | 1ull) << 32;
+  }();
+  return hi ^ (seq.fetch_add(1) + 1);
+}
+
 qcf_status topn_grid_launch(const float* scores, int C, int N, int32_t* sel, void* ws, cudaStream_t st) {
   const int G = (C + kGridSlice - 1) / kGridSlice;
   const int cap = topn_grid_capacity();
   if (cap <= 0) return set_error(QCF_ERR_CUDA, "qcf_topn_select_ws: cooperative occupancy query failed");
   if (G > cap) return set_error(QCF_ERR_SHAPE, "qcf_topn_select_ws: %d scores need %d resident CTAs, at most %d", C, G, cap);
-  cudaError_t e = cudaMemsetAsync(ws, 0, kGridZeroBytes, st);
-  if (e != cudaSuccess) return cuda_error(e, "qcf_topn_select_ws: workspace clear");
   unsigned int* w = static_cast<unsigned int*>(ws);
+  unsigned long long tag = next_call_tag();
   unsigned int* status = device_status_ptr();
-  void* args[] = {const_cast<float**>(&scores), &C, &N, &sel, &w, &status};
+  void* args[] = {const_cast<float**>(&scores), &C, &N, &sel, &w, &tag, &status};
   LaunchScope ls(KC_TOPN, st);
-  e = cudaLaunchCooperativeKernel(reinterpret_cast<void*>(topn_grid_kernel), dim3(G), dim3(kGridThreads), args,
-                                  kGridSmem, st);
+  const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<void*>(topn_grid_kernel), dim3(G),
+                                                    dim3(kGridThreads), args, kGridSmem, st);
   return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_topn_select_ws: cooperative launch");
 }
 

@@ -153,6 +153,7 @@ def test_topn_select_grid_exact(Q, C):
     # index across CTAs; beyond one resident grid the call is the one-CTA kernel
     rng = np.random.default_rng(C + 1)
     ws = Q.workspace(Q._lib.lib().qcf_topn_select_workspace_size(C), DEV, "topn_test")
+    ws.fill_(0xFF)   # the scratch needs no clearing: every call resets what it uses
     for kind in ("ties", "continuous", "unit_interval", "one_value", "negative"):
         if kind == "ties":
             v = (rng.integers(0, 9, C) * 0.125).astype(np.float32)
