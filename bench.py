@@ -257,6 +257,50 @@ def time_dedupe(dm, store, fr, spec, req, cs, xs, reps):
     return out
 
 
+def measure_host_link(fr, device):
+    """Host link as the request uses it: one 256 MB pinned copy each way (the link's rate),
+    and the request's own chunk-K/V copy pattern alone on a stream (one copy per chunk,
+    layer and K or V: the copy engine's rate at these sizes)."""
+    st = torch.cuda.Stream(device)
+    big_h = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
+    big_d = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def best_ms(fn, reps=3):
+        best = 1e30
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(st)
+            with torch.cuda.stream(st):
+                fn()
+            b.record(st)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    h2d_ms = best_ms(lambda: big_d.copy_(big_h, non_blocking=True))
+    d2h_ms = best_ms(lambda: big_h.copy_(big_d, non_blocking=True))
+    del big_h, big_d
+    dst_k = [torch.empty_like(c.K[0], device=device) for c in fr.chunks]
+    dst_v = [torch.empty_like(c.V[0], device=device) for c in fr.chunks]
+    L = fr.chunks[0].K.shape[0]
+
+    def pattern():
+        for l in range(L):
+            for c, dk, dv in zip(fr.chunks, dst_k, dst_v):
+                dk.copy_(c.K[l], non_blocking=True)
+                dv.copy_(c.V[l], non_blocking=True)
+
+    pat_ms = best_ms(pattern)
+    pat_bytes = sum(c.K.numel() * 2 + c.V.numel() * 2 for c in fr.chunks)
+    n_copies = 2 * L * len(fr.chunks)
+    return {"h2d_gb_per_s": round((256 << 20) / (h2d_ms * 1e-3) / 1e9, 1),
+            "d2h_gb_per_s": round((256 << 20) / (d2h_ms * 1e-3) / 1e9, 1),
+            "request_copies": {"copies": n_copies, "bytes": int(pat_bytes), "ms": round(pat_ms, 3),
+                               "gb_per_s": round(pat_bytes / (pat_ms * 1e-3) / 1e9, 1)},
+            "method": "256 MB pinned copies (best of 3); the request's chunk K/V copies alone on one stream"}
+
+
 def time_storage_tier(dm, store, fr, cs, xs, reps):
     """TTFT of the same request with the chunks' K/V read from files layer by layer (the
     storage tier) instead of pinned host memory: O_DIRECT reads where the file system
@@ -473,6 +517,7 @@ def run_gpu(args):
         out["shared_chunks"] = dedupe
     if storage:
         out["storage_tier"] = storage
+    out["host_link"] = measure_host_link(fr, device)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(dm, fr, budget_s=args.cpu_budget)
     if rank == 0:
