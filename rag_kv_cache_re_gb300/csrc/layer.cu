@@ -106,8 +106,9 @@ static qcf_status check_model(const qcf_model* m, const char* who) {
 // One decoder layer on rows x (validated by the caller).
 // `probe` only selects the timing classes (the probe's 64-row GEMMs are weight-bound
 // and are accounted apart from the recompute GEMMs).
-// The first kernel is launched plainly (it may follow an event wait or a foreign
-// kernel); for layers of up to kPdlMaxRows rows the six after it, which follow this
+// The first kernel is launched plainly unless the caller knows it follows this
+// library's kernels directly (first_pdl); for layers of up to kPdlMaxRows rows the six
+// after it, which follow this
 // library's kernels directly, are launched programmatically so each one's set-up
 // overlaps the tail of the one before.  Measured on GB300 (8B layer shapes): the
 // 64- and 832-row layers of a fused prefill gain ~5% per request; the 5184-row layers
@@ -116,12 +117,14 @@ static qcf_status check_model(const qcf_model* m, const char* who) {
 constexpr int kPdlMaxRows = 2048;
 static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, const int32_t* rope_pos,
                                      const int32_t* cache_row, int n, __nv_bfloat16* Kc, __nv_bfloat16* Vc, int T,
-                                     const LayerBufs& b, cudaStream_t st, bool probe = false) {
+                                     const LayerBufs& b, cudaStream_t st, bool probe = false,
+                                     bool first_pdl = false) {
   const qcf_dims& d = m->dims;
   const qcf_layer_weights& w = m->layers[layer];
   const int D = d.head_dim, Hq = d.n_heads, Hkv = d.n_kv_heads;
   const bool pdl = n <= kPdlMaxRows;
-  cudaError_t e = launch_rmsnorm(x, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, b.h, st);
+  cudaError_t e = launch_rmsnorm(x, n, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, b.h, st,
+                                 first_pdl && pdl);
   if (e != cudaSuccess) return cuda_error(e, "layer: rmsnorm");
   EpiParams ep{};
   ep.q_out = b.q;
@@ -205,19 +208,24 @@ struct ChunkOffsets {
 };
 
 // Probe KV prefix for one layer: anchor rows of every chunk from the staging
-// buffer [chunk][layer][anchor][Hkv*D] into probe cache rows chunk*A + a, keys
-// re-rotated by the chunk's offset, values copied.  One thread per (row, head,
-// group of 8 rotation pairs).
+// buffer [chunk][layer][anchor][Hkv*D] into probe cache rows chunk*A + a of every
+// probe layer (layer l's cache at l * layer_stride elements), keys re-rotated by the
+// chunk's offset, values copied.  One thread per (layer, row, head, group of 8
+// rotation pairs).
 __global__ void anchor_assemble_kernel(const __nv_bfloat16* __restrict__ stK, const __nv_bfloat16* __restrict__ stV,
-                                       int layer, int n_layers_staged, int A, int Hkv, int D,
+                                       int n_layers_staged, int A, int Hkv, int D,
                                        const float* __restrict__ cos_t, const float* __restrict__ sin_t,
                                        const ChunkOffsets co, __nv_bfloat16* __restrict__ pK,
-                                       __nv_bfloat16* __restrict__ pV) {
+                                       __nv_bfloat16* __restrict__ pV, size_t layer_stride) {
   const int half = D / 2, groups = half / 8;
   const int per_row = Hkv * groups;
-  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   const int rows = co.n_chunks * A;
-  if (tid >= rows * per_row) return;
+  const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gtid >= static_cast<long long>(n_layers_staged) * rows * per_row) return;
+  const int layer = static_cast<int>(gtid / (static_cast<long long>(rows) * per_row));
+  const int tid = static_cast<int>(gtid - static_cast<long long>(layer) * rows * per_row);
+  pK += static_cast<size_t>(layer) * layer_stride;
+  pV += static_cast<size_t>(layer) * layer_stride;
   const int row = tid / per_row;
   const int rem = tid - row * per_row;
   const int h = rem / groups, k0 = (rem - h * groups) * 8;
@@ -254,7 +262,7 @@ struct RequestLayout {
   int32_t* probe_row;    // [Q] probe cache rows nA..nA+Q-1
   __nv_bfloat16* stK;    // [n_chunks][crit][A][HD]
   __nv_bfloat16* stV;
-  __nv_bfloat16* pK;     // [nA+Q][HD]
+  __nv_bfloat16* pK;     // [crit][nA+Q][HD]: the probe cache of each probe layer
   __nv_bfloat16* pV;
   __nv_bfloat16* q_crit; // [Q][Hq*D]
   float* scores;         // [C]
@@ -288,8 +296,10 @@ static bool carve_request(Carve& c, const qcf_dims& d, int C, int Q, int nA, int
   const size_t staged = static_cast<size_t>(n_chunks) * (crit > 0 ? crit : 1) * (n_anchor > 0 ? n_anchor : 1) * HD;
   r->stK = c.take<__nv_bfloat16>(staged);
   r->stV = c.take<__nv_bfloat16>(staged);
-  r->pK = c.take<__nv_bfloat16>(static_cast<size_t>(nA + Q) * HD);
-  r->pV = c.take<__nv_bfloat16>(static_cast<size_t>(nA + Q) * HD);
+  // one probe cache per probe layer, so every layer's anchor rows are assembled in one launch
+  const size_t probe_layers = crit > 0 ? crit : 1;
+  r->pK = c.take<__nv_bfloat16>(probe_layers * (nA + Q) * HD);
+  r->pV = c.take<__nv_bfloat16>(probe_layers * (nA + Q) * HD);
   r->q_crit = c.take<__nv_bfloat16>(static_cast<size_t>(Q) * d.n_heads * d.head_dim);
   r->scores = c.take<float>(C);
   r->scores_acc = c.take<float>(C);
@@ -892,15 +902,18 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
     if (all_layers && (s = layers_now()) != QCF_OK) return s;   // the probe profiles every layer
     if (crit > 0) {
       if ((e = cudaStreamWaitEvent(cs, ev_anchor, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+      const size_t pstride = static_cast<size_t>(nA + Q) * d.n_kv_heads * d.head_dim;
+      if (nA > 0) {
+        const long long threads = static_cast<long long>(crit) * nA * d.n_kv_heads * (d.head_dim / 16);
+        LaunchScope ls(KC_ROPE, cs);
+        anchor_assemble_kernel<<<static_cast<unsigned int>((threads + 255) / 256), 256, 0, cs>>>(
+            rl.stK, rl.stV, crit, A, d.n_kv_heads, d.head_dim, m->rope.cos, m->rope.sin, co, rl.pK, rl.pV, pstride);
+      }
       for (int l = 0; l < crit; ++l) {
-        if (nA > 0) {
-          const int threads = nA * d.n_kv_heads * (d.head_dim / 16);
-          LaunchScope ls(KC_ROPE, cs);
-          anchor_assemble_kernel<<<(threads + 255) / 256, 256, 0, cs>>>(rl.stK, rl.stV, l, crit, A, d.n_kv_heads,
-                                                                        d.head_dim, m->rope.cos, m->rope.sin, co, rl.pK,
-                                                                        rl.pV);
-        }
-        s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK, rl.pV, nA + Q, rl.lb, cs, true);
+        // consecutive probe layers follow each other directly (QCAll puts a profile and an
+        // event wait between them): their first launch is programmatic too
+        s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK + l * pstride, rl.pV + l * pstride,
+                               nA + Q, rl.lb, cs, true, !all_layers);
         if (s != QCF_OK) return s;
         if (all_layers) {   // QCAll: this probe layer's q against this layer's re-rotated keys
           if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
@@ -915,8 +928,9 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
     // critical layer: q = RoPE(RMSNorm(x) W_q) only
     {
       const qcf_layer_weights& w = m->layers[crit];
-      if ((e = launch_rmsnorm(rl.x, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, rl.lb.h, cs)) !=
-          cudaSuccess)
+      // programmatic when it follows the last probe layer's down projection directly
+      if ((e = launch_rmsnorm(rl.x, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, rl.lb.h, cs,
+                              crit > 0 && !all_layers && Q <= kPdlMaxRows)) != cudaSuccess)
         return cuda_error(e, "qcf_request_prefill: rmsnorm");
       EpiParams ep{};
       ep.q_out = q_crit;
