@@ -487,6 +487,11 @@ static EventPool& event_pool() {
 }
 
 // Everything a request needs between validation and its launches.
+// Pinned host memory feeds a layer's chunk K/V (~10 MB for the 8B request) faster
+// than a 832-row layer recomputes, so the copies run several layers ahead: the
+// recompute waits for them every 4 layers.
+constexpr int kPinnedWaitStride = 4;
+
 struct ReqPlan {
   bool all_layers = false, hkvd = false;
   int C = 0, Q = 0, T = 0, N = 0, crit = 0, A = 0, nA = 0;
@@ -499,6 +504,11 @@ struct ReqPlan {
   int32_t* sel = nullptr;
   __nv_bfloat16* q_crit = nullptr;
   size_t ws_used = 0;
+  // The recompute waits for the copy stream every wait_stride layers, each time for the
+  // layers up to the next wait: fewer event waits split the programmatic launch chain,
+  // at the price of waiting for up to wait_stride - 1 later layers' copies.  1 where the
+  // copies are the slow side (files).
+  int wait_stride = 1;
 };
 
 // Validates a request and carves its buffers from ws.
@@ -977,11 +987,14 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
     // pipelined per-layer recompute of the selected rows and the query
     if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, rl.rows, 0, ns, rl.x, cs)) != cudaSuccess)
       return cuda_error(e, "qcf_request_prefill: embed");
+    const int stride = std::max(1, P.wait_stride);
     for (int l = 0; l < L; ++l) {
-      if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+      const bool wait_here = l % stride == 0;
+      if (wait_here && (e = cudaStreamWaitEvent(cs, ev_layer[std::min(l + stride - 1, L - 1)], 0)) != cudaSuccess)
+        return cuda_error(e, "qcf_request_prefill: wait");
       __nv_bfloat16* Kl = reinterpret_cast<__nv_bfloat16*>(out->K_layers[l]);
       __nv_bfloat16* Vl = reinterpret_cast<__nv_bfloat16*>(out->V_layers[l]);
-      s = layer_forward_impl(m, l, rl.x, rl.rows, rl.rows, ns, Kl, Vl, T, rl.lb, cs);
+      s = layer_forward_impl(m, l, rl.x, rl.rows, rl.rows, ns, Kl, Vl, T, rl.lb, cs, false, !wait_here);
       if (s != QCF_OK) return s;
     }
     if ((e = launch_lm_head(m, rl.x + static_cast<size_t>(ns - 1) * d.d_model, out->last_logits, out->first_token,
@@ -1212,6 +1225,7 @@ qcf_status qcf_request_prefill(const qcf_model* m, const qcf_request* r, const q
   if ((s = request_copy_anchors(m, r, P, xs)) != QCF_OK) return s;
   if ((e = cudaEventRecord(ev_anchor, xs)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: record");
   if ((s = request_copy_layers(m, r, out, P, xs, ev_crit, ev_layer, true)) != QCF_OK) return s;
+  P.wait_stride = kPinnedWaitStride;
   return request_compute(m, r, out, P, cs, ev_anchor, ev_crit, ev_layer,
                          [&] { return request_copy_layers(m, r, out, P, xs, ev_crit, ev_layer, false); });
 }
