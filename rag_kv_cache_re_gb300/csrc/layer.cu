@@ -178,6 +178,8 @@ __global__ void iota_kernel(int32_t* out, int n, int start) {
 
 // rows[i] = sel[i] for i < N, then the query rows C, C+1, ...
 __global__ void make_rows_kernel(const int32_t* __restrict__ sel, int N, int C, int n, int32_t* __restrict__ rows) {
+  pdl_wait();  // the selection comes from the kernel before
+  pdl_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) rows[i] = i < N ? sel[i] : C + (i - N);
 }
@@ -307,7 +309,7 @@ static bool carve_request(Carve& c, const qcf_dims& d, int C, int Q, int nA, int
   r->sel = c.take<int32_t>(N > 0 ? N : 1);
   r->prof_ws_bytes = qcf_profile_scores_workspace_size(Q, C, d.n_heads, d.n_kv_heads, d.head_dim);
   r->prof_ws = c.take<uint8_t>(r->prof_ws_bytes);
-  r->lm_ws = c.take<uint8_t>(256);
+  r->lm_ws = c.take<uint8_t>(qcf_lm_head_workspace_size(&d));
   return c.ok;
 }
 
@@ -379,7 +381,7 @@ static bool carve_hkvd(Carve& c, const qcf_dims& d, int C, int Q, const std::vec
   H->lb.gemm_ws = c.take<uint8_t>(gws);
   H->lb.attn_ws_bytes = aws;
   H->lb.attn_ws = c.take<uint8_t>(aws > 0 ? aws : 1);
-  H->lm_ws = c.take<uint8_t>(256);
+  H->lm_ws = c.take<uint8_t>(qcf_lm_head_workspace_size(&d));
   return c.ok;
 }
 
@@ -975,17 +977,19 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
         if ((e = cudaMemcpyAsync(sel, r->forced_sel, N * sizeof(int32_t), cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
           return cuda_error(e, "qcf_request_prefill: forced selection");
       } else {
-        s = qcf_topn_select(scores, C, N, sel, cs);
+        s = topn_launch(scores, C, N, sel, cs, true);
         if (s != QCF_OK) return s;
       }
     }
     ns = N + Q;
     {
       LaunchScope ls(KC_MISC, cs);
-      make_rows_kernel<<<(ns + 255) / 256, 256, 0, cs>>>(sel, N, C, ns, rl.rows);
+      if ((e = launch_pdl(make_rows_kernel, dim3((ns + 255) / 256), dim3(256), 0, cs, static_cast<const int32_t*>(sel), N,
+                          C, ns, rl.rows)) != cudaSuccess)
+        return cuda_error(e, "qcf_request_prefill: rows");
     }
     // pipelined per-layer recompute of the selected rows and the query
-    if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, rl.rows, 0, ns, rl.x, cs)) != cudaSuccess)
+    if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, rl.rows, 0, ns, rl.x, cs, true)) != cudaSuccess)
       return cuda_error(e, "qcf_request_prefill: embed");
     const int stride = std::max(1, P.wait_stride);
     for (int l = 0; l < L; ++l) {
@@ -998,7 +1002,7 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
       if (s != QCF_OK) return s;
     }
     if ((e = launch_lm_head(m, rl.x + static_cast<size_t>(ns - 1) * d.d_model, out->last_logits, out->first_token,
-                            rl.lm_ws, cs)) != cudaSuccess)
+                            rl.lm_ws, cs, ns <= kPdlMaxRows)) != cudaSuccess)
       return cuda_error(e, "qcf_request_prefill: lm head");
     x_final = rl.x;
   }
@@ -1120,7 +1124,7 @@ size_t qcf_full_prefill_workspace_size(const qcf_dims* dims, int T) {
   Carve c{nullptr, 0};
   c.take<float>(static_cast<size_t>(T) * dims->d_model);
   c.take<int32_t>(T);
-  c.take<uint8_t>(256);
+  c.take<uint8_t>(qcf_lm_head_workspace_size(dims));
   c.take<uint8_t>(layer_ws_bytes(*dims, T, T));
   return c.used;
 }
@@ -1142,7 +1146,7 @@ qcf_status qcf_full_prefill(const qcf_model* m, const int32_t* ids, int T, qcf_b
   Carve c{static_cast<uint8_t*>(ws), ws_bytes};
   float* x = c.take<float>(static_cast<size_t>(T) * m->dims.d_model);
   int32_t* pos = c.take<int32_t>(T);
-  void* lm_ws = c.take<uint8_t>(256);
+  void* lm_ws = c.take<uint8_t>(qcf_lm_head_workspace_size(&m->dims));
   LayerBufs b;
   if (!carve_layer(c, m->dims, T, T, &b)) return set_error(QCF_ERR_WORKSPACE, "qcf_full_prefill: workspace");
   if ((s = gemm_ws_prepare(b.gemm_ws, b.gemm_ws_bytes, st)) != QCF_OK) return s;

@@ -113,9 +113,10 @@ qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const 
 
 // Row kernels (rows.cu).
 cudaError_t launch_embed(const __nv_bfloat16* embed, int vocab, int d, const int32_t* ids, const int32_t* rows,
-                         int row_offset, int n, float* x, cudaStream_t st);
+                         int row_offset, int n, float* x, cudaStream_t st, bool pdl = false);
+// best_ws: qcf_lm_head_workspace_size() bytes (one argmax key per CTA)
 cudaError_t launch_lm_head(const qcf_model* m, const float* x_last, float* logits, int32_t* token, void* best_ws,
-                           cudaStream_t st);
+                           cudaStream_t st, bool pdl = false);
 cudaError_t launch_reposition(const __nv_bfloat16* src, __nv_bfloat16* dst, int64_t n_rows, int Hkv, int D,
                               const int32_t* seg_start, const int32_t* seg_delta, int n_seg, const qcf_rope_table* t,
                               cudaStream_t st);
@@ -135,6 +136,9 @@ size_t profile_tc_workspace_size(int nq, int C, int Hq, int Hkv);
 qcf_status profile_tc_launch(const __nv_bfloat16* q, const __nv_bfloat16* K, int nq, int C, int Hq, int Hkv,
                              float scale, float* scores, void* ws, cudaStream_t st);
 constexpr int kProfileTcMaxGroup = 16;  // heads per KV head served by the tensor-core profile
+// top-N on one CTA (select.cu): the body of qcf_topn_select, optionally launched
+// programmatically (the kernel waits for its predecessor before reading the scores)
+qcf_status topn_launch(const float* scores, int C, int N, int32_t* sel, cudaStream_t st, bool pdl);
 // exact top-N over a cooperative grid (topn_grid.cu); workspace and launch
 size_t topn_grid_workspace_size(int C);
 int topn_grid_max_scores();  // largest C whose CTAs all stay resident on the current device (0 if unknown)

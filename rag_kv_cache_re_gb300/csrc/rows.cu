@@ -1,5 +1,6 @@
 // Row-wise HBM-bound kernels: RoPE re-rotation of reused keys, row gather and
 // K/V scatter, embedding rows, RMSNorm, and the LM head with argmax.
+#include <algorithm>
 #include <cstring>
 
 #include "qcf_internal.cuh"
@@ -176,6 +177,8 @@ __global__ void scatter_kv_kernel(const __nv_bfloat16* __restrict__ k_new, const
 __global__ void embed_rows_kernel(const __nv_bfloat16* __restrict__ embed, int vocab, int d,
                                   const int32_t* __restrict__ ids, const int32_t* __restrict__ rows, int row_offset,
                                   int n, float* __restrict__ x, unsigned int* status) {
+  pdl_wait();  // ids and the row table may come from the kernel before
+  pdl_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= n) return;
@@ -249,13 +252,17 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
   return (static_cast<unsigned long long>(ord) << 32) | static_cast<unsigned int>(0xFFFFFFFFu - idx);
 }
 
-// logits = W_lm * RMSNorm(x_last) * g (fp32 h kept in shared memory); argmax by
-// atomicMax on (orderable value, inverted index) so ties keep the lowest index.
+// logits = W_lm * RMSNorm(x_last) * g (fp32 h kept in shared memory); argmax as the
+// largest (orderable value, inverted index) key, so ties keep the lowest index: each
+// CTA writes its best key to its own slot (nothing to clear first), and
+// argmax_finalize_kernel takes the largest slot.
 __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ x_last, int d, int vocab,
                                                       const __nv_bfloat16* __restrict__ g, float eps,
                                                       const __nv_bfloat16* __restrict__ W,
                                                       float* __restrict__ logits,
                                                       unsigned long long* __restrict__ best) {
+  pdl_wait();  // x_last comes from the kernel before
+  pdl_launch_dependents();
   extern __shared__ float hs[];
   __shared__ float red[8];
   __shared__ unsigned long long bred[8];
@@ -312,39 +319,59 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
   if (threadIdx.x == 0) {
     unsigned long long b = 0ull;
     for (int w = 0; w < 8; ++w) b = bred[w] > b ? bred[w] : b;
-    atomicMax(best, b);
+    best[blockIdx.x] = b;
   }
 }
 
-__global__ void argmax_finalize_kernel(const unsigned long long* best, int32_t* token) {
-  *token = static_cast<int32_t>(0xFFFFFFFFu - static_cast<unsigned int>(*best & 0xFFFFFFFFull));
+// One warp: the largest of the LM head's n per-CTA keys.
+__global__ void argmax_finalize_kernel(const unsigned long long* best, int n, int32_t* token) {
+  pdl_wait();
+  unsigned long long b = 0ull;
+  for (int i = threadIdx.x; i < n; i += 32) b = best[i] > b ? best[i] : b;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, b, o);
+    b = y > b ? y : b;
+  }
+  if (threadIdx.x == 0) *token = static_cast<int32_t>(0xFFFFFFFFu - static_cast<unsigned int>(b & 0xFFFFFFFFull));
 }
 
 cudaError_t launch_embed(const __nv_bfloat16* embed, int vocab, int d, const int32_t* ids, const int32_t* rows,
-                         int row_offset, int n, float* x, cudaStream_t st) {
+                         int row_offset, int n, float* x, cudaStream_t st, bool pdl) {
   if (n <= 0) return cudaSuccess;
   LaunchScope ls(KC_EMBED, st);
+  if (pdl)
+    return launch_pdl(embed_rows_kernel, dim3((n + 7) / 8), dim3(256), 0, st, embed, vocab, d, ids, rows, row_offset,
+                      n, x, device_status_ptr());
   embed_rows_kernel<<<(n + 7) / 8, 256, 0, st>>>(embed, vocab, d, ids, rows, row_offset, n, x, device_status_ptr());
   return cudaGetLastError();
 }
 
+// CTAs of the LM head: four per SM, at most kLmHeadSlots (one argmax key slot each).
+constexpr int kLmHeadSlots = 4096;
+static int lm_head_ctas() { return std::min(4 * num_sms(), kLmHeadSlots); }
+
 cudaError_t launch_lm_head(const qcf_model* m, const float* x_last, float* logits, int32_t* token, void* best_ws,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool pdl) {
   unsigned long long* best = static_cast<unsigned long long*>(best_ws);
-  cudaError_t e = cudaMemsetAsync(best, 0, sizeof(unsigned long long), st);
-  if (e != cudaSuccess) return e;
-  const int d = m->dims.d_model;
+  const int d = m->dims.d_model, ctas = lm_head_ctas();
+  const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(m->g_final);
+  const __nv_bfloat16* W = reinterpret_cast<const __nv_bfloat16*>(m->lm_head);
+  cudaError_t e;
   {
     LaunchScope ls(KC_LMHEAD, st);
-    lm_head_kernel<<<4 * num_sms(), 256, d * sizeof(float), st>>>(
-        x_last, d, m->dims.vocab, reinterpret_cast<const __nv_bfloat16*>(m->g_final), m->dims.eps,
-        reinterpret_cast<const __nv_bfloat16*>(m->lm_head), logits, best);
+    if (pdl) {
+      e = launch_pdl(lm_head_kernel, dim3(ctas), dim3(256), d * sizeof(float), st, x_last, d, m->dims.vocab, g,
+                     m->dims.eps, W, logits, best);
+    } else {
+      lm_head_kernel<<<ctas, 256, d * sizeof(float), st>>>(x_last, d, m->dims.vocab, g, m->dims.eps, W, logits, best);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
   }
-  {
-    LaunchScope ls(KC_LMHEAD, st);
-    argmax_finalize_kernel<<<1, 1, 0, st>>>(best, token);
-  }
-  return cudaGetLastError();
+  LaunchScope ls(KC_LMHEAD, st);
+  return launch_pdl(argmax_finalize_kernel, dim3(1), dim3(32), 0, st, static_cast<const unsigned long long*>(best),
+                    ctas, token);
 }
 
 cudaError_t launch_rmsnorm(const float* x, int n, int d, const __nv_bfloat16* g, float eps, __nv_bfloat16* h,
@@ -491,7 +518,7 @@ qcf_status qcf_embed_rows(const qcf_model* m, const int32_t* ids, const int32_t*
 
 size_t qcf_lm_head_workspace_size(const qcf_dims* dims) {
   (void)dims;
-  return 256;
+  return kLmHeadSlots * sizeof(unsigned long long);
 }
 
 qcf_status qcf_lm_head(const qcf_model* m, const float* x_last, float* logits, int32_t* token, void* ws,

@@ -212,6 +212,8 @@ __device__ __forceinline__ int topn_level_bins(int lv) { return lv == 2 ? 1024 :
 
 __global__ void __launch_bounds__(kTopnThreads, 1) topn_kernel(const float* __restrict__ scores, int C, int N,
                                                             int32_t* __restrict__ sel) {
+  pdl_wait();  // the scores come from the kernel before
+  pdl_launch_dependents();
   extern __shared__ __align__(16) unsigned int tsm[];
   unsigned int* ckey = tsm;                                 // [kTopnCap] candidate keys
   int* cidx = reinterpret_cast<int*>(tsm + kTopnCap);       // [kTopnCap] candidate indices
@@ -439,6 +441,29 @@ cudaError_t launch_kv_deviation(const __nv_bfloat16* k_new, const __nv_bfloat16*
 
 using namespace qcf;
 
+namespace qcf {
+qcf_status topn_launch(const float* scores, int C, int N, int32_t* sel, cudaStream_t st, bool pdl) {
+  if (!scores || (!sel && N > 0)) return set_error(QCF_ERR_INVALID_ARG, "qcf_topn_select: NULL pointer");
+  if (C < 0 || C > (1 << 24) || N < 0 || N > C) return set_error(QCF_ERR_SHAPE, "qcf_topn_select: C=%d N=%d", C, N);
+  if (take_fault(4) || !aligned16(scores)) return set_error(QCF_ERR_ALIGN, "qcf_topn_select: scores not 16-byte aligned");
+  if (N == 0) return QCF_OK;
+  static PerDevice<cudaError_t> smem_attr;
+  const cudaError_t attr = smem_attr.get(current_device(), [] {
+    return cudaFuncSetAttribute(topn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopnSmem);
+  });
+  if (attr != cudaSuccess) return cuda_error(attr, "qcf_topn_select: smem attribute");
+  LaunchScope ls(KC_TOPN, st);
+  cudaError_t e;
+  if (pdl) {
+    e = launch_pdl(topn_kernel, dim3(1), dim3(kTopnThreads), kTopnSmem, st, scores, C, N, sel);
+  } else {
+    topn_kernel<<<1, kTopnThreads, kTopnSmem, st>>>(scores, C, N, sel);
+    e = cudaGetLastError();
+  }
+  return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_topn_select: launch");
+}
+}  // namespace qcf
+
 extern "C" {
 
 qcf_status qcf_anchor_keynorm_topk(const qcf_bf16* K, const int32_t* chunk_start, int n_chunks, int Hkv, int D,
@@ -496,20 +521,7 @@ qcf_status qcf_kv_deviation(const qcf_bf16* k_new, const qcf_bf16* v_new, const 
 }
 
 qcf_status qcf_topn_select(const float* scores, int C, int N, int32_t* sel, void* stream) {
-  if (!scores || (!sel && N > 0)) return set_error(QCF_ERR_INVALID_ARG, "qcf_topn_select: NULL pointer");
-  if (C < 0 || C > (1 << 24) || N < 0 || N > C) return set_error(QCF_ERR_SHAPE, "qcf_topn_select: C=%d N=%d", C, N);
-  if (take_fault(4) || !aligned16(scores)) return set_error(QCF_ERR_ALIGN, "qcf_topn_select: scores not 16-byte aligned");
-  if (N == 0) return QCF_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  static PerDevice<cudaError_t> smem_attr;
-  const cudaError_t attr = smem_attr.get(current_device(), [] {
-    return cudaFuncSetAttribute(topn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopnSmem);
-  });
-  if (attr != cudaSuccess) return cuda_error(attr, "qcf_topn_select: smem attribute");
-  LaunchScope ls(KC_TOPN, st);
-  topn_kernel<<<1, kTopnThreads, kTopnSmem, st>>>(scores, C, N, sel);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? QCF_OK : cuda_error(e, "qcf_topn_select: launch");
+  return topn_launch(scores, C, N, sel, static_cast<cudaStream_t>(stream), false);
 }
 
 size_t qcf_topn_select_workspace_size(int C) {
