@@ -274,6 +274,8 @@ struct RequestLayout {
   void* prof_ws;
   size_t prof_ws_bytes;
   void* lm_ws;
+  void* topn_ws;         // the cooperative top-N's scratch (context above 16384 tokens)
+  size_t topn_ws_bytes;
 };
 
 static bool carve_request(Carve& c, const qcf_dims& d, int C, int Q, int nA, int N, int n_chunks, int crit,
@@ -307,6 +309,8 @@ static bool carve_request(Carve& c, const qcf_dims& d, int C, int Q, int nA, int
   r->scores_acc = c.take<float>(C);
   r->scores_tmp = c.take<float>(C);
   r->sel = c.take<int32_t>(N > 0 ? N : 1);
+  r->topn_ws_bytes = qcf_topn_select_workspace_size(C);   // 0 up to 16384 context tokens
+  r->topn_ws = c.take<uint8_t>(r->topn_ws_bytes > 0 ? r->topn_ws_bytes : 1);
   r->prof_ws_bytes = qcf_profile_scores_workspace_size(Q, C, d.n_heads, d.n_kv_heads, d.head_dim);
   r->prof_ws = c.take<uint8_t>(r->prof_ws_bytes);
   r->lm_ws = c.take<uint8_t>(qcf_lm_head_workspace_size(&d));
@@ -977,7 +981,9 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
         if ((e = cudaMemcpyAsync(sel, r->forced_sel, N * sizeof(int32_t), cudaMemcpyDeviceToDevice, cs)) != cudaSuccess)
           return cuda_error(e, "qcf_request_prefill: forced selection");
       } else {
-        s = topn_launch(scores, C, N, sel, cs, true);
+        // above 16384 context tokens the selection spreads over a cooperative grid
+        s = rl.topn_ws_bytes > 0 ? qcf_topn_select_ws(scores, C, N, sel, rl.topn_ws, rl.topn_ws_bytes, cs)
+                                 : topn_launch(scores, C, N, sel, cs, true);
         if (s != QCF_OK) return s;
       }
     }
