@@ -473,21 +473,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int h = g * G + hh;
     if (check && valid && (prow < 0 || prow >= T || (r > 0 && pos[r - 1] >= prow))) flag_status(status, QCF_DEV_BAD_INDEX);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    {  // the Q row into TMEM as 64 packed bf16 pairs
+    {  // the Q row into TMEM as 64 packed bf16 pairs (all 16 loads in flight before the stores)
       const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(valid ? r : 0) * Hq + h) * D);
+      uint32_t w[64];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t w[32];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 v = valid ? src[half * 8 + ch] : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * ch] = v.x;
-          w[4 * ch + 1] = v.y;
-          w[4 * ch + 2] = v.z;
-          w[4 * ch + 3] = v.w;
-        }
-        tmem_st32u(tmem_base + lane_base + kTcQCol + half * 32, w);
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * ch] = v.x;
+        w[4 * ch + 1] = v.y;
+        w[4 * ch + 2] = v.z;
+        w[4 * ch + 3] = v.w;
       }
+      tmem_st32u(tmem_base + lane_base + kTcQCol, w);
+      tmem_st32u(tmem_base + lane_base + kTcQCol + 32, w + 32);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
