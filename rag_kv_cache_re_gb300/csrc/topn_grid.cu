@@ -17,7 +17,8 @@
 //            candidate list
 //   resolve  every CTA loads the candidates into shared memory and finishes the
 //            selection there (the remaining key bits give K* and how many K*-valued keys
-//            are taken; two 12-bit rounds over their indices give the last index taken)
+//            are taken; one warp ranks their indices when at most 32 keys equal K*, else
+//            two 12-bit rounds over the indices give the last index taken)
 //   output   each CTA publishes how many of its scores are taken; after the last barrier
 //            it writes its taken indices, in order, at the sum of the counts before it
 // When every key bit is fixed and still more than kGridCap keys equal K*, the CTAs
@@ -43,7 +44,7 @@ constexpr int kGridSmem = 2 * kGridCap * 4 + kGridHistMax * 4;   // candidate ke
 // candidate list and per-CTA counts.
 constexpr size_t kGridCtlWords = 64;
 constexpr size_t kGridHistWords = 2048 + 2048 + 1024;
-constexpr size_t kGridZeroBytes = (kGridCtlWords + kGridHistWords) * 4;
+constexpr size_t kGridHeadBytes = (kGridCtlWords + kGridHistWords) * 4;   // control words and histograms
 
 __device__ __forceinline__ unsigned int grid_order_key(float f) {
   unsigned int b = __float_as_uint(f);
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kGridThreads, 1)
 
 size_t topn_grid_workspace_size(int C) {
   const int G = (C + kGridSlice - 1) / kGridSlice;
-  return kGridZeroBytes + static_cast<size_t>(2 * kGridCap) * 4 + static_cast<size_t>(2 * G) * 4 + 256;
+  return kGridHeadBytes + static_cast<size_t>(2 * kGridCap) * 4 + static_cast<size_t>(2 * G) * 4 + 256;
 }
 
 static int topn_grid_capacity() {
