@@ -1422,24 +1422,32 @@ qcf_status qcf_batch_prefill(const qcf_model* m, const qcf_request* reqs, const 
       if ((e = cudaEventRecord(ev_crit_of(i), xs)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: record");
     }
   }
-  for (int l = 0; l < L; ++l) {
-    bool need_k = false;
-    for (int i = 0; i < n_req; ++i) need_k |= P[i].crit != l;
-    const int b = l & 1;
-    if ((e = stage(l, need_k ? B.K[b] : nullptr, B.V[b])) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: layer copy");
-    for (int i = 0; i < n_req; ++i) {
-      if ((e = launch_stage_scatter(B.K[b], B.V[b], B.src_row[i], B.delta[i], P[i].C, U.rows, d.n_kv_heads, d.head_dim,
-                                    &m->rope, reinterpret_cast<__nv_bfloat16*>(outs[i].K_layers[l]),
-                                    reinterpret_cast<__nv_bfloat16*>(outs[i].V_layers[l]), P[i].crit != l, true, xs)) !=
-          cudaSuccess)
-        return cuda_error(e, "qcf_batch_prefill: scatter");
-      if ((e = cudaEventRecord(ev_layer_of(i)[l], xs)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: record");
+  // the per-layer staging copies (most of the host's calls) are enqueued after the first
+  // request's probe launches, as for a single request
+  auto enqueue_layers = [&]() -> qcf_status {
+    for (int l = 0; l < L; ++l) {
+      bool need_k = false;
+      for (int i = 0; i < n_req; ++i) need_k |= P[i].crit != l;
+      const int b = l & 1;
+      if ((e = stage(l, need_k ? B.K[b] : nullptr, B.V[b])) != cudaSuccess)
+        return cuda_error(e, "qcf_batch_prefill: layer copy");
+      for (int i = 0; i < n_req; ++i) {
+        if ((e = launch_stage_scatter(B.K[b], B.V[b], B.src_row[i], B.delta[i], P[i].C, U.rows, d.n_kv_heads,
+                                      d.head_dim, &m->rope, reinterpret_cast<__nv_bfloat16*>(outs[i].K_layers[l]),
+                                      reinterpret_cast<__nv_bfloat16*>(outs[i].V_layers[l]), P[i].crit != l, true,
+                                      xs)) != cudaSuccess)
+          return cuda_error(e, "qcf_batch_prefill: scatter");
+        if ((e = cudaEventRecord(ev_layer_of(i)[l], xs)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: record");
+      }
     }
-  }
-  if (h2d_bytes) *h2d_bytes = h2d;
+    if (h2d_bytes) *h2d_bytes = h2d;
+    return QCF_OK;
+  };
   // compute: the requests one after another, each waiting only for the layers it reaches
   for (int i = 0; i < n_req; ++i) {
-    qcf_status s = request_compute(m, &reqs[i], &outs[i], P[i], cs, ev_anchor, ev_crit_of(i), ev_layer_of(i));
+    P[i].wait_stride = kPinnedWaitStride;
+    qcf_status s = request_compute(m, &reqs[i], &outs[i], P[i], cs, ev_anchor, ev_crit_of(i), ev_layer_of(i),
+                                   i == 0 ? std::function<qcf_status()>(enqueue_layers) : std::function<qcf_status()>());
     if (s != QCF_OK) return s;
   }
   return QCF_OK;
