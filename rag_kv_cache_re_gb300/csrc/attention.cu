@@ -331,7 +331,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                           const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ pos, int n, int T, int Hq,
                           int Hkv, int G, int BRp, float scale_log2, __nv_bfloat16* __restrict__ o,
                           float* __restrict__ lse, int split_tiles, int max_splits, float* __restrict__ part_o,
-                          float2* __restrict__ part_ml, unsigned int* status, int check, int heads_fast) {
+                          float2* __restrict__ part_ml, unsigned int* status, int check, int heads_fast,
+                          const int32_t* __restrict__ key0) {
   constexpr int D = 128;
   pdl_wait();  // q, pos and the cache come from the kernels before this one
   pdl_launch_dependents();
@@ -359,7 +360,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int g = static_cast<int>(heads_fast ? blockIdx.x : blockIdx.y);
   const int row0 = rb * BRp;
   const int row_end = min(n, row0 + BRp);
-  const int n_tiles_all = pos[row_end - 1] / kTcKeys + 1;
+  // the block's keys start at cache row kbase (several requests' caches in one buffer);
+  // its positions count from there
+  const int kbase = key0 ? key0[rb] : 0;
+  const int n_tiles_all = (pos[row_end - 1] - kbase) / kTcKeys + 1;
   const int t_begin = sp * split_tiles;
   if (t_begin >= n_tiles_all) return;
   const int t_end = min(n_tiles_all, t_begin + split_tiles);
@@ -410,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t* dst = ring + st * kTcKVBytes;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2)
-          tma_load_2d(dst + h2 * kTcBoxBytes, map, bar, g * D + h2 * 64, (t_begin + i) * kTcKeys);
+          tma_load_2d(dst + h2 * kTcBoxBytes, map, bar, g * D + h2 * 64, kbase + (t_begin + i) * kTcKeys);
       }
       // the last two groups have no K tile to wait for: their K share of the count arrives now
       if (is_k && ok)
@@ -469,9 +473,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int p_local = rho / G, hh = rho - p_local * G;
     const int r = row0 + p_local;
     const bool valid = p_local < BRp && r < row_end;
-    const int prow = valid ? pos[r] : -1;
+    const int prow = valid ? pos[r] - kbase : -1;   // relative to the block's first key
     const int h = g * G + hh;
-    if (check && valid && (prow < 0 || prow >= T || (r > 0 && pos[r - 1] >= prow))) flag_status(status, QCF_DEV_BAD_INDEX);
+    // positions ascend over all rows, or within each block when blocks have their own key base
+    if (check && valid && (prow < 0 || prow + kbase >= T || (r > (key0 ? row0 : 0) && pos[r - 1] - kbase >= prow)))
+      flag_status(status, QCF_DEV_BAD_INDEX);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     {  // the Q row into TMEM as 64 packed bf16 pairs (all 16 loads in flight before the stores)
       const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(valid ? r : 0) * Hq + h) * D);
@@ -709,9 +715,14 @@ size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D) {
 template <int D>
 static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,
                                 const __nv_bfloat16* V, int T, int Hq, int Hkv, float scale, __nv_bfloat16* o,
-                                float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc, bool pdl) {
+                                float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc, bool pdl,
+                                const int32_t* key0) {
   using Cfg = AttnCfg<D>;
-  const AttnPlan plan = plan_attn(n, T, Hq, Hkv, D);
+  AttnPlan plan = plan_attn(n, T, Hq, Hkv, D);
+  if (key0) {  // blocks with their own key base: whole key ranges only (the combine reads positions from 0)
+    plan.split_tiles = (T + plan.tile - 1) / plan.tile;
+    plan.max_splits = 1;
+  }
   const int G = plan.G;
   const int BR = plan.BR;
   const int warps = G * (BR / 16);
@@ -756,12 +767,13 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
     if (pdl) {
       cudaError_t e = launch_pdl(sparse_attn_tc_kernel, grid, dim3(kTcThreads), kTcSmem, st, tk, tv, q, pos, n, T, Hq,
                                  Hkv, G, BR, scale_log2, o, lse, plan.split_tiles, plan.max_splits, part_o, part_ml,
-                                 device_status_ptr(), check_enabled() ? 1 : 0, heads_fast);
+                                 device_status_ptr(), check_enabled() ? 1 : 0, heads_fast, key0);
       if (e != cudaSuccess) return cuda_error(e, "sparse_causal_attn: launch");
     } else {
       sparse_attn_tc_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tk, tv, q, pos, n, T, Hq, Hkv, G, BR, scale_log2, o, lse,
                                                                 plan.split_tiles, plan.max_splits, part_o, part_ml,
-                                                                device_status_ptr(), check_enabled() ? 1 : 0, heads_fast);
+                                                                device_status_ptr(), check_enabled() ? 1 : 0, heads_fast,
+                                                                key0);
     }
   } else {
     LaunchScope ls(kc, st);
@@ -787,12 +799,13 @@ static qcf_status attn_launch_d(const __nv_bfloat16* q, const int32_t* pos, int 
 
 qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K, const __nv_bfloat16* V,
                        int T, int Hq, int Hkv, int D, float scale, __nv_bfloat16* o, float* lse, void* ws,
-                       size_t ws_bytes, cudaStream_t st, KernelClass kc, bool pdl) {
+                       size_t ws_bytes, cudaStream_t st, KernelClass kc, bool pdl, const int32_t* key0) {
   if (n <= 0) return QCF_OK;
+  if (key0 && D != 128) return set_error(QCF_ERR_UNSUPPORTED, "sparse_causal_attn: per-block key bases need D = 128");
   switch (D) {  // the warp-MMA kernel (D = 16, 64) is launched plainly; its combine may still be programmatic
-    case 16: return attn_launch_d<16>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl);
-    case 64: return attn_launch_d<64>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl);
-    case 128: return attn_launch_d<128>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl);
+    case 16: return attn_launch_d<16>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl, nullptr);
+    case 64: return attn_launch_d<64>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl, nullptr);
+    case 128: return attn_launch_d<128>(q, pos, n, K, V, T, Hq, Hkv, scale, o, lse, ws, ws_bytes, st, kc, pdl, key0);
     default: return set_error(QCF_ERR_SHAPE, "sparse_causal_attn: head dim %d unsupported", D);
   }
 }

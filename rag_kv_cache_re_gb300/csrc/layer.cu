@@ -118,7 +118,7 @@ constexpr int kPdlMaxRows = 2048;
 static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, const int32_t* rope_pos,
                                      const int32_t* cache_row, int n, __nv_bfloat16* Kc, __nv_bfloat16* Vc, int T,
                                      const LayerBufs& b, cudaStream_t st, bool probe = false,
-                                     bool first_pdl = false) {
+                                     bool first_pdl = false, const int32_t* key0 = nullptr) {
   const qcf_dims& d = m->dims;
   const qcf_layer_weights& w = m->layers[layer];
   const int D = d.head_dim, Hq = d.n_heads, Hkv = d.n_kv_heads;
@@ -145,7 +145,7 @@ static qcf_status layer_forward_impl(const qcf_model* m, int layer, float* x, co
                              false, pdl, b.gemm_zeroed);
   if (s != QCF_OK) return s;
   s = attn_launch(b.q, cache_row, n, Kc, Vc, T, Hq, Hkv, D, 1.0f / sqrtf(static_cast<float>(D)), b.o, nullptr, b.attn_ws,
-                  b.attn_ws_bytes, st, probe ? KC_ATTN_PROBE : KC_ATTN, pdl);
+                  b.attn_ws_bytes, st, probe ? KC_ATTN_PROBE : KC_ATTN, pdl, key0);
   if (s != QCF_OK) return s;
   EpiParams eo{};
   eo.out = x;
@@ -840,7 +840,8 @@ static qcf_status request_copy_layers_storage(const qcf_model* m, const qcf_outp
 static qcf_status request_compute(const qcf_model* m, const qcf_request* r, const qcf_outputs* out, ReqPlan& P,
                                   cudaStream_t cs, cudaEvent_t ev_anchor, cudaEvent_t ev_crit,
                                   const cudaEvent_t* ev_layer,
-                                  const std::function<qcf_status()>& enqueue_layers = {}) {
+                                  const std::function<qcf_status()>& enqueue_layers = {},
+                                  bool probe_done = false) {
   const qcf_dims& d = m->dims;
   const int L = d.n_layers;
   const bool all_layers = P.all_layers, hkvd = P.hkvd;
@@ -901,70 +902,73 @@ static qcf_status request_compute(const qcf_model* m, const qcf_request* r, cons
                             H.lm_ws, cs)) != cudaSuccess)
       return cuda_error(e, "qcf_request_prefill: lm head");
   } else {
-    // probe: query rows at positions C..T-1 with the anchors as KV prefix (probe cache rows 0..nA-1)
-    if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, nullptr, C, Q, rl.x, cs)) != cudaSuccess)
-      return cuda_error(e, "qcf_request_prefill: embed");
-    {
-      LaunchScope ls(KC_MISC, cs);
-      iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_pos, Q, C);
-    }
-    {
-      LaunchScope ls(KC_MISC, cs);
-      iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_row, Q, nA);
-    }
     const float scale = 1.0f / sqrtf(static_cast<float>(d.head_dim));
     if (all_layers && (e = cudaMemsetAsync(rl.scores_acc, 0, static_cast<size_t>(C) * sizeof(float), cs)) != cudaSuccess)
       return cuda_error(e, "qcf_request_prefill: clear scores");
     if (all_layers && (s = layers_now()) != QCF_OK) return s;   // the probe profiles every layer
-    if (crit > 0) {
-      if ((e = cudaStreamWaitEvent(cs, ev_anchor, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
-      const size_t pstride = static_cast<size_t>(nA + Q) * d.n_kv_heads * d.head_dim;
-      if (nA > 0) {
-        const long long threads = static_cast<long long>(crit) * nA * d.n_kv_heads * (d.head_dim / 16);
-        LaunchScope ls(KC_ROPE, cs);
-        anchor_assemble_kernel<<<static_cast<unsigned int>((threads + 255) / 256), 256, 0, cs>>>(
-            rl.stK, rl.stV, crit, A, d.n_kv_heads, d.head_dim, m->rope.cos, m->rope.sin, co, rl.pK, rl.pV, pstride);
+    // probe (unless a batch ran it for several requests at once): query rows at positions
+    // C..T-1 with the anchors as KV prefix (probe cache rows 0..nA-1), then q at the critical layer
+    if (!probe_done) {
+      if ((e = launch_embed(embed, d.vocab, d.d_model, r->ids, nullptr, C, Q, rl.x, cs)) != cudaSuccess)
+        return cuda_error(e, "qcf_request_prefill: embed");
+      {
+        LaunchScope ls(KC_MISC, cs);
+        iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_pos, Q, C);
       }
-      for (int l = 0; l < crit; ++l) {
-        // consecutive probe layers follow each other directly (QCAll puts a profile and an
-        // event wait between them): their first launch is programmatic too
-        s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK + l * pstride, rl.pV + l * pstride,
-                               nA + Q, rl.lb, cs, true, !all_layers);
-        if (s != QCF_OK) return s;
-        if (all_layers) {   // QCAll: this probe layer's q against this layer's re-rotated keys
-          if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
-          s = qcf_profile_scores(reinterpret_cast<const qcf_bf16*>(rl.lb.q), out->K_layers[l], Q, C, d.n_heads,
-                                 d.n_kv_heads, d.head_dim, scale, rl.scores_tmp, rl.prof_ws, rl.prof_ws_bytes, cs);
+      {
+        LaunchScope ls(KC_MISC, cs);
+        iota_kernel<<<(Q + 255) / 256, 256, 0, cs>>>(rl.probe_row, Q, nA);
+      }
+      if (crit > 0) {
+        if ((e = cudaStreamWaitEvent(cs, ev_anchor, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+        const size_t pstride = static_cast<size_t>(nA + Q) * d.n_kv_heads * d.head_dim;
+        if (nA > 0) {
+          const long long threads = static_cast<long long>(crit) * nA * d.n_kv_heads * (d.head_dim / 16);
+          LaunchScope ls(KC_ROPE, cs);
+          anchor_assemble_kernel<<<static_cast<unsigned int>((threads + 255) / 256), 256, 0, cs>>>(
+              rl.stK, rl.stV, crit, A, d.n_kv_heads, d.head_dim, m->rope.cos, m->rope.sin, co, rl.pK, rl.pV, pstride);
+        }
+        for (int l = 0; l < crit; ++l) {
+          // consecutive probe layers follow each other directly (QCAll puts a profile and an
+          // event wait between them): their first launch is programmatic too
+          s = layer_forward_impl(m, l, rl.x, rl.probe_pos, rl.probe_row, Q, rl.pK + l * pstride, rl.pV + l * pstride,
+                                 nA + Q, rl.lb, cs, true, !all_layers);
           if (s != QCF_OK) return s;
-          LaunchScope ls(KC_MISC, cs);
-          add_f32_kernel<<<(C + 255) / 256, 256, 0, cs>>>(rl.scores_acc, rl.scores_tmp, C);
+          if (all_layers) {   // QCAll: this probe layer's q against this layer's re-rotated keys
+            if ((e = cudaStreamWaitEvent(cs, ev_layer[l], 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
+            s = qcf_profile_scores(reinterpret_cast<const qcf_bf16*>(rl.lb.q), out->K_layers[l], Q, C, d.n_heads,
+                                   d.n_kv_heads, d.head_dim, scale, rl.scores_tmp, rl.prof_ws, rl.prof_ws_bytes, cs);
+            if (s != QCF_OK) return s;
+            LaunchScope ls(KC_MISC, cs);
+            add_f32_kernel<<<(C + 255) / 256, 256, 0, cs>>>(rl.scores_acc, rl.scores_tmp, C);
+          }
         }
       }
-    }
-    // critical layer: q = RoPE(RMSNorm(x) W_q) only
-    {
-      const qcf_layer_weights& w = m->layers[crit];
-      // programmatic when it follows the last probe layer's down projection directly
-      if ((e = launch_rmsnorm(rl.x, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, rl.lb.h, cs,
-                              crit > 0 && !all_layers && Q <= kPdlMaxRows)) != cudaSuccess)
-        return cuda_error(e, "qcf_request_prefill: rmsnorm");
-      EpiParams ep{};
-      ep.q_out = q_crit;
-      ep.rope_pos = rl.probe_pos;
-      ep.cache_row = nullptr;
-      ep.cos_t = m->rope.cos;
-      ep.sin_t = m->rope.sin;
-      ep.Hq = d.n_heads;
-      ep.Hkv = d.n_kv_heads;
-      ep.D = d.head_dim;
-      ep.T = 1;
-      ep.max_pos = m->rope.max_pos;
-      ep.status = device_status_ptr();
-      s = gemm_launch(EPI_QKV_ROPE, rl.lb.h, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
-                      d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_PROBE, false, Q <= kPdlMaxRows,
-                      rl.lb.gemm_zeroed);
-      if (s != QCF_OK) return s;
-    }
+      // critical layer: q = RoPE(RMSNorm(x) W_q) only
+      {
+        const qcf_layer_weights& w = m->layers[crit];
+        // programmatic when it follows the last probe layer's down projection directly
+        if ((e = launch_rmsnorm(rl.x, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, rl.lb.h, cs,
+                                crit > 0 && !all_layers && Q <= kPdlMaxRows)) != cudaSuccess)
+          return cuda_error(e, "qcf_request_prefill: rmsnorm");
+        EpiParams ep{};
+        ep.q_out = q_crit;
+        ep.rope_pos = rl.probe_pos;
+        ep.cache_row = nullptr;
+        ep.cos_t = m->rope.cos;
+        ep.sin_t = m->rope.sin;
+        ep.Hq = d.n_heads;
+        ep.Hkv = d.n_kv_heads;
+        ep.D = d.head_dim;
+        ep.T = 1;
+        ep.max_pos = m->rope.max_pos;
+        ep.status = device_status_ptr();
+        s = gemm_launch(EPI_QKV_ROPE, rl.lb.h, Q, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
+                        d.n_heads * d.head_dim, ep, rl.lb.gemm_ws, rl.lb.gemm_ws_bytes, cs, KC_GEMM_PROBE, false, Q <= kPdlMaxRows,
+                        rl.lb.gemm_zeroed);
+        if (s != QCF_OK) return s;
+      }
+    }  // probe
     if ((s = layers_now()) != QCF_OK) return s;
     // profile the re-rotated critical-layer keys and select
     if ((e = cudaStreamWaitEvent(cs, ev_crit, 0)) != cudaSuccess) return cuda_error(e, "qcf_request_prefill: wait");
@@ -1092,6 +1096,171 @@ static bool carve_staging(Carve& c, const qcf_dims& d, const UniqueChunks& U, co
 }  // namespace qcf
 
 using namespace qcf;
+
+// ------------------------------------------------------------------ merged probe of a batch
+//
+// Requests of a batch that share their critical layer (QCFuse selector, head dim 128) run
+// the probe together: their query rows, each request's padded to whole attention row
+// blocks, go through the probe layers as one row set, so each probe layer's weights
+// stream once for the group instead of once per request.  Each request keeps its anchors
+// and query K/V in its own segment of one probe cache, and each attention row block reads
+// keys from its own request's segment only.  A group holds at most 128 rows: the GEMMs
+// then take the plan of a single request's probe and every row is computed as in its own
+// request's probe, so each request's q at the critical layer is bitwise what it would be
+// alone.
+constexpr int kMergedProbeRows = 128;
+
+struct MergedProbeMeta {
+  int n;
+  int C[kMaxBatch], Q[kMaxBatch], nA[kMaxBatch], roff[kMaxBatch], seg[kMaxBatch];
+};
+
+// Row tables of a merged probe: RoPE position (a padding row repeats its request's last
+// query position), cache row in the shared probe cache, and each row block's key base.
+__global__ void merged_probe_tables_kernel(const MergedProbeMeta meta, int M, int BR, int32_t* __restrict__ pos,
+                                           int32_t* __restrict__ row, int32_t* __restrict__ key0) {
+  const int mr = blockIdx.x * blockDim.x + threadIdx.x;
+  if (mr >= M) return;
+  int i = 0;
+  while (i + 1 < meta.n && meta.roff[i + 1] <= mr) ++i;
+  const int j = mr - meta.roff[i];
+  pos[mr] = meta.C[i] + min(j, meta.Q[i] - 1);
+  row[mr] = meta.seg[i] + meta.nA[i] + j;
+  if (mr % BR == 0) key0[mr / BR] = meta.seg[i];
+}
+
+struct MergedProbe {
+  std::vector<int> members;   // request indices
+  MergedProbeMeta meta{};
+  int M = 0, S = 0, crit = 0;
+  float* x = nullptr;
+  int32_t *pos = nullptr, *row = nullptr, *key0 = nullptr;
+  __nv_bfloat16 *pK = nullptr, *pV = nullptr, *q = nullptr;
+  LayerBufs lb{};
+};
+
+// Groups of requests whose probes merge (consecutive requests with the same critical layer,
+// at most kMergedProbeRows padded rows per group); requests in no group of two or more
+// run their own probe.
+static std::vector<MergedProbe> merged_probe_groups(const qcf_dims& d, const qcf_request* reqs, int n_req) {
+  std::vector<MergedProbe> groups;
+  if (d.head_dim != 128 || d.n_heads % d.n_kv_heads) return groups;
+  const int BR = 128 / (d.n_heads / d.n_kv_heads);
+  MergedProbe cur;
+  auto flush = [&]() {
+    if (cur.members.size() >= 2) groups.push_back(cur);
+    cur = MergedProbe{};
+  };
+  for (int i = 0; i < n_req; ++i) {
+    const qcf_request& r = reqs[i];
+    const bool ok = r.selector == QCF_SELECT_CRITICAL && r.crit_layer > 0 && r.query_len > 0;
+    const int Qp = ok ? (r.query_len + BR - 1) / BR * BR : 0;
+    if (!ok || Qp > kMergedProbeRows) {
+      flush();
+      continue;
+    }
+    if (!cur.members.empty() && (cur.crit != r.crit_layer || cur.M + Qp > kMergedProbeRows)) flush();
+    const int k = static_cast<int>(cur.members.size());
+    int C = 0;
+    for (int c = 0; c < r.n_chunks; ++c) C += r.chunk_len[c];
+    const int nA = r.n_anchor * r.n_chunks;
+    cur.crit = r.crit_layer;
+    cur.meta.C[k] = C;
+    cur.meta.Q[k] = r.query_len;
+    cur.meta.nA[k] = nA;
+    cur.meta.roff[k] = cur.M;
+    cur.meta.seg[k] = cur.S;
+    cur.meta.n = k + 1;
+    cur.M += Qp;
+    cur.S += nA + Qp;
+    cur.members.push_back(i);
+  }
+  flush();
+  return groups;
+}
+
+static bool carve_merged_probe(Carve& c, const qcf_dims& d, MergedProbe* g) {
+  const int BR = 128 / (d.n_heads / d.n_kv_heads);
+  const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim;
+  g->x = c.take<float>(static_cast<size_t>(g->M) * d.d_model);
+  g->pos = c.take<int32_t>(g->M);
+  g->row = c.take<int32_t>(g->M);
+  g->key0 = c.take<int32_t>(g->M / BR);
+  g->pK = c.take<__nv_bfloat16>(static_cast<size_t>(g->crit) * g->S * HD);
+  g->pV = c.take<__nv_bfloat16>(static_cast<size_t>(g->crit) * g->S * HD);
+  g->q = c.take<__nv_bfloat16>(static_cast<size_t>(g->M) * d.n_heads * d.head_dim);
+  return carve_layer(c, d, g->M, g->S, &g->lb);
+}
+
+// The probe of one merged group, up to each member's q at the critical layer (written to
+// the member's own q_crit buffer).
+static qcf_status run_merged_probe(const qcf_model* m, const qcf_request* reqs, const std::vector<ReqPlan>& P,
+                                   MergedProbe& g, cudaStream_t cs, cudaEvent_t ev_anchor) {
+  const qcf_dims& d = m->dims;
+  const int BR = 128 / (d.n_heads / d.n_kv_heads), crit = g.crit;
+  const size_t HD = static_cast<size_t>(d.n_kv_heads) * d.head_dim;
+  const size_t pstride = static_cast<size_t>(g.S) * HD;
+  const size_t qrow = static_cast<size_t>(d.n_heads) * d.head_dim;
+  const __nv_bfloat16* embed = reinterpret_cast<const __nv_bfloat16*>(m->embed);
+  qcf_status s = gemm_ws_prepare(g.lb.gemm_ws, g.lb.gemm_ws_bytes, cs);
+  if (s != QCF_OK) return s;
+  g.lb.gemm_zeroed = true;
+  cudaError_t e;
+  {
+    LaunchScope ls(KC_MISC, cs);
+    merged_probe_tables_kernel<<<(g.M + 127) / 128, 128, 0, cs>>>(g.meta, g.M, BR, g.pos, g.row, g.key0);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: probe tables");
+  }
+  for (int k = 0; k < g.meta.n; ++k) {   // each member's query tokens (padding rows repeat the last)
+    const int Qp = (g.meta.Q[k] + BR - 1) / BR * BR;
+    if ((e = launch_embed(embed, d.vocab, d.d_model, reqs[g.members[k]].ids, g.pos + g.meta.roff[k], 0, Qp,
+                          g.x + static_cast<size_t>(g.meta.roff[k]) * d.d_model, cs)) != cudaSuccess)
+      return cuda_error(e, "qcf_batch_prefill: embed");
+  }
+  if ((e = cudaStreamWaitEvent(cs, ev_anchor, 0)) != cudaSuccess) return cuda_error(e, "qcf_batch_prefill: wait");
+  for (int k = 0; k < g.meta.n; ++k) {   // each member's anchor rows at the start of its segment
+    const ReqPlan& p = P[g.members[k]];
+    if (p.nA == 0) continue;
+    const long long threads = static_cast<long long>(crit) * p.nA * d.n_kv_heads * (d.head_dim / 16);
+    LaunchScope ls(KC_ROPE, cs);
+    anchor_assemble_kernel<<<static_cast<unsigned int>((threads + 255) / 256), 256, 0, cs>>>(
+        p.rl.stK, p.rl.stV, crit, p.A, d.n_kv_heads, d.head_dim, m->rope.cos, m->rope.sin, p.co,
+        g.pK + static_cast<size_t>(g.meta.seg[k]) * HD, g.pV + static_cast<size_t>(g.meta.seg[k]) * HD, pstride);
+  }
+  for (int l = 0; l < crit; ++l) {
+    s = layer_forward_impl(m, l, g.x, g.pos, g.row, g.M, g.pK + l * pstride, g.pV + l * pstride, g.S, g.lb, cs, true,
+                           l > 0, g.key0);
+    if (s != QCF_OK) return s;
+  }
+  const qcf_layer_weights& w = m->layers[crit];
+  if ((e = launch_rmsnorm(g.x, g.M, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.g_attn), d.eps, g.lb.h, cs,
+                          true)) != cudaSuccess)
+    return cuda_error(e, "qcf_batch_prefill: rmsnorm");
+  EpiParams ep{};
+  ep.q_out = g.q;
+  ep.rope_pos = g.pos;
+  ep.cache_row = nullptr;
+  ep.cos_t = m->rope.cos;
+  ep.sin_t = m->rope.sin;
+  ep.Hq = d.n_heads;
+  ep.Hkv = d.n_kv_heads;
+  ep.D = d.head_dim;
+  ep.T = 1;
+  ep.max_pos = m->rope.max_pos;
+  ep.status = device_status_ptr();
+  s = gemm_launch(EPI_QKV_ROPE, g.lb.h, g.M, d.d_model, reinterpret_cast<const __nv_bfloat16*>(w.w_qkv),
+                  d.n_heads * d.head_dim, ep, g.lb.gemm_ws, g.lb.gemm_ws_bytes, cs, KC_GEMM_PROBE, false, true,
+                  g.lb.gemm_zeroed);
+  if (s != QCF_OK) return s;
+  for (int k = 0; k < g.meta.n; ++k) {
+    const ReqPlan& p = P[g.members[k]];
+    if ((e = cudaMemcpyAsync(p.q_crit, g.q + static_cast<size_t>(g.meta.roff[k]) * qrow,
+                             static_cast<size_t>(p.Q) * qrow * sizeof(__nv_bfloat16), cudaMemcpyDeviceToDevice, cs)) !=
+        cudaSuccess)
+      return cuda_error(e, "qcf_batch_prefill: q copy");
+  }
+  return QCF_OK;
+}
 
 extern "C" {
 
@@ -1321,6 +1490,8 @@ size_t qcf_batch_workspace_size(const qcf_dims* dims, const qcf_request* reqs, i
   Carve c{nullptr, 0};
   BatchStaging B;
   carve_staging(c, *dims, U, Cs, &B);
+  std::vector<MergedProbe> groups = merged_probe_groups(*dims, reqs, n_req);
+  for (MergedProbe& g : groups) carve_merged_probe(c, *dims, &g);
   return total + c.used + 256;
 }
 
@@ -1347,6 +1518,12 @@ qcf_status qcf_batch_prefill(const qcf_model* m, const qcf_request* reqs, const 
   Carve cv{static_cast<uint8_t*>(ws) + off, ws_bytes - off};
   BatchStaging B;
   if (!carve_staging(cv, d, U, Cs, &B)) return set_error(QCF_ERR_WORKSPACE, "qcf_batch_prefill: workspace too small");
+  std::vector<MergedProbe> groups = merged_probe_groups(d, reqs, n_req);
+  std::vector<char> probe_done(n_req, 0);
+  for (MergedProbe& g : groups) {
+    if (!carve_merged_probe(cv, d, &g)) return set_error(QCF_ERR_WORKSPACE, "qcf_batch_prefill: workspace too small");
+    for (int i : g.members) probe_done[i] = 1;
+  }
   // row maps: request row -> staging row, and the rotation offset of its chunk in this request
   std::vector<std::vector<int32_t>> src_row(n_req), delta(n_req);
   for (int i = 0; i < n_req; ++i) {
@@ -1443,11 +1620,17 @@ qcf_status qcf_batch_prefill(const qcf_model* m, const qcf_request* reqs, const 
     if (h2d_bytes) *h2d_bytes = h2d;
     return QCF_OK;
   };
-  // compute: the requests one after another, each waiting only for the layers it reaches
+  // compute: the merged probes, then the requests one after another, each waiting only for
+  // the layers it reaches
+  for (MergedProbe& g : groups) {
+    qcf_status s = run_merged_probe(m, reqs, P, g, cs, ev_anchor);
+    if (s != QCF_OK) return s;
+  }
   for (int i = 0; i < n_req; ++i) {
     P[i].wait_stride = kPinnedWaitStride;
     qcf_status s = request_compute(m, &reqs[i], &outs[i], P[i], cs, ev_anchor, ev_crit_of(i), ev_layer_of(i),
-                                   i == 0 ? std::function<qcf_status()>(enqueue_layers) : std::function<qcf_status()>());
+                                   i == 0 ? std::function<qcf_status()>(enqueue_layers) : std::function<qcf_status()>(),
+                                   probe_done[i] != 0);
     if (s != QCF_OK) return s;
   }
   return QCF_OK;

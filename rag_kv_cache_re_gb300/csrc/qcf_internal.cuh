@@ -149,7 +149,7 @@ size_t attn_workspace_size(int n, int T, int Hq, int Hkv, int D);
 qcf_status attn_launch(const __nv_bfloat16* q, const int32_t* pos, int n, const __nv_bfloat16* K,
                        const __nv_bfloat16* V, int T, int Hq, int Hkv, int D, float scale, __nv_bfloat16* o,
                        float* lse, void* ws, size_t ws_bytes, cudaStream_t st, KernelClass kc = KC_ATTN,
-                       bool pdl = false);
+                       bool pdl = false, const int32_t* key0 = nullptr);   // key0: per row block key base (D = 128)
 
 // ------------------------------------------------------------------ device side
 
