@@ -223,3 +223,32 @@ def test_full_prefill_5184_tokens_8b_layer_shape():
     top2 = np.sort(ref["logits"])[-2:]
     if top2[1] - top2[0] > 2 * error_stats(logits.cpu().numpy(), ref["logits"])[0]:
         assert int(tok.item()) == ref["token"]
+
+
+def test_llama8b_batch_with_merged_probe_equals_requests_alone(llama8b):
+    # two 8B requests sharing their chunks at different offsets: the batch runs both probes
+    # as one (128 query rows, each request's keys in its own probe-cache segment) and must
+    # give every output bitwise as each request alone
+    from rag_kv_cache_re_gb300 import qcf as Q
+    w = llama8b
+    M, req, ids = w["M"], w["req"], w["ids"]
+    orders = [ids, ids[3:] + ids[:3]]
+    queries = [w["query"], qd.query_tokens(1, req.query_len, w["spec"].vocab)]
+    cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
+    alone = []
+    for order, query in zip(orders, queries):
+        fr = M.FusedRequest(w["dm"], w["store"], order, query, req.ratio_bp)
+        fr.run(cs, xs)
+        torch.cuda.synchronize()
+        alone.append(fr)
+    batch = [M.FusedRequest(w["dm"], w["store"], order, query, req.ratio_bp) for order, query in zip(orders, queries)]
+    M.run_batch(batch, cs, xs)
+    torch.cuda.synchronize()
+    assert Q.qcf_query_status() == 0
+    for a, b in zip(alone, batch):
+        assert torch.equal(a.q_crit, b.q_crit)
+        assert torch.equal(a.scores, b.scores)
+        assert torch.equal(a.selected, b.selected)
+        assert torch.equal(a.logits, b.logits) and int(a.token_host.item()) == int(b.token_host.item())
+        for l in (0, req.crit_layer, w["spec"].n_layers - 1):
+            assert torch.equal(a.K[l], b.K[l]) and torch.equal(a.V[l], b.V[l]), f"layer {l}"
