@@ -436,9 +436,13 @@ qcf_status qcf_storage_status(int* err);
  * chunks the same arrays).  On copy_stream every distinct chunk's K and V of a layer
  * cross the host link once, into a shared staging area, and are written from there into
  * each request's fused cache with that request's own offset (keys re-rotated, values
- * copied); on compute_stream the requests then run one after another exactly as
- * qcf_request_prefill would, each waiting only for the layers it reaches.  Results equal
- * those of qcf_request_prefill per request.
+ * copied).  On compute_stream, consecutive requests with the same critical layer
+ * (critical-layer selector, head dim 128, at most 128 query rows together once each
+ * request's are rounded up to the attention row block) run their probe as one: each
+ * probe layer's weights stream once for the group, each request attending only to its
+ * own anchors and query rows; then every request runs its profile, selection and
+ * recompute as qcf_request_prefill would, waiting only for the layers it reaches.
+ * Results are bitwise those of qcf_request_prefill per request.
  *   reqs, outs   host arrays [n_req], 1 <= n_req <= 64, any selectors
  *   ws           device, qcf_batch_workspace_size(dims, reqs, n_req) bytes, caller-owned
  *   h2d_bytes    host, nullable: bytes this call sends host -> device
