@@ -1,6 +1,7 @@
 // Decoder layer forward for recomputed rows, full prefill, and the per-request
 // fused-prefill driver (probe -> profile -> top-N -> pipelined per-layer recompute).
 #include <errno.h>
+#include <fcntl.h>
 #include <unistd.h>
 
 #include <algorithm>
@@ -695,8 +696,9 @@ static int read_full(int fd, uint8_t* dst, size_t bytes, int64_t offset) {
   return 0;
 }
 
-// A small pool of reader threads: one layer's blocks (a chunk's keys or values each)
-// are read concurrently, so a storage device sees several requests in flight.
+// A pool of reader threads: one layer's blocks (a chunk's keys or values each, in pieces
+// of at most kReadPiece bytes) are read concurrently, so a storage device sees several
+// requests in flight and page-cache copies use several cores.
 class ReadPool {
  public:
   static ReadPool& get() {
@@ -713,9 +715,10 @@ class ReadPool {
   }
 
  private:
-  static constexpr int kThreads = 8;
   ReadPool() {
-    for (int i = 0; i < kThreads; ++i) threads_.emplace_back([this] { work(); });
+    const unsigned hw = std::thread::hardware_concurrency();
+    const int n = hw >= 16 ? 16 : (hw >= 8 ? static_cast<int>(hw) : 8);
+    for (int i = 0; i < n; ++i) threads_.emplace_back([this] { work(); });
   }
   ~ReadPool() {
     {
@@ -746,23 +749,40 @@ class ReadPool {
   std::vector<std::thread> threads_;
 };
 
+// Read pieces: page-cache reads are memory copies, split finely over the threads; direct
+// reads go to the device in larger requests (both multiples of the 4096-byte O_DIRECT
+// alignment).
+constexpr size_t kReadPiece = 256 << 10;
+constexpr size_t kReadPieceDirect = 1 << 20;
+static size_t read_piece(int fd) {
+  const int fl = fcntl(fd, F_GETFL);
+  return fl != -1 && (fl & O_DIRECT) ? kReadPieceDirect : kReadPiece;
+}
+
 static void CUDART_CB storage_read_fn(void* arg) {
   StorageRead* rd = static_cast<StorageRead*>(arg);
   StorageCtx* c = rd->ctx;
   if (c->err == 0 && (rd->keys || rd->values)) {
     std::vector<std::function<void()>> tasks;
-    std::vector<int> errs(2 * c->files.size(), 0);
-    size_t row0 = 0;
+    size_t n_pieces = 0;
+    for (size_t i = 0; i < c->files.size(); ++i)
+      n_pieces += 2 * ((static_cast<size_t>(c->len[i]) * c->row_bytes + kReadPiece - 1) / kReadPiece);
+    std::vector<int> errs(n_pieces, 0);
+    size_t row0 = 0, piece = 0;
+    auto add = [&](int fd, uint8_t* dst, size_t bytes, int64_t off) {
+      const size_t step = read_piece(fd);
+      for (size_t done = 0; done < bytes; done += step) {
+        const size_t n = bytes - done < step ? bytes - done : step;
+        int* err = &errs[piece++];
+        tasks.emplace_back([=] { *err = read_full(fd, dst + done, n, off + static_cast<int64_t>(done)); });
+      }
+    };
     for (size_t i = 0; i < c->files.size(); ++i) {
       const qcf_chunk_file f = c->files[i];
       const size_t bytes = static_cast<size_t>(c->len[i]) * c->row_bytes;
       const int64_t layer_off = static_cast<int64_t>(rd->layer) * f.layer_stride;
-      uint8_t* kdst = c->buf[rd->buf] + row0 * c->row_bytes;
-      uint8_t* vdst = c->buf[rd->buf] + (c->C + row0) * c->row_bytes;
-      int* ek = &errs[2 * i];
-      int* ev = &errs[2 * i + 1];
-      if (rd->keys) tasks.emplace_back([=] { *ek = read_full(f.fd, kdst, bytes, f.k_offset + layer_off); });
-      if (rd->values) tasks.emplace_back([=] { *ev = read_full(f.fd, vdst, bytes, f.v_offset + layer_off); });
+      if (rd->keys) add(f.fd, c->buf[rd->buf] + row0 * c->row_bytes, bytes, f.k_offset + layer_off);
+      if (rd->values) add(f.fd, c->buf[rd->buf] + (c->C + row0) * c->row_bytes, bytes, f.v_offset + layer_off);
       row0 += static_cast<size_t>(c->len[i]);
     }
     ReadPool::get().run(tasks);
