@@ -255,22 +255,40 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 // logits = W_lm * RMSNorm(x_last) * g (fp32 h kept in shared memory); argmax as the
 // largest (orderable value, inverted index) key, so ties keep the lowest index: each
 // CTA writes its best key to its own slot (nothing to clear first), and
-// argmax_finalize_kernel takes the largest slot.
-__global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ x_last, int d, int vocab,
-                                                      const __nv_bfloat16* __restrict__ g, float eps,
-                                                      const __nv_bfloat16* __restrict__ W,
-                                                      float* __restrict__ logits,
-                                                      unsigned long long* __restrict__ best) {
-  pdl_wait();  // x_last comes from the kernel before
-  pdl_launch_dependents();
+// argmax_finalize_kernel takes the largest slot.  One warp per vocabulary row, eight
+// 16-byte weight loads per lane in flight: the first batch of a warp's first row is
+// requested before the dependency wait (the weights are constant), the next row's
+// while the current one is reduced.
+constexpr int kLmLoads = 8;
+__global__ void __launch_bounds__(256, 4) lm_head_kernel(const float* __restrict__ x_last, int d, int vocab,
+                                                         const __nv_bfloat16* __restrict__ g, float eps,
+                                                         const __nv_bfloat16* __restrict__ W,
+                                                         float* __restrict__ logits,
+                                                         unsigned long long* __restrict__ best) {
   extern __shared__ float hs[];
   __shared__ float red[8];
   __shared__ unsigned long long bred[8];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int n8 = d / 8;                    // 16-byte pieces of a row
+  const int iters = (n8 + 32 * kLmLoads - 1) / (32 * kLmLoads);
+  uint4 wv[kLmLoads];
+  auto issue = [&](int row, int it) {      // pieces lane + 32 (it * kLmLoads + u) of `row`
+    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(row) * d);
+#pragma unroll
+    for (int u = 0; u < kLmLoads; ++u) {
+      const int i = lane + 32 * (it * kLmLoads + u);
+      if (i < n8) wv[u] = __ldcs(wr + i);
+    }
+  };
+  const int nwarps = gridDim.x * 8;
+  int v = blockIdx.x * 8 + wid;
+  if (v < vocab) issue(v, 0);
+  pdl_wait();  // x_last comes from the kernel before
+  pdl_launch_dependents();
   float ss = 0.f;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = x_last[i];
-    ss += v * v;
+    const float xv = x_last[i];
+    ss += xv * xv;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -282,20 +300,14 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
   for (int i = threadIdx.x; i < d; i += blockDim.x) hs[i] = x_last[i] * inv * __bfloat162float(g[i]);
   __syncthreads();
   unsigned long long mine = 0ull;
-  const int nwarps = gridDim.x * 8;
-  for (int v = blockIdx.x * 8 + wid; v < vocab; v += nwarps) {
-    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(v) * d);
+  for (; v < vocab; v += nwarps) {
     float acc = 0.f;
-    // four independent 16-byte weight loads per lane in flight before their FMAs
-    const int n8 = d / 8;
-    for (int i0 = lane; i0 < n8; i0 += 128) {
-      uint4 wv[4];
+    // each lane sums its pieces in increasing order
+    for (int it = 0; it < iters; ++it) {
+      if (it > 0) issue(v, it);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (i0 + 32 * u < n8) wv[u] = __ldcs(wr + i0 + 32 * u);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + 32 * u;
+      for (int u = 0; u < kLmLoads; ++u) {
+        const int i = lane + 32 * (it * kLmLoads + u);
         if (i < n8) {
           float f[8];
           bf16x8_to_f32(wv[u], f);
@@ -306,6 +318,7 @@ __global__ void __launch_bounds__(256) lm_head_kernel(const float* __restrict__ 
         }
       }
     }
+    if (v + nwarps < vocab) issue(v + nwarps, 0);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
