@@ -38,8 +38,9 @@ struct GemmCfg {
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int STAGES = BN >= 224 ? 4 : (BN == 128 ? 6 : 8);
+  // two accumulator buffers; the allocation is a power of two (BN = 224 uses 448 of 512)
+  static constexpr int TMEM_COLS = BN == 224 ? 512 : 2 * BN;
   static_assert(kBM * BN * 4 <= STAGES * STAGE_BYTES, "a residual tile must fit the stages");
   static constexpr int EPI_BYTES = 4 * 32 * 33 * 4;   // one 32x32 fp32 transpose tile per epilogue warp
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
@@ -213,6 +214,8 @@ __device__ __forceinline__ void tile_epilogue(const Loader& ld, const EpiParams&
       return reinterpret_cast<float4*>(out + static_cast<size_t>(row0 + i * 4 + rr) * ep.ldo + n0 + c * 32 + cq);
     };
     auto row_ok = [&](int i) { return row0 + i * 4 + rr < M; };
+    // chunks of this tile inside the row (all of them but in a ragged last column tile)
+    const int nch = min(BN / 32, (ep.ldo - n0) / 32);
     float4 xa[8], xb[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -235,17 +238,19 @@ __device__ __forceinline__ void tile_epilogue(const Loader& ld, const EpiParams&
       __syncwarp();
     };
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; c += 2) {   // BN / 32 is even
+    for (int c = 0; c < nch; c += 2) {
+      if (c + 1 < nch) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (row_ok(i)) xb[i] = *xptr(c + 1, i);
+        for (int i = 0; i < 8; ++i)
+          if (row_ok(i)) xb[i] = *xptr(c + 1, i);
+      }
       add_store(c, xa);
-      if (c + 2 < BN / 32) {
+      if (c + 2 < nch) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (row_ok(i)) xa[i] = *xptr(c + 2, i);
       }
-      add_store(c + 1, xb);
+      if (c + 1 < nch) add_store(c + 1, xb);
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ep.out);
@@ -373,16 +378,17 @@ template <int BN>
 __device__ __forceinline__ void add_tile_staged(uint32_t taddr, const CUtensorMap* tmX, uint8_t* region,
                                                 const float* first, const float* rest, size_t step, int parts,
                                                 int own, uint64_t* bar, uint32_t phase, int row0, int n0,
-                                                unsigned int* status) {
+                                                unsigned int* status, int nbox) {
   constexpr int kBox = 32 * 32 * 4;            // one x box
   constexpr int kPart = BN * 32 * 4;           // a warp's rows of one partial
   const int lane = threadIdx.x & 31;
   float* xs = reinterpret_cast<float*>(region);
   const float* ps = reinterpret_cast<const float*>(region + (BN / 32) * kBox);
+  // nbox: the x boxes inside the row (fewer than BN / 32 only in a ragged last column tile)
   if (lane == 0) {
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>((BN / 32) * kBox + (parts - 1) * kPart));
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox * kBox + (parts - 1) * kPart));
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) tma_load_2d(xs + c * 1024, tmX, bar, n0 + c * 32, row0);
+    for (int c = 0; c < nbox; ++c) tma_load_2d(xs + c * 1024, tmX, bar, n0 + c * 32, row0);
   }
   __syncwarp();
   if (parts > 1 && lane < parts && lane != own) {
@@ -395,7 +401,7 @@ __device__ __forceinline__ void add_tile_staged(uint32_t taddr, const CUtensorMa
     return;
   }
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < nbox; ++c) {
     float v[32];
     if (parts == 1) {
       tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v);
@@ -440,7 +446,7 @@ __device__ __forceinline__ void add_tile_staged(uint32_t taddr, const CUtensorMa
   __syncwarp();
   if (lane == 0) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) tma_store_2d(tmX, xs + c * 1024, n0 + c * 32, row0);
+    for (int c = 0; c < nbox; ++c) tma_store_2d(tmX, xs + c * 1024, n0 + c * 32, row0);
     bulk_commit_group();
     bulk_wait_group0();
   }
@@ -583,7 +589,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_m = (M + kBM - 1) / kBM;
-  const int tiles_n = N / BN;
+  const int tiles_n = (N + BN - 1) / BN;  // BN = 224: the last column tile is ragged
   const int kb_total = K / kBK;
   UnitWalk walk;
   walk.init(tiles_m, tiles_n, kb_total, splits, groups);
@@ -732,8 +738,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (M <= 2048 && !peek.next(nx) && r < M) {
           const char* xr = reinterpret_cast<const char*>(static_cast<const float*>(ep.out) + static_cast<size_t>(r) * ep.ldo +
                                                          static_cast<size_t>(nt) * BN);
+          const int row_bytes = min(BN, N - nt * BN) * 4;
 #pragma unroll 1
-          for (int b = 0; b < BN * 4; b += 128) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xr + b));
+          for (int b = 0; b < row_bytes; b += 128) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xr + b));
         }
       }
       const bool got = mbar_wait(&tfull[acc], (local >> 1) & 1);
@@ -761,7 +768,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (staged) {
         if (warp_live)
           add_tile_staged<BN>(taddr, &tmX, smem + static_cast<size_t>(quarter) * BN * 32 * 4, nullptr, nullptr, 0, 1, 0,
-                              &xbar[quarter], 0, row - lane, n0, status);
+                              &xbar[quarter], 0, row - lane, n0, status, min(BN, N - n0) / 32);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -851,14 +858,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if constexpr (EPI == EPI_ADD_F32) {
               if (passes == 1) {
                 add_tile_staged<BN>(taddr, &tmX, reinterpret_cast<uint8_t*>(sp), pfirst, prest, w.step * kSlot, w.parts,
-                                    own, &xbar[quarter], 0, row - lane, n0, status);
+                                    own, &xbar[quarter], 0, row - lane, n0, status, min(BN, N - n0) / 32);
               } else if constexpr (BN == 256) {
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h)
                   add_tile_staged<BN / 2>(taddr + static_cast<uint32_t>(h * BN / 2), &tmX, reinterpret_cast<uint8_t*>(sp),
                                           pfirst + h * (BN / 2) * 32, prest + h * (BN / 2) * 32, w.step * kSlot,
                                           w.parts, own, &xbar[quarter], static_cast<uint32_t>(h), row - lane,
-                                          n0 + h * (BN / 2), status);
+                                          n0 + h * (BN / 2), status, min(BN / 2, N - n0 - h * (BN / 2)) / 32);
               }
             } else {
               if (passes == 1) {
@@ -923,7 +930,7 @@ constexpr int kSkGainPerPart = 13;
 //    through the TMA ring are ~29 / 55 / 65 GB/s for BN = 64 / 128 / 256, under an
 //    aggregate of ~6.5 TB/s from HBM; a k split adds the last arriver's fixup, about
 //    0.6 us per 32-column chunk and pair of partials, plus 1 us.
-static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
+static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim, bool w_kn = false) {
   const int sms = num_sms();
   const int tiles_m = (M + kBM - 1) / kBM;
   const int kb = K / kBK;
@@ -950,6 +957,13 @@ static GemmPlan plan_gemm(int M, int N, int K, EpiKind epi, int head_dim) {
       const long long parts = std::min<long long>(groups, (kb + per - 1) / per + 1);  // per shared tile, at most
       if (lockstep - per > kSkMinGain + kSkGainPerPart * std::max<long long>(0, parts - 2))
         return GemmPlan{bn, 1, tiles, groups};
+    }
+    // A residual add whose 256-wide tiles fill one lockstep round on part of the SMs
+    // (the 832-row O projection: 112 tiles on 152 SMs) runs 224-wide tiles instead: more
+    // CTAs, each with 7/8 of the work, the last column tile ragged.
+    if (epi == EPI_ADD_F32 && !w_kn && bn == 256 && tiles <= sms) {
+      const int tiles224 = tiles_m * ((N + 223) / 224);
+      if (tiles224 > tiles && tiles224 <= sms) return GemmPlan{224, 1, tiles224, 0};
     }
     return GemmPlan{bn, 1, tiles, 0};
   }
@@ -1075,7 +1089,7 @@ qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const 
   if (M <= 0) return QCF_OK;
   if (K % kBK || N % 64 || K <= 0 || N <= 0) return set_error(QCF_ERR_SHAPE, "gemm: K=%d N=%d (K%%64, N%%64 required)", K, N);
   const int hd = epi == EPI_QKV_ROPE ? ep.D : 16;
-  GemmPlan p = plan_gemm(M, N, K, epi, hd);
+  GemmPlan p = plan_gemm(M, N, K, epi, hd, w_kn);
   float* part = nullptr;
   unsigned int* cnt = nullptr;
   if (p.splits > 1 || p.groups > 0) {
@@ -1110,6 +1124,9 @@ qcf_status gemm_launch(EpiKind epi, const __nv_bfloat16* A, int M, int K, const 
     }
   }
   switch (p.BN) {
+    case 224:  // residual add only (plan_gemm)
+      if (epi != EPI_ADD_F32) return set_error(QCF_ERR_UNSUPPORTED, "gemm: BN 224 serves the residual add only");
+      return launch_cfg<224, EPI_ADD_F32, 0, false>(ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
     case 256: return dispatch_epi<256>(epi, hd, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
     case 128: return dispatch_epi<128>(epi, hd, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
     default: return dispatch_epi<64>(epi, hd, ta, tb, tx, M, N, K, p.splits, p.groups, ep, part, cnt, st, grid, pdl);
