@@ -274,7 +274,10 @@ def test_sparse_causal_attn_writes_only_its_rows(Q, T, n, Hq, Hkv, D):
                                    (832, 6144, 4096), (832, 28672, 4096), (832, 4096, 4096), (832, 4096, 14336),
                                    (1664, 4096, 14336), (64, 6144, 4096), (64, 4096, 14336),
                                    # tiles ending inside a warp's 32 rows (staged copies and stores past M)
-                                   (837, 4096, 14336), (837, 6144, 4096), (100, 4096, 14336)])
+                                   (837, 4096, 14336), (837, 6144, 4096), (100, 4096, 14336),
+                                   # residual adds on 224-wide tiles with a ragged last column tile of 64
+                                   # or 32 columns (and a row tail): no column past N may be written
+                                   (256, 512, 128), (300, 256, 64), (837, 4096, 4096)])
 def test_linear_store_and_add(Q, M, N, K):
     A = qd.normal_bf16((M, K), 1.0, 31, DEV)
     W = qd.normal_bf16((N, K), 0.02, 32, DEV)
